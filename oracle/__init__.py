@@ -1,0 +1,145 @@
+"""CPU oracle for the GIE zonal scatter.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  It shares no code with the CUDA path, and the
+product never calls it.
+
+Two independent formulations of the same definitions (deepmd-kit pull request
+"fused Triton zonal scatter for the GIE head", section "What"):
+
+* variant A (``zs_oracle.c``, fp64, sequential): stable CSR by counting sort,
+  forward as a per-node walk of that CSR in order, backward as direct loops;
+  every value comes with the sum of |terms| that formed it.
+* variant B (``composition.py``, torch CPU fp64): the reference composition the
+  page replaces -- broadcast the coupling over each degree's radial rows into
+  a materialised (E, 15, C) message, then ``index_add_`` it onto the
+  destinations; its backward is the same composition's adjoint.
+
+Pins against things other than the oracle itself live in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "zs_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle_zs.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no GPU code involved)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.oracle_build_csr.restype = ctypes.c_int64
+            lib.oracle_build_csr.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P]
+            lib.oracle_forward.restype = None
+            lib.oracle_forward.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                           P, ctypes.c_int64, P, P]
+            lib.oracle_backward.restype = None
+            lib.oracle_backward.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int32,
+                                            ctypes.c_int32, P, ctypes.c_int64, P, P, P, P]
+            lib.oracle_slot_of_row.restype = ctypes.c_int
+            lib.oracle_slot_of_row.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def build_csr(dst: np.ndarray, N: int):
+    """Stable destination CSR: (row_ptr int32 (N+1,), perm int32 (E,), bad count)."""
+    dst = _c(dst, np.int32)
+    E = dst.shape[0]
+    row_ptr = np.zeros(N + 1, np.int32)
+    perm = np.zeros(E, np.int32)
+    bad = _load().oracle_build_csr(_ptr(dst), E, N, _ptr(row_ptr), _ptr(perm))
+    return row_ptr, perm, int(bad)
+
+
+def forward(coup, rad, row_ptr, perm, N: int, nodes=None):
+    """Forward in fp64: (out, absum), each (n_out, 16, C)."""
+    coup = _c(coup, np.float32)
+    rad = _c(rad, np.float32)
+    C = rad.shape[2] if rad.ndim == 3 else 0
+    row_ptr = _c(row_ptr, np.int32)
+    perm = _c(perm, np.int32)
+    nodes_a = None if nodes is None else _c(nodes, np.int32)
+    n_out = N if nodes_a is None else nodes_a.shape[0]
+    out = np.zeros((n_out, 16, C), np.float64)
+    absum = np.zeros((n_out, 16, C), np.float64)
+    if n_out and C:
+        _load().oracle_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), N, C,
+                               _ptr(nodes_a), 0 if nodes_a is None else n_out,
+                               _ptr(out), _ptr(absum))
+    return out, absum
+
+
+def backward(g, coup, rad, dst, N: int, edges=None):
+    """Backward in fp64: (d_coup (n,15), d_rad (n,3,C), abs_dcoup, abs_drad)."""
+    g = _c(g, np.float32)
+    coup = _c(coup, np.float32)
+    rad = _c(rad, np.float32)
+    dst = _c(dst, np.int32)
+    E = dst.shape[0]
+    C = rad.shape[2]
+    edges_a = None if edges is None else _c(edges, np.int64)
+    n_out = E if edges_a is None else edges_a.shape[0]
+    d_coup = np.zeros((n_out, 15), np.float64)
+    d_rad = np.zeros((n_out, 3, C), np.float64)
+    a_dc = np.zeros((n_out, 15), np.float64)
+    a_dr = np.zeros((n_out, 3, C), np.float64)
+    if n_out and C:
+        _load().oracle_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C,
+                                _ptr(edges_a), 0 if edges_a is None else n_out,
+                                _ptr(d_coup), _ptr(d_rad), _ptr(a_dc), _ptr(a_dr))
+    return d_coup, d_rad, a_dc, a_dr
+
+
+def slot_of_row(r: int) -> int:
+    return int(_load().oracle_slot_of_row(r))
+
+
+def normalised_error(got, ref, absum):
+    """max |got - ref| / absum, with absum == 0 requiring got == 0 exactly.
+
+    Returns (max normalised error, count of nonzero values where absum == 0).
+    NaN in got where ref is finite counts as an infinite error.
+    """
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    absum = np.asarray(absum, np.float64)
+    zero = absum == 0
+    bad_zero = int(np.count_nonzero(got[zero] != 0))
+    nz = ~zero
+    if not np.any(nz):
+        return 0.0, bad_zero
+    err = np.abs(got[nz] - ref[nz]) / absum[nz]
+    err = np.where(np.isnan(err), np.inf, err)
+    return float(err.max()), bad_zero

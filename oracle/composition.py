@@ -1,0 +1,73 @@
+"""Variant B of the oracle: the reference composition.  TEST INFRASTRUCTURE ONLY.
+
+The deepmd-kit pull request "fused Triton zonal scatter for the GIE head",
+section "What", describes the eager composition that the fused operator
+replaces: broadcast each edge's zonal coupling over its degree's radial rows
+(materialising the (E, 15, C) message) and ``index_add_`` it onto the
+destination nodes.  This module writes that composition in torch CPU fp64, and
+its adjoint (the gradients the composition's autograd would give), so that it
+shares no code or loop structure with the C oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# zonal row -> radial slot for the lmax = 3 ladder, degree groups of 3/5/7 rows
+# (section "Boundary and layout contract": "row groups 3/5/7")
+ROW_GROUPS = (3, 5, 7)
+
+
+def slot_index() -> torch.Tensor:
+    return torch.repeat_interleave(torch.arange(len(ROW_GROUPS)), torch.tensor(ROW_GROUPS))
+
+
+def _valid(dst: torch.Tensor, N: int) -> torch.Tensor:
+    return (dst >= 0) & (dst < N)
+
+
+def message(coup, rad) -> torch.Tensor:
+    """(E, 15, C) fp64 message: coupling broadcast over its degree's radial row."""
+    coup = torch.as_tensor(np.asarray(coup)).to(torch.float64)
+    rad = torch.as_tensor(np.asarray(rad)).to(torch.float64)
+    return coup[:, :, None] * rad[:, slot_index(), :]
+
+
+def forward(coup, rad, dst, N: int, chunk: int = 1 << 16) -> np.ndarray:
+    """(N, 16, C) fp64: scalar row zero, rows 1..15 = index_add of the message."""
+    coup_t = torch.as_tensor(np.asarray(coup))
+    rad_t = torch.as_tensor(np.asarray(rad))
+    dst_t = torch.as_tensor(np.asarray(dst)).to(torch.int64)
+    E = dst_t.shape[0]
+    C = rad_t.shape[2]
+    out = torch.zeros((N, 16, C), dtype=torch.float64)
+    body = out[:, 1:, :]
+    for a in range(0, E, chunk):
+        b = min(E, a + chunk)
+        d = dst_t[a:b]
+        keep = _valid(d, N)
+        msg = message(coup_t[a:b][keep].numpy(), rad_t[a:b][keep].numpy())
+        body.index_add_(0, d[keep], msg)
+    return out.numpy()
+
+
+def backward(g, coup, rad, dst, N: int):
+    """Adjoint of the composition: (d_coup (E,15), d_rad (E,3,C)) in fp64.
+
+    d_msg = g[dst, 1:, :]; d_coup = sum_c d_msg * rad[:, slot(r)];
+    d_rad[:, s] = sum over rows r of slot s of d_msg[:, r] * coup[:, r].
+    """
+    g_t = torch.as_tensor(np.asarray(g)).to(torch.float64)
+    coup_t = torch.as_tensor(np.asarray(coup)).to(torch.float64)
+    rad_t = torch.as_tensor(np.asarray(rad)).to(torch.float64)
+    dst_t = torch.as_tensor(np.asarray(dst)).to(torch.int64)
+    E = dst_t.shape[0]
+    C = rad_t.shape[2]
+    keep = _valid(dst_t, N)
+    d_msg = torch.zeros((E, 15, C), dtype=torch.float64)
+    d_msg[keep] = g_t[dst_t[keep], 1:, :]
+    idx = slot_index()
+    d_coup = (d_msg * rad_t[:, idx, :]).sum(dim=2)
+    d_rad = torch.zeros((E, 3, C), dtype=torch.float64)
+    d_rad.index_add_(1, idx, d_msg * coup_t[:, :, None])
+    return d_coup.numpy(), d_rad.numpy()
