@@ -1,0 +1,416 @@
+"""Benchmark of the zonal-scatter hot path on GB300.
+
+One step = stable destination CSR build + forward + backward (every step of
+the path) over one synthetic graph shaped like the 4096-atom diamond frame
+of the deepmd-kit pull request "fused Triton zonal scatter for the GIE head"
+(section "Numbers": N=4096, E=647170, C=32, fp32).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config n4096]
+                    [--impl zs|reference] [--no-cpu-baseline] [--no-e2e]
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead (the only other place this file runs it).
+Under torchrun every rank runs an independent replica (the path needs no
+exchange between GPUs); ``value`` is the total over ranks divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "zonal-scatter fwd+bwd edges/s at N=4096,E=647170,C=32; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {
+    "fwd": "equivariant_interatomic_potential_gb300/csrc/zs_forward.cu",
+    "bwd": "equivariant_interatomic_potential_gb300/csrc/zs_backward.cu",
+    "csr": "equivariant_interatomic_potential_gb300/csrc/zs_csr.cu",
+}
+
+
+# ---------------------------------------------------------------- byte models
+
+def algorithmic_bytes(N: int, E: int, C: int) -> dict:
+    """Bytes each step must move at least (fp32 data, int32 indices)."""
+    fwd = E * (4 + 60 + 12 * C) + 4 * (N + 1) + 64 * N * C
+    bwd = E * (4 + 60 + 12 * C + 60 + 12 * C) + 64 * N * C
+    csr = E * (4 + 4) + 4 * (N + 1)
+    return {"fwd": fwd, "bwd": bwd, "csr": csr}
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "copy_gbs"):
+            if key in d:
+                return float(d[key]), "measured"
+        for v in d.values():
+            if isinstance(v, dict) and "hbm_gbs" in v:
+                return float(v["hbm_gbs"]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload][kernel_key]
+        if e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel_key]):
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"zs_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu_arm(args, rank: int, world: int) -> dict | None:
+    import torch
+    import torch.distributed as dist
+
+    from equivariant_interatomic_potential_gb300 import workloads, zs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = workloads.make_workload(args.config)
+    N, E, C = w.N, w.E, w.C
+    dev = torch.device("cuda", local)
+    lib = zs.load()
+
+    dst = torch.from_numpy(w.dst).to(dev)
+    coup = torch.from_numpy(w.coup).to(dev)
+    rad = torch.from_numpy(w.rad).to(dev)
+    g = torch.from_numpy(w.grad_out).to(dev)
+    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(E, dtype=torch.int32, device=dev)
+    bad = torch.empty(1, dtype=torch.int32, device=dev)
+    ws_csr = torch.empty(max(1, zs.zs_build_csr_workspace_bytes(E, N)), dtype=torch.uint8, device=dev)
+    ws_fwd = torch.empty(max(1, zs.zs_forward_workspace_bytes(E, N, C)), dtype=torch.uint8, device=dev)
+    out = torch.empty((N, 16, C), dtype=torch.float32, device=dev)
+    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev)
+    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    P = lambda t: t.data_ptr()  # noqa: E731
+    csr_ws_bytes, fwd_ws_bytes = ws_csr.numel(), ws_fwd.numel()
+
+    def csr():
+        st = lib.zs_build_csr(P(dst), E, N, P(row_ptr), P(perm), P(bad), P(ws_csr), csr_ws_bytes, sp)
+        assert st == 0, lib.zs_last_error()
+
+    def fwd():
+        st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, 3, P(out), P(ws_fwd), fwd_ws_bytes, sp)
+        assert st == 0, lib.zs_last_error()
+
+    def bwd():
+        st = lib.zs_backward(P(g), P(coup), P(rad), P(dst), E, N, C, 3, P(d_coup), P(d_rad), sp)
+        assert st == 0, lib.zs_last_error()
+
+    passes = max(1, (max(N, 1).bit_length() + 7) // 8) if E > 0 else 0
+    launches_per_step = (3 * passes + 1) + 2 + (1 if E > 0 else 0)
+
+    for _ in range(args.warmup):
+        csr(); fwd(); bwd()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for k in ("csr", "fwd", "bwd")}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            for k, fn in (("csr", csr), ("fwd", fwd), ("bwd", bwd)):
+                ev[k][i][0].record(stream)
+                fn()
+                ev[k][i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    per = {k: [a.elapsed_time(b) * 1e3 for a, b in ev[k]] for k in ev}   # microseconds
+    clock = clocks.summary()
+
+    # end to end through the public API: pinned host buffers in, results out
+    e2e = None
+    if not args.no_e2e:
+        h_dst = torch.from_numpy(w.dst).pin_memory()
+        h_coup = torch.from_numpy(w.coup).pin_memory()
+        h_rad = torch.from_numpy(w.rad).pin_memory()
+        h_g = torch.from_numpy(w.grad_out).pin_memory()
+        h_out = torch.empty_like(out, device="cpu").pin_memory()
+        h_dc = torch.empty_like(d_coup, device="cpu").pin_memory()
+        h_dr = torch.empty_like(d_rad, device="cpu").pin_memory()
+
+        def e2e_step():
+            dst.copy_(h_dst, non_blocking=True)
+            coup.copy_(h_coup, non_blocking=True)
+            rad.copy_(h_rad, non_blocking=True)
+            g.copy_(h_g, non_blocking=True)
+            zs.zs_build_csr(dst, N, row_ptr=row_ptr, perm=perm, bad_dst_count=bad, workspace=ws_csr)
+            zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
+            zs.zs_backward(g, coup, rad, dst, N, d_coup=d_coup, d_rad=d_rad)
+            h_out.copy_(out, non_blocking=True)
+            h_dc.copy_(d_coup, non_blocking=True)
+            h_dr.copy_(d_rad, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        h2d = sum(t.numel() * t.element_size() for t in (h_dst, h_coup, h_rad, h_g))
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dc, h_dr))
+        e2e = {"value": world * E * args.steps / (e2e_ms / 1e3), "unit": "edges/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if rank != 0:
+        return None
+
+    ab = algorithmic_bytes(N, E, C)
+    peak, peak_kind = measured_peaks()
+    kernels = {}
+    for k in ("csr", "fwd", "bwd"):
+        us = statistics.mean(per[k])
+        gbs = ab[k] / (us * 1e-6) / 1e9
+        kernels[k] = {"us_mean": us, "us_median": statistics.median(per[k]), "algorithmic_bytes": ab[k],
+                      "GBs": gbs, "frac_of_" + peak_kind: gbs / peak,
+                      "edges_per_s": E / (us * 1e-6)}
+    dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_mean"])
+    roof = {"kernel": {"fwd": "zs_forward", "bwd": "zs_backward"}[dom], "bound": "hbm",
+            "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
+            "frac": kernels[dom]["GBs"] / peak, "peak_kind": peak_kind,
+            "traffic": ncu_traffic(dom, args.config),
+            "algorithmic_bytes_per_launch": ab[dom]}
+    ms_per_step = total_ms / args.steps
+    fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
+    res = {
+        "metric": METRIC,
+        "value": world * E * args.steps / (total_ms / 1e3),
+        "unit": "edges/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: N={N}, E={E}, C={C}, lmax=3 (rows 3/5/7), fp32, seed {w.seed}",
+                   "step": "csr_build + forward + backward",
+                   "l2": "inputs larger than L2 (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "fwd_bwd_edges_per_s": E / (fwd_bwd_us * 1e-6),
+        "kernels": kernels,
+        "roofline": roof,
+        "clocks": clock,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    return res
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def run_oracle(config: str, min_seconds: float) -> dict:
+    """The fp64 oracle (single-threaded C) on the full graph, repeated until
+    min_seconds of CPU work has been timed."""
+    import oracle
+    from equivariant_interatomic_potential_gb300 import workloads
+
+    w = workloads.make_workload(config)
+    oracle.build()
+    reps, t_csr, t_fwd, t_bwd = 0, 0.0, 0.0, 0.0
+    while reps == 0 or (t_csr + t_fwd + t_bwd) < min_seconds:
+        a = time.perf_counter()
+        row_ptr, perm, _ = oracle.build_csr(w.dst, w.N)
+        b = time.perf_counter()
+        oracle.forward(w.coup, w.rad, row_ptr, perm, w.N)
+        c = time.perf_counter()
+        oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
+        d = time.perf_counter()
+        t_csr += b - a
+        t_fwd += c - b
+        t_bwd += d - c
+        reps += 1
+    tot = t_csr + t_fwd + t_bwd
+    return {"value": w.E * reps / tot, "unit": "edges/s", "cores": 1, "kind": "oracle",
+            "sample": f"full {config} graph (N={w.N}, E={w.E}, C={w.C}), csr+forward+backward, "
+                      f"{reps} repetition(s), {tot:.1f} s, fp64 sequential C",
+            "ms_per_step": tot / reps * 1e3,
+            "fwd_bwd_edges_per_s": w.E * reps / (t_fwd + t_bwd)}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--config", default="n4096")
+    ap.add_argument("--impl", default="zs", choices=["zs", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle on the host cores, rank 0 only
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        steps = []
+        base = None
+        for i in range(args.warmup + args.steps):
+            r = run_oracle(args.config, 0.0)
+            if i >= args.warmup:
+                steps.append(r["ms_per_step"])
+            base = r
+        E = {"tiny": 2048, "n1000": 158002, "n4096": 647170, "zipf": 647170, "large": 5177344}[args.config]
+        ms = statistics.mean(steps)
+        val = E / (ms / 1e3)
+        res = {"impl": "reference", "metric": METRIC, "value": val, "unit": "edges/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+               "config": {"workload": f"{args.config}", "step": "csr_build + forward + backward"},
+               "cpu_baseline": {"value": val, "unit": "edges/s", "cores": 1, "kind": "oracle",
+                                "sample": base["sample"].split(",")[0] + ", one repetition per step"},
+               "e2e": {"value": val, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+               "wall_s": time.perf_counter() - t0}
+        print(json.dumps(res))
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    try:
+        res = run_gpu_arm(args, rank, world)
+        if rank == 0 and res is not None:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = run_oracle(args.config, args.cpu_seconds)
+            print(json.dumps(res))
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+    del torch
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,48 @@
+// Status strings and the per-thread error message of libzs.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "zs_common.cuh"
+
+namespace {
+thread_local char g_last_error[512] = {0};
+}
+
+namespace zs {
+
+zs_status fail(zs_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+zs_status check_launch(const char* what) {
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        return fail(ZS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(err), cudaGetErrorName(err));
+    }
+    return ZS_OK;
+}
+
+}  // namespace zs
+
+extern "C" {
+
+const char* zs_status_string(int status) {
+    switch (status) {
+        case ZS_OK: return "ZS_OK";
+        case ZS_ERR_INVALID_ARG: return "ZS_ERR_INVALID_ARG";
+        case ZS_ERR_UNSUPPORTED: return "ZS_ERR_UNSUPPORTED";
+        case ZS_ERR_CUDA: return "ZS_ERR_CUDA";
+        case ZS_ERR_TIMEOUT: return "ZS_ERR_TIMEOUT";
+        default: return "ZS_ERR_UNKNOWN";
+    }
+}
+
+const char* zs_last_error(void) { return g_last_error; }
+
+int zs_version(void) { return 10000; }
+
+}  // extern "C"

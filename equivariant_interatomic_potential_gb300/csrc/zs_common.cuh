@@ -1,0 +1,112 @@
+// Shared definitions of libzs's CUDA sources (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zs.h"
+
+namespace zs {
+
+constexpr int kRows = 15;   // zonal rows of the lmax = 3 ladder (3 + 5 + 7)
+constexpr int kSlots = 3;   // radial slots, one per degree 1..3
+constexpr int kD = 16;      // node rows: scalar row + 15
+
+// Degree group of zonal row r as a radial slot (row groups 3/5/7).
+__host__ __device__ __forceinline__ int slot_of_row(int r) { return r < 3 ? 0 : (r < 8 ? 1 : 2); }
+
+// Record a message for zs_last_error() and return the status.
+zs_status fail(zs_status st, const char* fmt, ...);
+// Check the last launch on this thread; ZS_ERR_CUDA with a message on failure.
+zs_status check_launch(const char* what);
+
+__host__ __device__ __forceinline__ bool aligned16(const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Streaming loads: data read once, kept out of L1.
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_stream(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ int ld_stream_i(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+// Read-only load that may be cached in L1 (gathered, reused data).
+__device__ __forceinline__ float4 ld_ro4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+// Streaming stores (written once, not re-read by this kernel).
+__device__ __forceinline__ void st_stream4(float* p, float4 v) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_stream(float* p, float v) {
+    asm volatile("st.global.cs.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 f4_fma(float s, float4 a, float4 acc) {
+    acc.x = fmaf(s, a.x, acc.x);
+    acc.y = fmaf(s, a.y, acc.y);
+    acc.z = fmaf(s, a.z, acc.z);
+    acc.w = fmaf(s, a.w, acc.w);
+    return acc;
+}
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ float4 f4_shfl(float4 v, int src) {
+    v.x = __shfl_sync(0xffffffffu, v.x, src);
+    v.y = __shfl_sync(0xffffffffu, v.y, src);
+    v.z = __shfl_sync(0xffffffffu, v.z, src);
+    v.w = __shfl_sync(0xffffffffu, v.w, src);
+    return v;
+}
+__device__ __forceinline__ float4 f4_shfl_xor(float4 v, int m) {
+    v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+    v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+    v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+    v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+    return v;
+}
+__device__ __forceinline__ float f4_dot(float4 a, float4 b) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+}
+
+// First index i in [0, n) with a[i] >= key (n if none).
+__device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int64_t key) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if ((int64_t)__ldg(a + mid) < key) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+inline int num_sms() {
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached = v > 0 ? v : 1;
+    }
+    return cached;
+}
+
+template <class T>
+__host__ __device__ __forceinline__ constexpr T imin(T a, T b) { return a < b ? a : b; }
+template <class T>
+__host__ __device__ __forceinline__ constexpr T imax(T a, T b) { return a < b ? b : a; }
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace zs

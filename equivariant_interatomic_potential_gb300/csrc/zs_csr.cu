@@ -1,0 +1,258 @@
+// Stable destination CSR for the zonal scatter (row_ptr, perm).
+//
+// The forward of the deepmd-kit pull request "fused Triton zonal scatter for
+// the GIE head" walks a destination CSR whose within-node order is the edge
+// order ("stable-sort CSR order", section "What").  Built here as an LSD
+// radix sort of destination keys with 8-bit digits, each pass in three
+// launches with no inter-CTA waiting:
+//   upsweep   -- per tile of 2048 keys, a 256-bin digit histogram
+//   scan      -- per digit, exclusive scan of its histogram row over tiles
+//   downsweep -- per tile, stable rank of every key among equal digits
+//                (warp match + per-warp running counts), then scatter
+// and a final pass that reads the sorted keys to write row_ptr.
+// Every step is integer arithmetic in a fixed order, so perm is unique and
+// bit-identical to a sequential counting sort.  Keys outside [0, N) sort as
+// key N, after all valid ones.
+#include "zs_common.cuh"
+
+namespace zs {
+namespace {
+
+constexpr int kCsrWarps = 8;
+constexpr int kCsrThreads = kCsrWarps * 32;
+constexpr int kCsrItems = 8;
+constexpr int kTile = kCsrWarps * kCsrItems * 32;  // 2048 keys per tile
+constexpr int kRadix = 256;
+
+__device__ __forceinline__ int32_t key_of(const int32_t* keys_in, int64_t idx, int32_t N, bool first) {
+    int32_t k = __ldg(keys_in + idx);
+    if (first) k = (k >= 0 && k < N) ? k : N;
+    return k;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+template <bool kFirst>
+__global__ void __launch_bounds__(kCsrThreads)
+csr_upsweep(const int32_t* __restrict__ keys_in, int64_t E, int32_t N, int shift,
+            int32_t* __restrict__ hist, int T) {
+    __shared__ int cnt[kCsrWarps][kRadix];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < kCsrWarps * kRadix; i += kCsrThreads) (&cnt[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)warp * kCsrItems * 32;
+#pragma unroll
+    for (int i = 0; i < kCsrItems; ++i) {
+        const int64_t idx = base + i * 32 + lane;
+        const bool valid = idx < E;
+        const int digit = valid ? ((key_of(keys_in, idx, N, kFirst) >> shift) & (kRadix - 1)) : kRadix;
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        if (valid && lane == __ffs(peers) - 1) cnt[warp][digit] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int d = tid; d < kRadix; d += kCsrThreads) {
+        int s = 0;
+#pragma unroll
+        for (int w = 0; w < kCsrWarps; ++w) s += cnt[w][d];
+        hist[(int64_t)d * T + blockIdx.x] = s;
+    }
+}
+
+// One warp per digit: exclusive scan of hist[d, 0..T) in place, total to tot[d].
+__global__ void __launch_bounds__(kCsrThreads)
+csr_scan(int32_t* __restrict__ hist, int T, int32_t* __restrict__ tot) {
+    constexpr int R = 8;
+    const int lane = threadIdx.x & 31;
+    const int d = blockIdx.x * kCsrWarps + (threadIdx.x >> 5);
+    if (d >= kRadix) return;
+    int32_t* row = hist + (int64_t)d * T;
+    int carry = 0;
+    for (int base = 0; base < T; base += 32 * R) {
+        int v[R];
+        int s = 0;
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int i = base + lane * R + k;
+            v[k] = i < T ? row[i] : 0;
+            s += v[k];
+        }
+        int incl = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int run = carry + incl - s;
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int i = base + lane * R + k;
+            if (i < T) row[i] = run;
+            run += v[k];
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tot[d] = carry;
+}
+
+template <bool kFirst>
+__global__ void __launch_bounds__(kCsrThreads)
+csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
+              int64_t E, int32_t N, int shift,
+              const int32_t* __restrict__ hist, const int32_t* __restrict__ tot, int T,
+              int32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out) {
+    __shared__ int cnt[kCsrWarps][kRadix];
+    __shared__ int wsum[kCsrWarps];
+    __shared__ int dbase[kRadix];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < kCsrWarps * kRadix; i += kCsrThreads) (&cnt[0][0])[i] = 0;
+
+    // Exclusive scan of the 256 digit totals (kCsrThreads == kRadix).
+    {
+        const int v = tot[tid];
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int pre = 0;
+        for (int w = 0; w < warp; ++w) pre += wsum[w];
+        dbase[tid] = pre + incl - v;
+    }
+    __syncthreads();
+
+    const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)warp * kCsrItems * 32;
+    int32_t key[kCsrItems], val[kCsrItems];
+    int rank[kCsrItems], dig[kCsrItems];
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int i = 0; i < kCsrItems; ++i) {
+        const int64_t idx = base + i * 32 + lane;
+        const bool valid = idx < E;
+        key[i] = valid ? key_of(keys_in, idx, N, kFirst) : 0;
+        val[i] = valid ? (kFirst ? (int32_t)idx : __ldg(vals_in + idx)) : 0;
+        dig[i] = valid ? ((key[i] >> shift) & (kRadix - 1)) : kRadix;
+        const unsigned peers = __match_any_sync(0xffffffffu, dig[i]);
+        rank[i] = valid ? cnt[warp][dig[i]] + __popc(peers & lt) : 0;
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) cnt[warp][dig[i]] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    {
+        const int d = tid;  // one thread per digit
+        int run = dbase[d] + hist[(int64_t)d * T + blockIdx.x];
+#pragma unroll
+        for (int w = 0; w < kCsrWarps; ++w) {
+            const int c = cnt[w][d];
+            cnt[w][d] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kCsrItems; ++i) {
+        if (dig[i] < kRadix) {
+            const int pos = cnt[warp][dig[i]] + rank[i];
+            keys_out[pos] = key[i];
+            vals_out[pos] = val[i];
+        }
+    }
+}
+
+// row_ptr from sorted keys: position j is the first of every node in
+// (key[j-1], key[j]]; the count of keys equal to N (invalid) is E - row_ptr[N].
+__global__ void __launch_bounds__(256)
+csr_row_ptr(const int32_t* __restrict__ sorted, int64_t E, int32_t N,
+            int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j > E) return;
+    const int64_t kprev = j > 0 ? (int64_t)sorted[j - 1] : -1;
+    const int64_t kcur = j < E ? (int64_t)sorted[j] : (int64_t)N + 1;
+    const int64_t hi = kcur < (int64_t)N ? kcur : (int64_t)N;
+    for (int64_t n = kprev + 1; n <= hi; ++n) {
+        row_ptr[n] = (int32_t)j;
+        if (n == N && bad) *bad = (int32_t)(E - j);
+    }
+}
+
+struct CsrPlan {
+    int T = 0;
+    int passes = 0;
+    size_t off_k[2] = {0, 0}, off_v[2] = {0, 0}, off_hist = 0, off_tot = 0, bytes = 0;
+};
+
+CsrPlan csr_plan(int64_t E, int32_t N) {
+    CsrPlan p;
+    if (E <= 0) return p;
+    p.T = (int)((E + kTile - 1) / kTile);
+    const uint32_t maxkey = (uint32_t)N;
+    const int bits = maxkey == 0 ? 1 : 32 - __builtin_clz(maxkey);
+    p.passes = (bits + 7) / 8;
+    const size_t ebytes = align_up((size_t)E * 4, 256);
+    size_t off = 0;
+    p.off_k[0] = off; off += ebytes;
+    p.off_v[0] = off; off += ebytes;
+    p.off_k[1] = off; off += ebytes;
+    p.off_v[1] = off; off += ebytes;
+    p.off_hist = off; off += align_up((size_t)kRadix * p.T * 4, 256);
+    p.off_tot = off; off += align_up((size_t)kRadix * 4, 256);
+    p.bytes = off;
+    return p;
+}
+
+}  // namespace
+}  // namespace zs
+
+using namespace zs;
+
+extern "C" size_t zs_build_csr_workspace_bytes(int64_t E, int32_t N) {
+    if (E < 0 || N < 0) return 0;
+    return csr_plan(E, N).bytes;
+}
+
+extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
+                                  int32_t* row_ptr, int32_t* perm, int32_t* bad_dst_count,
+                                  void* workspace, size_t workspace_bytes, zs_stream_t stream) {
+    if (E < 0 || N < 0) return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: negative size (E=%lld, N=%d)", (long long)E, N);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: E=%lld exceeds the int32 index range", (long long)E);
+    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: row_ptr is NULL");
+    if (E > 0 && (!dst || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: dst or perm is NULL with E > 0");
+    const CsrPlan p = csr_plan(E, N);
+    if (workspace_bytes < p.bytes) return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: workspace of %zu bytes, %zu needed", workspace_bytes, p.bytes);
+    if (p.bytes > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: workspace NULL or not 256-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const int32_t* sorted = nullptr;
+    if (E > 0) {
+        int32_t* hist = reinterpret_cast<int32_t*>(ws + p.off_hist);
+        int32_t* tot = reinterpret_cast<int32_t*>(ws + p.off_tot);
+        const int32_t* kin = dst;
+        const int32_t* vin = nullptr;
+        for (int pass = 0; pass < p.passes; ++pass) {
+            const bool first = pass == 0, last = pass == p.passes - 1;
+            const int shift = 8 * pass;
+            int32_t* kout = reinterpret_cast<int32_t*>(ws + p.off_k[pass & 1]);
+            int32_t* vout = last ? perm : reinterpret_cast<int32_t*>(ws + p.off_v[pass & 1]);
+            if (first) csr_upsweep<true><<<p.T, kCsrThreads, 0, s>>>(kin, E, N, shift, hist, p.T);
+            else csr_upsweep<false><<<p.T, kCsrThreads, 0, s>>>(kin, E, N, shift, hist, p.T);
+            csr_scan<<<kRadix / kCsrWarps, kCsrThreads, 0, s>>>(hist, p.T, tot);
+            if (first) csr_downsweep<true><<<p.T, kCsrThreads, 0, s>>>(kin, vin, E, N, shift, hist, tot, p.T, kout, vout);
+            else csr_downsweep<false><<<p.T, kCsrThreads, 0, s>>>(kin, vin, E, N, shift, hist, tot, p.T, kout, vout);
+            kin = kout;
+            vin = vout;
+        }
+        sorted = kin;
+    }
+    const int64_t threads = E + 1;
+    csr_row_ptr<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(sorted, E, N, row_ptr, bad_dst_count);
+    return check_launch("zs_build_csr");
+}

@@ -1,0 +1,393 @@
+// Forward zonal scatter, lmax = 3:
+//   out[n,0,:] = 0,  out[n,1+r,c] = sum over n's CSR positions j (in order)
+//                                   of coup[e,r] * rad[e,slot(r),c], e = perm[j]
+// (deepmd-kit pull request "fused Triton zonal scatter for the GIE head",
+// section "What", forward bullet: a node-parallel walk of the stable
+// destination CSR, message accumulated in registers, the (E,15,C) message
+// never materialised, padded (N,16,C) output with a zero scalar row).
+//
+// Work split.  The pages use one program per node; on a 152-SM part with a
+// skewed in-degree (one node can own 1/6 of all edges) that leaves most SMs
+// idle while one streams.  Here every warp owns a fixed window of CSR
+// POSITIONS instead, so all warps move the same number of bytes whatever the
+// degree distribution:
+//   * a node that lies inside one warp's window is summed in CSR order in
+//     registers and written directly;
+//   * a node cut by window edges is summed piecewise: the pieces inside one
+//     CTA are added in shared memory in window order, and a node that crosses
+//     CTA windows leaves one partial per CTA in the workspace, which a second
+//     small kernel adds in CTA order.
+// Every sum is therefore formed in one fixed order: run to run bitwise
+// deterministic, no floating-point atomics.
+#include "zs_common.cuh"
+
+namespace zs {
+namespace {
+
+constexpr int kFwdWarps = 8;
+constexpr int kFwdThreads = kFwdWarps * 32;
+constexpr int kSubWin = 256;                   // CSR positions per warp
+constexpr int kCtaWin = kFwdWarps * kSubWin;   // CSR positions per CTA (C == 32 path)
+constexpr int kGenWin = 256;                   // CSR positions per warp (per-channel path)
+constexpr int kC32 = 32;
+constexpr int kNodeFloats32 = kD * kC32;       // 512 floats per node at C = 32
+constexpr int kPartFloats32 = kRows * kC32;    // 480 floats per partial at C = 32
+constexpr unsigned kFull = 0xffffffffu;
+
+// --------------------------------------------------------------------------
+// C == 32 path.  Lane layout: group g = lane/8 owns zonal rows 4g..4g+3 (row
+// 15 is padding), quad q = lane%8 owns channels 4q..4q+3.  Rows 4g..4g+2
+// share one radial slot; row 4g+3 uses the slot of lane+8 for g == 0 (row 3
+// is the first degree-2 row) and the lane's own slot otherwise.
+// --------------------------------------------------------------------------
+
+struct Lane32 {
+    int lane, g, q, slo, src_hi;
+    __device__ __forceinline__ explicit Lane32(int l) : lane(l), g(l >> 3), q(l & 7) {
+        slo = g == 0 ? 0 : (g == 1 ? 1 : 2);
+        src_hi = g == 0 ? lane + 8 : lane;
+    }
+};
+
+// Sum the messages of CSR positions [s, t) into acc (rows 4g..4g+3, channels 4q..4q+3).
+__device__ __forceinline__ void accumulate32(const float* __restrict__ coup, const float* __restrict__ rad,
+                                             const int32_t* __restrict__ perm, int64_t E,
+                                             int s, int t, float (*cs)[16], const Lane32& L, float4 acc[4]) {
+    const float* radq = rad + L.slo * kC32 + 4 * L.q;
+    for (int base = s; base < t; base += 32) {
+        const int cnt = min(32, t - base);
+        int e_l = -1;
+        if (L.lane < cnt) {
+            e_l = ld_stream_i(perm + base + L.lane);
+            if ((uint32_t)e_l >= (uint64_t)E) e_l = -1;   // malformed perm: contributes nothing
+        }
+        // Stage the 32 coupling rows (15 floats each) into shared memory.
+#pragma unroll
+        for (int it = 0; it < kRows; ++it) {
+            const int v = it * 32 + L.lane;
+            const int j = v / kRows;
+            const int r = v - j * kRows;
+            const int e = __shfl_sync(kFull, e_l, j);
+            float c = 0.f;
+            if (j < cnt && e >= 0) c = __ldg(coup + (int64_t)e * kRows + r);
+            cs[j][r] = c;
+        }
+        __syncwarp();
+        for (int j0 = 0; j0 < cnt; j0 += 8) {
+            float4 a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = __shfl_sync(kFull, e_l, j0 + u);
+                a[u] = (j0 + u < cnt && e >= 0) ? ld_stream4(radq + (int64_t)e * (kSlots * kC32))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float4 b = f4_shfl(a[u], L.src_hi);
+                const float4 c4 = *reinterpret_cast<const float4*>(&cs[j0 + u][4 * L.g]);
+                acc[0] = f4_fma(c4.x, a[u], acc[0]);
+                acc[1] = f4_fma(c4.y, a[u], acc[1]);
+                acc[2] = f4_fma(c4.z, a[u], acc[2]);
+                acc[3] = f4_fma(c4.w, b, acc[3]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Write rows 1..15 of one node from acc, and the zero scalar row.
+__device__ __forceinline__ void store_node32(float* __restrict__ node, const float4 acc[4], const Lane32& L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 4 * L.g + i;
+        if (r < kRows) *reinterpret_cast<float4*>(node + (1 + r) * kC32 + 4 * L.q) = acc[i];
+    }
+    if (L.g == 3) *reinterpret_cast<float4*>(node + 4 * L.q) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ void store_part32(float* __restrict__ part, const float4 acc[4], const Lane32& L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 4 * L.g + i;
+        if (r < kRows) *reinterpret_cast<float4*>(part + r * kC32 + 4 * L.q) = acc[i];
+    }
+}
+
+__device__ __forceinline__ void load_part32(const float* __restrict__ part, float4 acc[4], const Lane32& L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 4 * L.g + i;
+        acc[i] = r < kRows ? *reinterpret_cast<const float4*>(part + r * kC32 + 4 * L.q)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+__device__ __forceinline__ void zero_node32(float* __restrict__ node, int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float4*>(node + 4 * (lane + 32 * k)) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// First node to visit for window [p0, ...): the node containing p0 when it
+// starts before p0, else the first node starting at or after p0.
+__device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
+    const int n_lb = lower_bound_i32(row_ptr, N + 1, p0);
+    if (n_lb >= 1 && n_lb <= N && (int64_t)__ldg(row_ptr + n_lb) > p0) return n_lb - 1;
+    return n_lb;
+}
+
+__global__ void __launch_bounds__(kFwdThreads)
+fwd_c32_main(const float* __restrict__ coup, const float* __restrict__ rad,
+             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+             int64_t E, int32_t N, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
+    __shared__ __align__(16) float cs[kFwdWarps][32][16];
+    __shared__ __align__(16) float sp[kFwdWarps][2][kPartFloats32];
+    __shared__ int sp_node[kFwdWarps][2];
+    const int warp = threadIdx.x >> 5;
+    const Lane32 L(threadIdx.x & 31);
+    const int gw = blockIdx.x * kFwdWarps + warp;
+    cs[warp][L.lane][15] = 0.f;
+    if (L.lane < 2) sp_node[warp][L.lane] = -1;
+    __syncwarp();
+
+    if (gw < Wtot) {
+        const int64_t p0 = (int64_t)gw * kSubWin;
+        const int64_t p1 = min(p0 + kSubWin, E);
+        const bool is_last = gw == Wtot - 1;
+        for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
+            const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
+            if (a >= p1 && !(is_last && a == b)) break;
+            if (a == b) {                       // no edges: an all-zero node
+                zero_node32(out + (int64_t)n * kNodeFloats32, L.lane);
+                continue;
+            }
+            float4 acc[4] = {};
+            accumulate32(coup, rad, perm, E, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1), cs[warp], L, acc);
+            if (a >= p0 && b <= p1) {
+                store_node32(out + (int64_t)n * kNodeFloats32, acc, L);
+            } else {
+                const int slot = a < p0 ? 0 : 1;
+                store_part32(sp[warp][slot], acc, L);
+                if (L.lane == 0) sp_node[warp][slot] = n;
+            }
+            if (b > p1) break;
+        }
+    }
+    __syncthreads();
+
+    // Combine the warp pieces of nodes cut by window edges inside this CTA.
+    // The lowest warp holding a piece of node m adds the pieces in window order.
+    const int64_t P0 = (int64_t)blockIdx.x * kCtaWin;
+    const int64_t P1 = min(P0 + kCtaWin, E);
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
+        const int m = sp_node[warp][slot];
+        if (m < 0) continue;
+        if (warp > 0 && (sp_node[warp - 1][0] == m || sp_node[warp - 1][1] == m)) continue;
+        if (slot == 0 && sp_node[warp][1] == m) continue;  // cannot happen; keeps one leader per node
+        float4 acc[4];
+        load_part32(sp[warp][slot], acc, L);
+        for (int w2 = warp + 1; w2 < kFwdWarps && sp_node[w2][0] == m; ++w2) {
+            float4 t[4];
+            load_part32(sp[w2][0], t, L);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = f4_add(acc[i], t[i]);
+        }
+        const int a = __ldg(row_ptr + m), b = __ldg(row_ptr + m + 1);
+        if (a >= P0 && b <= P1) {
+            store_node32(out + (int64_t)m * kNodeFloats32, acc, L);
+        } else {
+            const int cslot = a < P0 ? 0 : 1;
+            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + cslot) * kPartFloats32, acc, L);
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Per-channel path (any C, any alignment).  One warp per window of kGenWin
+// positions, lane = channel within a chunk of 32 channels; every cut node
+// leaves a partial per window in the workspace.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, const float* __restrict__ rad,
+                                               const int32_t* __restrict__ perm, int64_t E, int C, int c,
+                                               int s, int t, float (*cs)[16], int lane, float acc[kRows]) {
+    const bool cok = c < C;
+    for (int base = s; base < t; base += 32) {
+        const int cnt = min(32, t - base);
+        int e_l = -1;
+        if (lane < cnt) {
+            e_l = __ldg(perm + base + lane);
+            if ((uint32_t)e_l >= (uint64_t)E) e_l = -1;
+        }
+#pragma unroll
+        for (int it = 0; it < kRows; ++it) {
+            const int v = it * 32 + lane;
+            const int j = v / kRows;
+            const int r = v - j * kRows;
+            const int e = __shfl_sync(kFull, e_l, j);
+            float cv = 0.f;
+            if (j < cnt && e >= 0) cv = __ldg(coup + (int64_t)e * kRows + r);
+            cs[j][r] = cv;
+        }
+        __syncwarp();
+        for (int j = 0; j < cnt; ++j) {
+            const int e = __shfl_sync(kFull, e_l, j);
+            if (e < 0 || !cok) continue;
+            const float* rp = rad + (int64_t)e * kSlots * C + c;
+            const float r0 = __ldg(rp), r1 = __ldg(rp + C), r2 = __ldg(rp + 2 * C);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float rv = r < 3 ? r0 : (r < 8 ? r1 : r2);
+                acc[r] = fmaf(cs[j][r], rv, acc[r]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kFwdThreads)
+fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
+             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+             int64_t E, int32_t N, int C, int Wtot, float* __restrict__ out, float* __restrict__ part) {
+    __shared__ float cs[kFwdWarps][32][16];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kFwdWarps + warp;
+    if (gw >= Wtot) return;
+    const int64_t V = (int64_t)kRows * C;
+    const int64_t p0 = (int64_t)gw * kGenWin;
+    const int64_t p1 = min(p0 + kGenWin, E);
+    const bool is_last = gw == Wtot - 1;
+    for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
+        const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
+        if (a >= p1 && !(is_last && a == b)) break;
+        float* node = out + (int64_t)n * kD * C;
+        if (a == b) {
+            for (int64_t i = lane; i < (int64_t)kD * C; i += 32) node[i] = 0.f;
+            continue;
+        }
+        const bool full = a >= p0 && b <= p1;
+        float* dstp = full ? node + C : part + ((int64_t)gw * 2 + (a < p0 ? 0 : 1)) * V;
+        if (full)
+            for (int c = lane; c < C; c += 32) node[c] = 0.f;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            const int c = c0 + lane;
+            float acc[kRows];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+            accumulate_gen(coup, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
+                           cs[warp], lane, acc);
+            if (c < C) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) dstp[(int64_t)r * C + c] = acc[r];
+            }
+        }
+        if (b > p1) break;
+    }
+}
+
+// --------------------------------------------------------------------------
+// Cross-window fix-up: for each node whose positions span more than one
+// window of `win` positions, add its window partials in window order and
+// write rows 1..15 and the zero scalar row.  Partial k of a node is the one
+// of window floor(a/win) + k, slot 1 for k == 0 (the node starts inside it)
+// and slot 0 after (the node runs in from the previous window).
+// Warp w adds partials k = w, w+8, ...; the eight warp sums are then added
+// in warp order.
+// --------------------------------------------------------------------------
+
+constexpr int kFixVals = 256;   // values per chunk: 8 per lane
+
+__global__ void __launch_bounds__(kFwdThreads)
+fwd_fixup(const int32_t* __restrict__ row_ptr, int32_t N, int C, int win,
+          const float* __restrict__ part, float* __restrict__ out) {
+    __shared__ float red[kFwdWarps][kFixVals];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t V = (int64_t)kRows * C;
+    for (int n = blockIdx.x; n < N; n += gridDim.x) {
+        const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
+        if (a >= b) continue;
+        const int wa = a / win, wb = (b - 1) / win;
+        if (wa == wb) continue;
+        const int np = wb - wa + 1;
+        float* node = out + (int64_t)n * kD * C;
+        for (int c = threadIdx.x; c < C; c += kFwdThreads) node[c] = 0.f;
+        for (int64_t v0 = 0; v0 < V; v0 += kFixVals) {
+            float s[kFixVals / 32];
+#pragma unroll
+            for (int i = 0; i < kFixVals / 32; ++i) s[i] = 0.f;
+            for (int k = warp; k < np; k += kFwdWarps) {
+                const float* p = part + ((int64_t)(wa + k) * 2 + (k == 0 ? 1 : 0)) * V + v0;
+#pragma unroll
+                for (int i = 0; i < kFixVals / 32; ++i) {
+                    const int64_t v = v0 + lane + 32 * i;
+                    if (v < V) s[i] += __ldg(p + lane + 32 * i);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kFixVals / 32; ++i) red[warp][lane + 32 * i] = s[i];
+            __syncthreads();
+            {
+                const int vl = threadIdx.x;   // kFwdThreads == kFixVals
+                const int64_t v = v0 + vl;
+                if (v < V) {
+                    float t = red[0][vl];
+#pragma unroll
+                    for (int w = 1; w < kFwdWarps; ++w) t += red[w][vl];
+                    node[C + v] = t;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+}  // namespace zs
+
+using namespace zs;
+
+extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
+    if (E < 0 || N < 0 || C < 1) return 0;
+    (void)N;
+    // Sized for the per-channel path (one partial pair per 256 positions),
+    // which also covers the C == 32 path (one pair per 2048 positions).
+    const int64_t windows = ceil_div(E > 0 ? E : 1, kGenWin);
+    return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256);
+}
+
+extern "C" zs_status zs_forward(const float* coup, const float* rad,
+                                const int32_t* row_ptr, const int32_t* perm,
+                                int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                float* out, void* workspace, size_t workspace_bytes,
+                                zs_stream_t stream) {
+    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_forward: lmax=%d, only lmax=3 (row groups 3/5/7) is supported", lmax);
+    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: E=%lld exceeds the int32 index range", (long long)E);
+    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_forward: row_ptr is NULL");
+    if (N > 0 && !out) return fail(ZS_ERR_INVALID_ARG, "zs_forward: out is NULL");
+    if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward: coup, rad or perm is NULL with E > 0");
+    const size_t need = zs_forward_workspace_bytes(E, N, C);
+    if (workspace_bytes < need) return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace NULL or not 256-byte aligned");
+    if (N == 0) return ZS_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* part = static_cast<float*>(workspace);
+    const bool fast = C == kC32 && aligned16(rad) && aligned16(out);
+    const int fix_grid = (int)imin<int64_t>(N, (int64_t)num_sms() * 8);
+    if (fast) {
+        const int64_t Wtot = ceil_div(E > 0 ? E : 1, kSubWin);
+        const int64_t ctas = ceil_div(Wtot, kFwdWarps);
+        fwd_c32_main<<<(unsigned)ctas, kFwdThreads, 0, s>>>(coup, rad, row_ptr, perm, E, N, (int)Wtot, out, part);
+        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, kCtaWin, part, out);
+    } else {
+        const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
+        const int64_t ctas = ceil_div(Wtot, kFwdWarps);
+        fwd_gen_main<<<(unsigned)ctas, kFwdThreads, 0, s>>>(coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
+        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, kGenWin, part, out);
+    }
+    return check_launch("zs_forward");
+}

@@ -1,0 +1,179 @@
+"""Python binding of libzs (include/zs.h): argument marshalling only.
+
+Every entry point has the name of the C function it calls.  Tensors must be
+CUDA tensors of the documented dtype and shape; outputs and workspaces are
+allocated with torch when not given.  All compute runs in libzs's kernels;
+there is no fallback, and a missing or unbuildable library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+ZS_OK = 0
+STATUS_NAMES = {0: "ZS_OK", 1: "ZS_ERR_INVALID_ARG", 2: "ZS_ERR_UNSUPPORTED", 3: "ZS_ERR_CUDA", 4: "ZS_ERR_TIMEOUT"}
+
+
+class ZsError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libzs.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libzs.so not found at {_build.LIB}; run equivariant_interatomic_potential_gb300.build")
+        lib = ctypes.CDLL(_build.LIB)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.zs_status_string.restype = ctypes.c_char_p
+        lib.zs_status_string.argtypes = [ctypes.c_int]
+        lib.zs_last_error.restype = ctypes.c_char_p
+        lib.zs_last_error.argtypes = []
+        lib.zs_version.restype = ctypes.c_int
+        lib.zs_version.argtypes = []
+        lib.zs_build_csr_workspace_bytes.restype = SZ
+        lib.zs_build_csr_workspace_bytes.argtypes = [I64, I32]
+        lib.zs_build_csr.restype = ctypes.c_int
+        lib.zs_build_csr.argtypes = [P, I64, I32, P, P, P, P, SZ, P]
+        lib.zs_forward_workspace_bytes.restype = SZ
+        lib.zs_forward_workspace_bytes.argtypes = [I64, I32, I32]
+        lib.zs_forward.restype = ctypes.c_int
+        lib.zs_forward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
+        lib.zs_backward.restype = ctypes.c_int
+        lib.zs_backward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P]
+        _lib = lib
+        return lib
+
+
+def declared_functions(header: str | None = None) -> list[str]:
+    """Names of the functions include/zs.h declares (ZS_API prototypes)."""
+    header = header or os.path.join(_build.INCLUDE, "zs.h")
+    with open(header) as f:
+        text = f.read()
+    return re.findall(r"ZS_API\s+[\w\s\*]*?\b(zs_\w+)\s*\(", text)
+
+
+def _check(fn: str, status: int):
+    if status != ZS_OK:
+        raise ZsError(fn, status, load().zs_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple):
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def zs_build_csr_workspace_bytes(E: int, N: int) -> int:
+    return int(load().zs_build_csr_workspace_bytes(E, N))
+
+
+def zs_forward_workspace_bytes(E: int, N: int, C: int) -> int:
+    return int(load().zs_forward_workspace_bytes(E, N, C))
+
+
+def zs_build_csr(dst: torch.Tensor, N: int, row_ptr=None, perm=None, bad_dst_count=None,
+                 workspace=None, stream=None):
+    """Stable destination CSR.  Returns (row_ptr (N+1,), perm (E,), bad_dst_count (1,)) int32."""
+    E = dst.shape[0]
+    dev = dst.device
+    _need(dst, "dst", torch.int32, (E,))
+    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev) if row_ptr is None else row_ptr
+    perm = torch.empty(E, dtype=torch.int32, device=dev) if perm is None else perm
+    bad_dst_count = torch.empty(1, dtype=torch.int32, device=dev) if bad_dst_count is None else bad_dst_count
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    need = zs_build_csr_workspace_bytes(E, N)
+    if workspace is None:
+        workspace = _workspace(need, dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("zs_build_csr", load().zs_build_csr(_ptr(dst), E, N, _ptr(row_ptr), _ptr(perm), _ptr(bad_dst_count),
+                                               _ptr(workspace), wbytes, _stream(stream)))
+    return row_ptr, perm, bad_dst_count
+
+
+def zs_forward(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,
+               out=None, workspace=None, stream=None, lmax: int = 3):
+    """Forward zonal scatter.  Returns out (N, 16, C) fp32."""
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(coup, "coup", torch.float32, (E, 15))
+    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    out = torch.empty((N, 16, C), dtype=torch.float32, device=dev) if out is None else out
+    _need(out, "out", torch.float32, (N, 16, C))
+    if workspace is None:
+        workspace = _workspace(zs_forward_workspace_bytes(E, N, C), dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("zs_forward", load().zs_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), E, N, C, lmax,
+                                           _ptr(out), _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+def zs_backward(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, N: int,
+                d_coup=None, d_rad=None, stream=None, lmax: int = 3):
+    """Backward.  Returns (d_coup (E, 15), d_rad (E, 3, C)) fp32."""
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(g, "g", torch.float32, (N, 16, C))
+    _need(coup, "coup", torch.float32, (E, 15))
+    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(dst, "dst", torch.int32, (E,))
+    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev) if d_coup is None else d_coup
+    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_coup, "d_coup", torch.float32, (E, 15))
+    _need(d_rad, "d_rad", torch.float32, (E, 3, C))
+    _check("zs_backward", load().zs_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C, lmax,
+                                             _ptr(d_coup), _ptr(d_rad), _stream(stream)))
+    return d_coup, d_rad

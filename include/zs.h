@@ -1,0 +1,149 @@
+/*
+ * zs.h -- C ABI of libzs: the zonal scatter of the geometric initial
+ * embedding (GIE) of an SO(3)-equivariant interatomic potential, lmax = 3,
+ * forward and backward, with the stable destination CSR it walks.
+ *
+ * What the operation is: deepmd-kit pull request "fused Triton zonal scatter
+ * for the GIE head (DP_GIE_SCATTER_INFER)", section "What" (forward bullet:
+ * a node-parallel walk of the stable destination CSR that accumulates the
+ * message without materialising the (E, D-1, C) surface and writes the
+ * padded (N, D, C) node layout with a zero scalar row; backward bullet: one
+ * edge-parallel pass giving the (E, D-1) coupling and (E, lmax, C) radial
+ * gradients; last bullet: the reduction follows the stable-sort CSR order)
+ * and section "Boundary and layout contract" (contiguous inputs, the packed
+ * lmax = 3 row layout of degree groups 3/5/7).
+ *
+ * Notation: D = 16 node rows, R = 15 zonal rows, rows 0..2 are degree 1,
+ * rows 3..7 degree 2, rows 8..14 degree 3; radial slot s = degree - 1.
+ *   coup  (E, 15)     fp32, row-major, contiguous
+ *   rad   (E, 3, C)   fp32, row-major, contiguous
+ *   out   (N, 16, C)  fp32, row-major, contiguous
+ *   g     (N, 16, C)  fp32 cotangent of out (row 0 is never read)
+ *   forward:  out[n,0,c] = 0,
+ *             out[n,1+r,c] = sum over CSR positions j of node n, in order,
+ *                            of coup[e,r] * rad[e,s(r),c], e = perm[j]
+ *   backward: d_coup[e,r]  = sum_c g[dst[e],1+r,c] * rad[e,s(r),c]
+ *             d_rad[e,s,c] = sum over rows r of slot s of g[dst[e],1+r,c] * coup[e,r]
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  Inputs are
+ *     only read.  Outputs are fully overwritten (the caller need not zero
+ *     them).  The library never allocates or frees memory; scratch comes from
+ *     the caller's workspace, sized by the matching *_workspace_bytes query.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and is asynchronous: no entry point synchronises the
+ *     host.  A status other than ZS_OK means nothing was enqueued, except
+ *     ZS_ERR_CUDA, which reports a failed launch (see zs_last_error()).
+ *   - E = 0 and N = 0 are valid.  Sizes are limited to E < 2^31 (perm and
+ *     row_ptr are int32); all address arithmetic inside is 64-bit.
+ *   - Results are bitwise deterministic run to run for the same inputs.
+ *   - Destinations outside [0, N) belong to no node (reading of the pages,
+ *     which leave them undefined): the CSR build counts them and places them
+ *     after all valid edges; the backward gives those edges zero gradients.
+ *   - Any C >= 1 is accepted.  C == 32 with 16-byte aligned float4 operands
+ *     (rad and out in the forward; g, rad and d_rad in the backward) takes
+ *     the vectorised path; every other case takes a per-channel path with
+ *     the same results up to fp32 rounding order.
+ */
+#ifndef ZS_H_
+#define ZS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZS_API __attribute__((visibility("default")))
+#else
+#define ZS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* zs_stream_t;
+
+typedef enum zs_status {
+    ZS_OK = 0,
+    ZS_ERR_INVALID_ARG = 1,  /* null pointer with nonzero size, negative size, E >= 2^31, C < 1, workspace too small */
+    ZS_ERR_UNSUPPORTED = 2,  /* lmax != 3 */
+    ZS_ERR_CUDA = 3,         /* a CUDA call or launch failed; zs_last_error() has the message */
+    ZS_ERR_TIMEOUT = 4       /* reserved: a bounded device wait ran out (no current kernel waits) */
+} zs_status;
+
+/* Static, human-readable name of a status code. */
+ZS_API const char* zs_status_string(int status);
+
+/* Message of the last ZS_ERR_* returned on the calling host thread ("" if none). */
+ZS_API const char* zs_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+ZS_API int zs_version(void);
+
+/*
+ * Bytes of device workspace zs_build_csr needs for E edges and N nodes
+ * (0 when E == 0).  The workspace must be 256-byte aligned.
+ */
+ZS_API size_t zs_build_csr_workspace_bytes(int64_t E, int32_t N);
+
+/*
+ * Stable destination CSR ("stable-sort CSR order", pull request "fused
+ * Triton zonal scatter for the GIE head", section "What").
+ *   dst            (E,)   int32 destination node of each edge
+ *   row_ptr        (N+1,) int32 out: node n owns CSR positions [row_ptr[n], row_ptr[n+1])
+ *   perm           (E,)   int32 out: edge id at each CSR position; within a node,
+ *                         edge ids ascend (stable); edges with dst outside [0, N)
+ *                         fill positions [row_ptr[N], E) in ascending edge order
+ *   bad_dst_count  (1,)   int32 out, may be NULL: number of edges with dst outside [0, N)
+ *   workspace             device scratch of zs_build_csr_workspace_bytes(E, N) bytes
+ * The result is bit-identical to a sequential counting sort.
+ */
+ZS_API zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
+                       int32_t* row_ptr, int32_t* perm, int32_t* bad_dst_count,
+                       void* workspace, size_t workspace_bytes, zs_stream_t stream);
+
+/*
+ * Bytes of device workspace zs_forward needs (partial sums of nodes whose
+ * edges are split across work units).  256-byte alignment required.
+ */
+ZS_API size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C);
+
+/*
+ * Forward zonal scatter (pull request "fused Triton zonal scatter for the
+ * GIE head", section "What", forward bullet).
+ *   coup (E,15), rad (E,3,C)  inputs, indexed by edge id
+ *   row_ptr (N+1,), perm (E,) a CSR as produced by zs_build_csr; positions
+ *                             row_ptr[N]..E-1 are ignored
+ *   E                         length of perm and number of rows of coup/rad
+ *   lmax                      must be 3 (else ZS_ERR_UNSUPPORTED)
+ *   out (N,16,C)              output, fully written: row 0 and the rows of
+ *                             nodes without edges are exact zeros
+ * Each node's sum is formed in fp32 in a fixed order: CSR order within
+ * fixed windows of positions, windows combined in ascending order.
+ */
+ZS_API zs_status zs_forward(const float* coup, const float* rad,
+                     const int32_t* row_ptr, const int32_t* perm,
+                     int64_t E, int32_t N, int32_t C, int32_t lmax,
+                     float* out, void* workspace, size_t workspace_bytes,
+                     zs_stream_t stream);
+
+/*
+ * Backward of the zonal scatter (pull request "fused Triton zonal scatter
+ * for the GIE head", section "What", backward bullet): one edge-parallel
+ * pass writing both operand gradients.
+ *   g (N,16,C)     cotangent of out; row 0 is not read
+ *   coup, rad, dst the forward's inputs, indexed by edge id
+ *   d_coup (E,15)  output, fully written
+ *   d_rad (E,3,C)  output, fully written
+ * Edges with dst outside [0, N) get zero gradients.  Needs no workspace.
+ */
+ZS_API zs_status zs_backward(const float* g, const float* coup, const float* rad,
+                      const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
+                      float* d_coup, float* d_rad, zs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZS_H_ */

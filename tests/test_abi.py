@@ -1,0 +1,113 @@
+"""libzs builds for sm_103a, loads, exports every declared symbol, and rejects
+bad arguments on the host.  No GPU is needed: every call here returns before
+any CUDA call is made."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from equivariant_interatomic_potential_gb300 import build, zs
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return zs.load()
+
+
+def test_header_declares_the_boundary():
+    names = zs.declared_functions()
+    for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_build_csr_workspace_bytes",
+               "zs_forward_workspace_bytes", "zs_status_string", "zs_last_error", "zs_version"):
+        assert fn in names
+
+
+def test_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for fn in zs.declared_functions():
+        assert fn in exported, fn
+        assert getattr(lib, fn) is not None
+    # nothing else of ours leaks out of the library
+    ours = {s for s in exported if s.startswith("zs_") or "zs" in s.split("_")[0]}
+    assert ours <= set(zs.declared_functions())
+
+
+def test_built_for_sm_103a():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert build.up_to_date()
+
+
+def test_status_strings(lib):
+    assert lib.zs_status_string(0) == b"ZS_OK"
+    assert lib.zs_status_string(1) == b"ZS_ERR_INVALID_ARG"
+    assert lib.zs_status_string(2) == b"ZS_ERR_UNSUPPORTED"
+    assert lib.zs_status_string(3) == b"ZS_ERR_CUDA"
+    assert lib.zs_status_string(4) == b"ZS_ERR_TIMEOUT"
+    assert lib.zs_status_string(99) == b"ZS_ERR_UNKNOWN"
+    assert lib.zs_version() == 10000
+
+
+FAKE = 1 << 20   # a non-null, 256-byte aligned address never dereferenced by these calls
+
+
+def test_forward_argument_checks(lib):
+    ws = lib.zs_forward_workspace_bytes(100, 10, 32)
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 2, FAKE, FAKE, ws, None) == UNSUPPORTED
+    assert b"lmax" in lib.zs_last_error()
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, -1, 10, 32, 3, FAKE, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, -1, 32, 3, FAKE, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 0, 3, FAKE, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, None, FAKE, 100, 10, 32, 3, FAKE, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(None, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, None, FAKE, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE, ws - 1, None) == INVALID
+    assert b"workspace" in lib.zs_last_error()
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE + 4, ws, None) == INVALID
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 1 << 31, 10, 32, 3, FAKE, FAKE, 1 << 40, None) == INVALID
+    # N == 0 is valid and enqueues nothing
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 0, 32, 3, None, FAKE, ws, None) == 0
+
+
+def test_backward_argument_checks(lib):
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 4, FAKE, FAKE, None) == UNSUPPORTED
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, -5, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, -3, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward(FAKE, FAKE, FAKE, None, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, None, FAKE, None) == INVALID
+    assert lib.zs_backward(None, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    # E == 0 is valid and enqueues nothing
+    assert lib.zs_backward(None, None, None, None, 0, 10, 32, 3, None, None, None) == 0
+
+
+def test_build_csr_argument_checks(lib):
+    ws = lib.zs_build_csr_workspace_bytes(5000, 100)
+    assert lib.zs_build_csr(FAKE, -1, 100, FAKE, FAKE, None, FAKE, ws, None) == INVALID
+    assert lib.zs_build_csr(FAKE, 5000, -1, FAKE, FAKE, None, FAKE, ws, None) == INVALID
+    assert lib.zs_build_csr(FAKE, 5000, 100, None, FAKE, None, FAKE, ws, None) == INVALID
+    assert lib.zs_build_csr(None, 5000, 100, FAKE, FAKE, None, FAKE, ws, None) == INVALID
+    assert lib.zs_build_csr(FAKE, 5000, 100, FAKE, FAKE, None, FAKE, ws - 1, None) == INVALID
+    assert lib.zs_build_csr(FAKE, 5000, 100, FAKE, FAKE, None, FAKE + 8, ws, None) == INVALID
+    assert lib.zs_build_csr(FAKE, (1 << 31) - 1, 100, FAKE, FAKE, None, FAKE, 1 << 40, None) == INVALID
+
+
+def test_workspace_sizes(lib):
+    assert lib.zs_build_csr_workspace_bytes(0, 10) == 0
+    assert lib.zs_build_csr_workspace_bytes(-1, 10) == 0
+    # four int32 arrays of E plus a 256 x tiles histogram, 256-byte aligned pieces
+    E = 647170
+    tiles = -(-E // 2048)
+    want = 4 * (-(-E * 4 // 256) * 256) + (-(-256 * tiles * 4 // 256) * 256) + 1024
+    assert lib.zs_build_csr_workspace_bytes(E, 4096) == want
+    # forward: a pair of 15 x C partials per 256 CSR positions
+    assert lib.zs_forward_workspace_bytes(E, 4096, 32) == -(-(-(-E // 256) * 2 * 15 * 32 * 4) // 256) * 256
+    assert lib.zs_forward_workspace_bytes(0, 4096, 32) == 2 * 15 * 32 * 4
+    assert lib.zs_forward_workspace_bytes(10, 4096, 0) == 0
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        zs.zs_build_csr(torch.zeros(4, dtype=torch.int32), 3)
