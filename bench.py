@@ -34,7 +34,8 @@ METRIC = "zonal-scatter fwd+bwd edges/s at N=4096,E=647170,C=32; % of HBM roofli
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
     "fwd": "equivariant_interatomic_potential_gb300/csrc/zs_forward.cu",
-    "bwd": "equivariant_interatomic_potential_gb300/csrc/zs_backward.cu",
+    "bwd_csr": "equivariant_interatomic_potential_gb300/csrc/zs_backward.cu",
+    "bwd_edge": "equivariant_interatomic_potential_gb300/csrc/zs_backward.cu",
     "csr": "equivariant_interatomic_potential_gb300/csrc/zs_csr.cu",
 }
 
@@ -188,9 +189,16 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, 3, P(out), P(ws_fwd), fwd_ws_bytes, sp)
         assert st == 0, lib.zs_last_error()
 
-    def bwd():
+    def bwd_edge():
         st = lib.zs_backward(P(g), P(coup), P(rad), P(dst), E, N, C, 3, P(d_coup), P(d_rad), sp)
         assert st == 0, lib.zs_last_error()
+
+    def bwd_csr():
+        st = lib.zs_backward_csr(P(g), P(coup), P(rad), P(row_ptr), P(perm), E, N, C, 3, P(d_coup), P(d_rad), sp)
+        assert st == 0, lib.zs_last_error()
+
+    bwd, bwd_other, other_name = (bwd_csr, bwd_edge, "bwd_edge") if args.backward == "csr" else \
+        (bwd_edge, bwd_csr, "bwd_csr")
 
     passes = max(1, (max(N, 1).bit_length() + 7) // 8) if E > 0 else 0
     launches_per_step = (3 * passes + 1) + 2 + (1 if E > 0 else 0)
@@ -222,6 +230,15 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     total_ms = t0.elapsed_time(t1)
     per = {k: [a.elapsed_time(b) * 1e3 for a, b in ev[k]] for k in ev}   # microseconds
     clock = clocks.summary()
+    # the other backward entry point, timed on its own for comparison
+    oth = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in oth:
+        a.record(stream)
+        bwd_other()
+        b.record(stream)
+    torch.cuda.synchronize()
+    per[other_name] = [a.elapsed_time(b) * 1e3 for a, b in oth]
+    zs.zs_check_timeouts()
 
     # end to end through the public API: pinned host buffers in, results out
     e2e = None
@@ -241,7 +258,10 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
             g.copy_(h_g, non_blocking=True)
             zs.zs_build_csr(dst, N, row_ptr=row_ptr, perm=perm, bad_dst_count=bad, workspace=ws_csr)
             zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
-            zs.zs_backward(g, coup, rad, dst, N, d_coup=d_coup, d_rad=d_rad)
+            if args.backward == "csr":
+                zs.zs_backward_csr(g, coup, rad, row_ptr, perm, N, d_coup=d_coup, d_rad=d_rad)
+            else:
+                zs.zs_backward(g, coup, rad, dst, N, d_coup=d_coup, d_rad=d_rad)
             h_out.copy_(out, non_blocking=True)
             h_dc.copy_(d_coup, non_blocking=True)
             h_dr.copy_(d_rad, non_blocking=True)
@@ -279,17 +299,19 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     ab = algorithmic_bytes(N, E, C)
     peak, peak_kind = measured_peaks()
     kernels = {}
-    for k in ("csr", "fwd", "bwd"):
+    ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
+    for k in ("csr", "fwd", "bwd", other_name):
         us = statistics.mean(per[k])
         gbs = ab[k] / (us * 1e-6) / 1e9
         kernels[k] = {"us_mean": us, "us_median": statistics.median(per[k]), "algorithmic_bytes": ab[k],
                       "GBs": gbs, "frac_of_" + peak_kind: gbs / peak,
                       "edges_per_s": E / (us * 1e-6)}
     dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_mean"])
-    roof = {"kernel": {"fwd": "zs_forward", "bwd": "zs_backward"}[dom], "bound": "hbm",
+    bwd_entry = "zs_backward_csr" if args.backward == "csr" else "zs_backward"
+    roof = {"kernel": {"fwd": "zs_forward", "bwd": bwd_entry}[dom], "bound": "hbm",
             "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
             "frac": kernels[dom]["GBs"] / peak, "peak_kind": peak_kind,
-            "traffic": ncu_traffic(dom, args.config),
+            "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config),
             "algorithmic_bytes_per_launch": ab[dom]}
     ms_per_step = total_ms / args.steps
     fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
@@ -307,7 +329,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": f"{args.config}: N={N}, E={E}, C={C}, lmax=3 (rows 3/5/7), fp32, seed {w.seed}",
-                   "step": "csr_build + forward + backward",
+                   "step": "zs_build_csr + zs_forward + " + bwd_entry,
                    "l2": "inputs larger than L2 (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd_bwd_edges_per_s": E / (fwd_bwd_us * 1e-6),
@@ -360,6 +382,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--config", default="n4096")
     ap.add_argument("--impl", default="zs", choices=["zs", "reference"])
+    ap.add_argument("--backward", default="csr", choices=["csr", "edge"],
+                    help="backward entry point timed in the step (the other is timed alongside)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -10,6 +10,8 @@ from .zs import (  # noqa: F401
     library_path,
     load,
     zs_backward,
+    zs_backward_csr,
+    zs_check_timeouts,
     zs_build_csr,
     zs_build_csr_workspace_bytes,
     zs_forward,

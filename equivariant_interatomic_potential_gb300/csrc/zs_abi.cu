@@ -26,9 +26,22 @@ zs_status check_launch(const char* what) {
     return ZS_OK;
 }
 
+unsigned int take_timeouts_forward();
+unsigned int take_timeouts_backward();
+
 }  // namespace zs
 
 extern "C" {
+
+zs_status zs_check_timeouts(void) {
+    const unsigned int f = zs::take_timeouts_forward();
+    const unsigned int b = zs::take_timeouts_backward();
+    if (f == 0xffffffffu || b == 0xffffffffu)
+        return zs::fail(ZS_ERR_CUDA, "zs_check_timeouts: %s", cudaGetErrorString(cudaGetLastError()));
+    if (f + b) return zs::fail(ZS_ERR_TIMEOUT, "zs_check_timeouts: %u bounded waits ran out", f + b);
+    return ZS_OK;
+}
+
 
 const char* zs_status_string(int status) {
     switch (status) {

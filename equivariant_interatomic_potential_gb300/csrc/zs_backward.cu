@@ -9,6 +9,7 @@
 // coup, rad, dst, d_coup and d_rad stream through HBM contiguously; the only
 // gathered operand is g (N x 16 x C, a few MB, resident in L2).
 #include "zs_common.cuh"
+#include "zs_tma.cuh"
 
 namespace zs {
 namespace {
@@ -123,6 +124,54 @@ bwd_c32(const float* __restrict__ g, const float* __restrict__ coup, const float
 // Per-channel path (any C, any alignment): lane = channel within a chunk of
 // 32; d_coup is reduced over the warp after the channel loop.
 // --------------------------------------------------------------------------
+// Gradients of one edge e whose destination is d (d < 0: no node, zero
+// gradients), lane = channel within chunks of 32.
+__device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const float* __restrict__ coup,
+                                             const float* __restrict__ rad, int64_t e, int d, int C, int lane,
+                                             float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    const bool ok = d >= 0;
+    float cv[15];
+#pragma unroll
+    for (int r = 0; r < 15; ++r) cv[r] = __ldg(coup + e * 15 + r);
+    float pc[15];
+#pragma unroll
+    for (int r = 0; r < 15; ++r) pc[r] = 0.f;
+    const float* rp = rad + e * 3 * C;
+    float* drp = d_rad + e * 3 * C;
+    const float* gn = g + (int64_t)(ok ? d : 0) * 16 * C;
+    for (int c = lane; c < C; c += 32) {
+        if (!ok) {
+            drp[c] = 0.f; drp[C + c] = 0.f; drp[2 * C + c] = 0.f;
+            continue;
+        }
+        const float r0 = __ldg(rp + c), r1 = __ldg(rp + C + c), r2 = __ldg(rp + 2 * C + c);
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int r = 0; r < 15; ++r) {
+            const float gv = __ldg(gn + (1 + r) * C + c);
+            const float rv = r < 3 ? r0 : (r < 8 ? r1 : r2);
+            pc[r] = fmaf(gv, rv, pc[r]);
+            if (r < 3) s0 = fmaf(gv, cv[r], s0);
+            else if (r < 8) s1 = fmaf(gv, cv[r], s1);
+            else s2 = fmaf(gv, cv[r], s2);
+        }
+        drp[c] = s0; drp[C + c] = s1; drp[2 * C + c] = s2;
+    }
+#pragma unroll
+    for (int r = 0; r < 15; ++r) {
+        float v = pc[r];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+        pc[r] = v;
+    }
+    if (lane < 15) {
+        float v = 0.f;
+#pragma unroll
+        for (int r = 0; r < 15; ++r) if (r == lane) v = pc[r];
+        d_coup[e * 15 + lane] = ok ? v : 0.f;
+    }
+}
+
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
         const int32_t* __restrict__ dst, int64_t E, int32_t N, int C,
@@ -130,51 +179,153 @@ bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t e = (int64_t)blockIdx.x * kBwdWarps + warp; e < E; e += (int64_t)gridDim.x * kBwdWarps) {
         const int d = __ldg(dst + e);
-        const bool ok = d >= 0 && d < N;
-        float cv[15];
+        bwd_gen_edge(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad);
+    }
+}
+
+// --------------------------------------------------------------------------
+// CSR-order backward.  The same gradients, with the edges visited in
+// destination order: each warp owns a window of CSR positions, loads the
+// cotangent rows g[n] of a node once into registers and reuses them for all
+// of the node's edges in the window, so g is read about once per node
+// instead of once per edge.  Radial rows and coupling rows arrive through
+// the warp's TMA ring; gradients are written to the edge's own rows.
+// Positions at or after row_ptr[N] hold edges without a node: zeros.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ int first_node_b(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
+    const int n_lb = lower_bound_i32(row_ptr, N + 1, p0);
+    if (n_lb >= 1 && n_lb <= N && (int64_t)__ldg(row_ptr + n_lb) > p0) return n_lb - 1;
+    return n_lb;
+}
+
+template <int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+                const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+                int64_t E, int32_t N, int64_t KW, int Wtot,
+                float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 3, q = lane & 7;
+    const int slo = gq == 0 ? 0 : (gq == 1 ? 1 : 2);
+    const int shi = gq == 0 ? 1 : slo;
+    const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0;
+    const int my_row = 4 * gq + (b2 ? 2 : 0) + (b1 ? 1 : 0);
+    const bool row_writer = (lane & 1) == 0 && my_row < 15;
+    const int gw = blockIdx.x * W + warp;
+    const int64_t p0 = gw < Wtot ? (int64_t)gw * KW : E;
+    const int64_t p1 = gw < Wtot ? imin<int64_t>(p0 + KW, E) : E;
+    TileRing<S> ring;
+    ring.init(smem + (size_t)warp * RingLayout<S>::kBytes, p0, p1, lane);
+    if (gw < Wtot) {
+        ring.prefetch_perm(perm, lane);
 #pragma unroll
-        for (int r = 0; r < 15; ++r) cv[r] = __ldg(coup + e * 15 + r);
-        float pc[15];
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, lane);
+        const int64_t vend = __ldg(row_ptr + N);
+        int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
+        int cur = -1, st = 0;
+        int64_t pos = p0;
+        while (pos < p1) {
+            const bool has_node = pos < vend;
+            int64_t t = p1;
+            float4 gr[4];
+            if (has_node) {
+                while ((int64_t)__ldg(row_ptr + n + 1) <= pos) ++n;
+                t = imin<int64_t>(__ldg(row_ptr + n + 1), p1);
+                const float* gn = g + (int64_t)n * (16 * kC32) + 4 * q;
 #pragma unroll
-        for (int r = 0; r < 15; ++r) pc[r] = 0.f;
-        const float* rp = rad + e * 3 * C;
-        float* drp = d_rad + e * 3 * C;
-        const float* gn = g + (int64_t)(ok ? d : 0) * 16 * C;
-        for (int c = lane; c < C; c += 32) {
-            if (!ok) {
-                drp[c] = 0.f; drp[C + c] = 0.f; drp[2 * C + c] = 0.f;
-                continue;
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * gq + i;
+                    gr[i] = r < 15 ? ld_ro4(gn + (1 + r) * kC32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
-            const float r0 = __ldg(rp + c), r1 = __ldg(rp + C + c), r2 = __ldg(rp + 2 * C + c);
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll
-            for (int r = 0; r < 15; ++r) {
-                const float gv = __ldg(gn + (1 + r) * C + c);
-                const float rv = r < 3 ? r0 : (r < 8 ? r1 : r2);
-                pc[r] = fmaf(gv, rv, pc[r]);
-                if (r < 3) s0 = fmaf(gv, cv[r], s0);
-                else if (r < 8) s1 = fmaf(gv, cv[r], s1);
-                else s2 = fmaf(gv, cv[r], s2);
+            while (pos < t) {
+                const int k = (int)((pos - p0) / kTileEdges);
+                if (k != cur) {
+                    if (cur >= 0) ring.refill(perm, coup, rad, E, lane);
+                    st = ring.acquire();
+                    cur = k;
+                }
+                const int64_t tb = p0 + (int64_t)k * kTileEdges;
+                const int64_t tend = imin<int64_t>(t, tb + kTileEdges);
+                const float* radst = ring.rad + (size_t)st * kTileEdges * 96;
+                const float* coupst = ring.coup + (size_t)st * kTileEdges * kCoupSlotFloats;
+                const int2* metast = ring.meta + st * kTileEdges;
+                const int j1 = (int)(tend - tb);
+#pragma unroll 2
+                for (int j = (int)(pos - tb); j < j1; ++j) {
+                    const int2 m = metast[j];
+                    if (m.x < 0) continue;
+                    const int64_t e = m.x;
+                    if (!has_node) {
+                        if (lane < 24) st_stream4(d_rad + e * (3 * kC32) + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
+                        if (lane < 15) st_stream(d_coup + e * 15 + lane, 0.f);
+                        continue;
+                    }
+                    const float* rrow = radst + j * 96;
+                    const float4 a = *reinterpret_cast<const float4*>(rrow + slo * kC32 + 4 * q);
+                    const float4 bb = *reinterpret_cast<const float4*>(rrow + shi * kC32 + 4 * q);
+                    const float* crow = coupst + j * kCoupSlotFloats + m.y + 4 * gq;
+                    const float4 c4 = make_float4(crow[0], crow[1], crow[2], gq == 3 ? 0.f : crow[3]);
+                    const float p0v = f4_dot(gr[0], a);
+                    const float p1v = f4_dot(gr[1], a);
+                    const float p2v = f4_dot(gr[2], a);
+                    const float p3v = f4_dot(gr[3], bb);
+                    const float x0 = b2 ? p0v : p2v, x1 = b2 ? p1v : p3v;
+                    const float k0 = (b2 ? p2v : p0v) + __shfl_xor_sync(kFull, x0, 4);
+                    const float k1 = (b2 ? p3v : p1v) + __shfl_xor_sync(kFull, x1, 4);
+                    float mm = (b1 ? k1 : k0) + __shfl_xor_sync(kFull, b1 ? k0 : k1, 2);
+                    mm += __shfl_xor_sync(kFull, mm, 1);
+                    if (row_writer) st_stream(d_coup + e * 15 + my_row, mm);
+                    float4 lo = make_float4(c4.x * gr[0].x, c4.x * gr[0].y, c4.x * gr[0].z, c4.x * gr[0].w);
+                    lo = f4_fma(c4.y, gr[1], lo);
+                    lo = f4_fma(c4.z, gr[2], lo);
+                    const float4 hi = make_float4(c4.w * gr[3].x, c4.w * gr[3].y, c4.w * gr[3].z, c4.w * gr[3].w);
+                    const float4 both = f4_add(lo, hi);
+                    const float4 y = f4_shfl_xor(gq == 0 ? hi : both, 8);
+                    if (gq < 3) {
+                        const float4 res = gq == 0 ? lo : (gq == 1 ? f4_add(y, both) : f4_add(both, y));
+                        st_stream4(d_rad + e * (3 * kC32) + gq * kC32 + 4 * q, res);
+                    }
+                }
+                pos = tend;
             }
-            drp[c] = s0; drp[C + c] = s1; drp[2 * C + c] = s2;
+            if (has_node) ++n;
         }
-#pragma unroll
-        for (int r = 0; r < 15; ++r) {
-            float v = pc[r];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-            pc[r] = v;
+    }
+    ring.drain();
+}
+
+// Per-channel CSR-order backward (any C, any alignment): same walk, no TMA.
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+            const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+            int64_t E, int32_t N, int C, int64_t KW, int Wtot,
+            float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kBwdWarps + warp;
+    if (gw >= Wtot) return;
+    const int64_t p0 = (int64_t)gw * KW;
+    const int64_t p1 = imin<int64_t>(p0 + KW, E);
+    const int64_t vend = __ldg(row_ptr + N);
+    int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
+    for (int64_t pos = p0; pos < p1; ++pos) {
+        int d = -1;
+        if (pos < vend) {
+            while ((int64_t)__ldg(row_ptr + n + 1) <= pos) ++n;
+            d = n;
         }
-        if (lane < 15) {
-            float v = 0.f;
-#pragma unroll
-            for (int r = 0; r < 15; ++r) if (r == lane) v = pc[r];
-            d_coup[e * 15 + lane] = ok ? v : 0.f;
-        }
+        const int e = __ldg(perm + pos);
+        if ((uint32_t)e >= (uint64_t)E) continue;
+        bwd_gen_edge(g, coup, rad, e, d, C, lane, d_coup, d_rad);
     }
 }
 
 }  // namespace
+
+unsigned int take_timeouts_backward() { return take_timeouts_local(); }
+
 }  // namespace zs
 
 using namespace zs;
@@ -201,4 +352,41 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
         bwd_gen<<<grid, kBwdThreads, 0, s>>>(g, coup, rad, dst, E, N, C, d_coup, d_rad);
     }
     return check_launch("zs_backward");
+}
+
+extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const float* rad,
+                                     const int32_t* row_ptr, const int32_t* perm,
+                                     int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                     float* d_coup, float* d_rad, zs_stream_t stream) {
+    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_backward_csr: lmax=%d, only lmax=3 (row groups 3/5/7) is supported", lmax);
+    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: E=%lld exceeds the int32 index range", (long long)E);
+    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: row_ptr is NULL");
+    if (E == 0) return ZS_OK;
+    if (!coup || !rad || !perm || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: NULL array with E > 0");
+    if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: g is NULL with N > 0");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
+    if (fast) {
+        constexpr int W = 7, S = 2;
+        const int64_t warps_max = (int64_t)num_sms() * W;
+        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max, kTileEdges);
+        const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
+        const int64_t ctas = (Wtot + W - 1) / W;
+        const int smem = W * RingLayout<S>::kBytes;
+        static bool attr_set = false;
+        if (!attr_set) {
+            cudaFuncSetAttribute(bwd_csr_c32_tma<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            attr_set = true;
+        }
+        bwd_csr_c32_tma<W, S><<<(unsigned)ctas, W * 32, smem, s>>>(g, coup, rad, row_ptr, perm, E, N, KW, (int)Wtot,
+                                                                     d_coup, d_rad);
+    } else {
+        const int64_t KW = 64;
+        const int64_t Wtot = (E + KW - 1) / KW;
+        const int64_t ctas = (Wtot + kBwdWarps - 1) / kBwdWarps;
+        bwd_csr_gen<<<(unsigned)ctas, kBwdThreads, 0, s>>>(g, coup, rad, row_ptr, perm, E, N, C, KW, (int)Wtot,
+                                                            d_coup, d_rad);
+    }
+    return check_launch("zs_backward_csr");
 }

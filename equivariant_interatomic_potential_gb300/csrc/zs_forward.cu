@@ -20,14 +20,15 @@
 // Every sum is therefore formed in one fixed order: run to run bitwise
 // deterministic, no floating-point atomics.
 #include "zs_common.cuh"
+#include "zs_tma.cuh"
 
 namespace zs {
 namespace {
 
 constexpr int kFwdWarps = 8;
 constexpr int kFwdThreads = kFwdWarps * 32;
-constexpr int kSubWin = 256;                   // CSR positions per warp
-constexpr int kCtaWin = kFwdWarps * kSubWin;   // CSR positions per CTA (C == 32 path)
+constexpr int kTmaWarps = 7;                   // warps per CTA of the C == 32 path (one CTA per SM)
+constexpr int kTmaStages = 2;                  // tiles of 32 edges per warp ring
 constexpr int kGenWin = 256;                   // CSR positions per warp (per-channel path)
 constexpr int kC32 = 32;
 constexpr int kNodeFloats32 = kD * kC32;       // 512 floats per node at C = 32
@@ -48,52 +49,6 @@ struct Lane32 {
         src_hi = g == 0 ? lane + 8 : lane;
     }
 };
-
-// Sum the messages of CSR positions [s, t) into acc (rows 4g..4g+3, channels 4q..4q+3).
-__device__ __forceinline__ void accumulate32(const float* __restrict__ coup, const float* __restrict__ rad,
-                                             const int32_t* __restrict__ perm, int64_t E,
-                                             int s, int t, float (*cs)[16], const Lane32& L, float4 acc[4]) {
-    const float* radq = rad + L.slo * kC32 + 4 * L.q;
-    for (int base = s; base < t; base += 32) {
-        const int cnt = min(32, t - base);
-        int e_l = -1;
-        if (L.lane < cnt) {
-            e_l = ld_stream_i(perm + base + L.lane);
-            if ((uint32_t)e_l >= (uint64_t)E) e_l = -1;   // malformed perm: contributes nothing
-        }
-        // Stage the 32 coupling rows (15 floats each) into shared memory.
-#pragma unroll
-        for (int it = 0; it < kRows; ++it) {
-            const int v = it * 32 + L.lane;
-            const int j = v / kRows;
-            const int r = v - j * kRows;
-            const int e = __shfl_sync(kFull, e_l, j);
-            float c = 0.f;
-            if (j < cnt && e >= 0) c = __ldg(coup + (int64_t)e * kRows + r);
-            cs[j][r] = c;
-        }
-        __syncwarp();
-        for (int j0 = 0; j0 < cnt; j0 += 8) {
-            float4 a[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = __shfl_sync(kFull, e_l, j0 + u);
-                a[u] = (j0 + u < cnt && e >= 0) ? ld_stream4(radq + (int64_t)e * (kSlots * kC32))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float4 b = f4_shfl(a[u], L.src_hi);
-                const float4 c4 = *reinterpret_cast<const float4*>(&cs[j0 + u][4 * L.g]);
-                acc[0] = f4_fma(c4.x, a[u], acc[0]);
-                acc[1] = f4_fma(c4.y, a[u], acc[1]);
-                acc[2] = f4_fma(c4.z, a[u], acc[2]);
-                acc[3] = f4_fma(c4.w, b, acc[3]);
-            }
-        }
-        __syncwarp();
-    }
-}
 
 // Write rows 1..15 of one node from acc, and the zero scalar row.
 __device__ __forceinline__ void store_node32(float* __restrict__ node, const float4 acc[4], const Lane32& L) {
@@ -128,6 +83,28 @@ __device__ __forceinline__ void zero_node32(float* __restrict__ node, int lane) 
         *reinterpret_cast<float4*>(node + 4 * (lane + 32 * k)) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Add the messages of the edges at tile positions [j0, j1) of stage st.
+template <int S>
+__device__ __forceinline__ void accumulate_tile32(const TileRing<S>& ring, int st, int j0, int j1,
+                                                  const Lane32& L, int shi, float4 acc[4]) {
+    const float* radst = ring.rad + (size_t)st * kTileEdges * 96;
+    const float* coupst = ring.coup + (size_t)st * kTileEdges * kCoupSlotFloats;
+    const int2* metast = ring.meta + st * kTileEdges;
+#pragma unroll 4
+    for (int j = j0; j < j1; ++j) {
+        const int2 m = metast[j];
+        if (m.x < 0) continue;
+        const float* rrow = radst + j * 96;
+        const float4 a = *reinterpret_cast<const float4*>(rrow + L.slo * kC32 + 4 * L.q);
+        const float4 b = *reinterpret_cast<const float4*>(rrow + shi * kC32 + 4 * L.q);
+        const float* crow = coupst + j * kCoupSlotFloats + m.y + 4 * L.g;
+        acc[0] = f4_fma(crow[0], a, acc[0]);
+        acc[1] = f4_fma(crow[1], a, acc[1]);
+        acc[2] = f4_fma(crow[2], a, acc[2]);
+        acc[3] = f4_fma(crow[3], b, acc[3]);   // row 15 of group 3 is padding, never stored
+    }
+}
+
 // First node to visit for window [p0, ...): the node containing p0 when it
 // starts before p0, else the first node starting at or after p0.
 __device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
@@ -136,69 +113,101 @@ __device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, i
     return n_lb;
 }
 
-__global__ void __launch_bounds__(kFwdThreads)
-fwd_c32_main(const float* __restrict__ coup, const float* __restrict__ rad,
-             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-             int64_t E, int32_t N, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
-    __shared__ __align__(16) float cs[kFwdWarps][32][16];
-    __shared__ __align__(16) float sp[kFwdWarps][2][kPartFloats32];
-    __shared__ int sp_node[kFwdWarps][2];
+// C == 32 forward with TMA-fed warps.  W warps per CTA, one CTA per SM, each
+// warp owns the window [gw*KW, gw*KW + KW) of CSR positions.
+template <int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
+            const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+            int64_t E, int32_t N, int64_t KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int sp_node[W][2];
     const int warp = threadIdx.x >> 5;
     const Lane32 L(threadIdx.x & 31);
-    const int gw = blockIdx.x * kFwdWarps + warp;
-    cs[warp][L.lane][15] = 0.f;
+    const int shi = L.g == 0 ? 1 : L.slo;
+    const int gw = blockIdx.x * W + warp;
+    const int64_t p0 = gw < Wtot ? (int64_t)gw * KW : E;
+    const int64_t p1 = gw < Wtot ? imin<int64_t>(p0 + KW, E) : E;
+    TileRing<S> ring;
+    ring.init(smem + (size_t)warp * RingLayout<S>::kBytes, p0, p1, L.lane);
     if (L.lane < 2) sp_node[warp][L.lane] = -1;
     __syncwarp();
 
+    float4 acc0[4] = {}, acc[4] = {};
+    bool have0 = false, have1 = false;
     if (gw < Wtot) {
-        const int64_t p0 = (int64_t)gw * kSubWin;
-        const int64_t p1 = min(p0 + kSubWin, E);
+        ring.prefetch_perm(perm, L.lane);
+#pragma unroll
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, L.lane);
         const bool is_last = gw == Wtot - 1;
+        int cur = -1, st = 0;
         for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
             const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
             if (a >= p1 && !(is_last && a == b)) break;
-            if (a == b) {                       // no edges: an all-zero node
+            if (a == b) {
                 zero_node32(out + (int64_t)n * kNodeFloats32, L.lane);
                 continue;
             }
-            float4 acc[4] = {};
-            accumulate32(coup, rad, perm, E, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1), cs[warp], L, acc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int64_t pos = imax<int64_t>(a, p0);
+            const int64_t t = imin<int64_t>(b, p1);
+            while (pos < t) {
+                const int k = (int)((pos - p0) / kTileEdges);
+                if (k != cur) {
+                    if (cur >= 0) ring.refill(perm, coup, rad, E, L.lane);
+                    st = ring.acquire();
+                    cur = k;
+                }
+                const int64_t tb = p0 + (int64_t)k * kTileEdges;
+                const int64_t tend = imin<int64_t>(t, tb + kTileEdges);
+                accumulate_tile32(ring, st, (int)(pos - tb), (int)(tend - tb), L, shi, acc);
+                pos = tend;
+            }
             if (a >= p0 && b <= p1) {
                 store_node32(out + (int64_t)n * kNodeFloats32, acc, L);
+            } else if (a < p0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
+                have0 = true;
+                if (L.lane == 0) sp_node[warp][0] = n;
             } else {
-                const int slot = a < p0 ? 0 : 1;
-                store_part32(sp[warp][slot], acc, L);
-                if (L.lane == 0) sp_node[warp][slot] = n;
+                have1 = true;
+                if (L.lane == 0) sp_node[warp][1] = n;
             }
             if (b > p1) break;
         }
     }
+    ring.drain();
+    // The ring is idle: its radial area holds this warp's two partials.
+    float* part = ring.rad;
+    if (have0) store_part32(part, acc0, L);
+    if (have1) store_part32(part + kPartFloats32, acc, L);
     __syncthreads();
 
-    // Combine the warp pieces of nodes cut by window edges inside this CTA.
-    // The lowest warp holding a piece of node m adds the pieces in window order.
-    const int64_t P0 = (int64_t)blockIdx.x * kCtaWin;
-    const int64_t P1 = min(P0 + kCtaWin, E);
+    // Combine the warp pieces of nodes cut by window edges inside this CTA:
+    // the lowest warp holding a piece of node m adds them in window order.
+    const int64_t P0 = imin<int64_t>((int64_t)blockIdx.x * W * KW, E);
+    const int64_t P1 = imin<int64_t>(P0 + (int64_t)W * KW, E);
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot) {
         const int m = sp_node[warp][slot];
         if (m < 0) continue;
         if (warp > 0 && (sp_node[warp - 1][0] == m || sp_node[warp - 1][1] == m)) continue;
-        if (slot == 0 && sp_node[warp][1] == m) continue;  // cannot happen; keeps one leader per node
-        float4 acc[4];
-        load_part32(sp[warp][slot], acc, L);
-        for (int w2 = warp + 1; w2 < kFwdWarps && sp_node[w2][0] == m; ++w2) {
-            float4 t[4];
-            load_part32(sp[w2][0], t, L);
+        float4 sum[4];
+        load_part32(part + slot * kPartFloats32, sum, L);
+        for (int w2 = warp + 1; w2 < W && sp_node[w2][0] == m; ++w2) {
+            float4 t4[4];
+            load_part32(reinterpret_cast<const float*>(smem + (size_t)w2 * RingLayout<S>::kBytes), t4, L);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = f4_add(acc[i], t[i]);
+            for (int i = 0; i < 4; ++i) sum[i] = f4_add(sum[i], t4[i]);
         }
         const int a = __ldg(row_ptr + m), b = __ldg(row_ptr + m + 1);
         if (a >= P0 && b <= P1) {
-            store_node32(out + (int64_t)m * kNodeFloats32, acc, L);
+            store_node32(out + (int64_t)m * kNodeFloats32, sum, L);
         } else {
             const int cslot = a < P0 ? 0 : 1;
-            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + cslot) * kPartFloats32, acc, L);
+            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + cslot) * kPartFloats32, sum, L);
         }
     }
 }
@@ -345,6 +354,9 @@ fwd_fixup(const int32_t* __restrict__ row_ptr, int32_t N, int C, int win,
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
+
+unsigned int take_timeouts_forward() { return take_timeouts_local(); }
+
 }  // namespace zs
 
 using namespace zs;
@@ -352,9 +364,10 @@ using namespace zs;
 extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
     if (E < 0 || N < 0 || C < 1) return 0;
     (void)N;
-    // Sized for the per-channel path (one partial pair per 256 positions),
-    // which also covers the C == 32 path (one pair per 2048 positions).
-    const int64_t windows = ceil_div(E > 0 ? E : 1, kGenWin);
+    // One pair of (15 x C) partials per window: per warp window of kGenWin
+    // positions on the per-channel path, per CTA window of at least
+    // kTmaWarps * 32 positions on the C == 32 path.
+    const int64_t windows = ceil_div(E > 0 ? E : 1, imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTileEdges)) + 1;
     return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256);
 }
 
@@ -376,13 +389,24 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
     if (N == 0) return ZS_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float* part = static_cast<float*>(workspace);
-    const bool fast = C == kC32 && aligned16(rad) && aligned16(out);
+    const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
     const int fix_grid = (int)imin<int64_t>(N, (int64_t)num_sms() * 8);
     if (fast) {
-        const int64_t Wtot = ceil_div(E > 0 ? E : 1, kSubWin);
-        const int64_t ctas = ceil_div(Wtot, kFwdWarps);
-        fwd_c32_main<<<(unsigned)ctas, kFwdThreads, 0, s>>>(coup, rad, row_ptr, perm, E, N, (int)Wtot, out, part);
-        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, kCtaWin, part, out);
+        // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
+        // the same number of CSR positions (at least one tile).
+        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
+        const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTileEdges);
+        const int64_t Wtot = imax<int64_t>(ceil_div(E, KW), 1);
+        const int64_t ctas = ceil_div(Wtot, kTmaWarps);
+        const int smem = kTmaWarps * RingLayout<kTmaStages>::kBytes;
+        static bool attr_set = false;
+        if (!attr_set) {
+            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            attr_set = true;
+        }
+        fwd_c32_tma<kTmaWarps, kTmaStages><<<(unsigned)ctas, kTmaWarps * 32, smem, s>>>(
+            coup, rad, row_ptr, perm, E, N, KW, (int)Wtot, out, part);
+        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, (int)(KW * kTmaWarps), part, out);
     } else {
         const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
         const int64_t ctas = ceil_div(Wtot, kFwdWarps);

@@ -61,6 +61,10 @@ def load(build_if_missing: bool = True):
         lib.zs_forward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
         lib.zs_backward.restype = ctypes.c_int
         lib.zs_backward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P]
+        lib.zs_backward_csr.restype = ctypes.c_int
+        lib.zs_backward_csr.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P]
+        lib.zs_check_timeouts.restype = ctypes.c_int
+        lib.zs_check_timeouts.argtypes = []
         _lib = lib
         return lib
 
@@ -177,3 +181,28 @@ def zs_backward(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: tor
     _check("zs_backward", load().zs_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C, lmax,
                                              _ptr(d_coup), _ptr(d_rad), _stream(stream)))
     return d_coup, d_rad
+
+
+def zs_backward_csr(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor,
+                    perm: torch.Tensor, N: int, d_coup=None, d_rad=None, stream=None, lmax: int = 3):
+    """Backward with edges visited in CSR order.  Returns (d_coup (E, 15), d_rad (E, 3, C)) fp32."""
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(g, "g", torch.float32, (N, 16, C))
+    _need(coup, "coup", torch.float32, (E, 15))
+    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev) if d_coup is None else d_coup
+    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_coup, "d_coup", torch.float32, (E, 15))
+    _need(d_rad, "d_rad", torch.float32, (E, 3, C))
+    _check("zs_backward_csr", load().zs_backward_csr(_ptr(g), _ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm),
+                                                     E, N, C, lmax, _ptr(d_coup), _ptr(d_rad), _stream(stream)))
+    return d_coup, d_rad
+
+
+def zs_check_timeouts() -> None:
+    """Raise ZsError if a bounded device wait ran out since the last check (synchronises)."""
+    _check("zs_check_timeouts", load().zs_check_timeouts())

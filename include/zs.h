@@ -69,7 +69,7 @@ typedef enum zs_status {
     ZS_ERR_INVALID_ARG = 1,  /* null pointer with nonzero size, negative size, E >= 2^31, C < 1, workspace too small */
     ZS_ERR_UNSUPPORTED = 2,  /* lmax != 3 */
     ZS_ERR_CUDA = 3,         /* a CUDA call or launch failed; zs_last_error() has the message */
-    ZS_ERR_TIMEOUT = 4       /* reserved: a bounded device wait ran out (no current kernel waits) */
+    ZS_ERR_TIMEOUT = 4       /* a bounded device wait ran out (see zs_check_timeouts) */
 } zs_status;
 
 /* Static, human-readable name of a status code. */
@@ -141,6 +141,36 @@ ZS_API zs_status zs_forward(const float* coup, const float* rad,
 ZS_API zs_status zs_backward(const float* g, const float* coup, const float* rad,
                       const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
                       float* d_coup, float* d_rad, zs_stream_t stream);
+
+/*
+ * Backward of the zonal scatter with the edges visited in destination (CSR)
+ * order: the same d_coup and d_rad as zs_backward, written for every edge,
+ * for callers that already hold the forward's CSR.  Each node's cotangent
+ * rows g[n] are read once per run of its edges instead of once per edge.
+ *   g (N,16,C), coup (E,15), rad (E,3,C)  as for zs_backward
+ *   row_ptr (N+1,), perm (E,)             the CSR zs_build_csr returned for
+ *                                         the edges' destinations; perm must
+ *                                         be a permutation of [0, E)
+ *   d_coup (E,15), d_rad (E,3,C)          outputs, fully written; edges at
+ *                                         positions >= row_ptr[N] (no node)
+ *                                         get zero gradients
+ * Needs no workspace.  The per-edge arithmetic is the same as zs_backward's,
+ * so both entry points return bitwise-equal gradients on the C == 32 path.
+ */
+ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float* rad,
+                                 const int32_t* row_ptr, const int32_t* perm,
+                                 int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                 float* d_coup, float* d_rad, zs_stream_t stream);
+
+/*
+ * Reads and clears the device-side count of bounded waits that ran out.
+ * The kernels that stream operands with asynchronous bulk copies wait for
+ * them with an iteration limit; a wait that reaches its limit is counted
+ * and the kernel returns instead of hanging the GPU (its outputs are then
+ * undefined).  Synchronises the device.  Returns ZS_ERR_TIMEOUT when any
+ * wait ran out since the previous call, ZS_OK otherwise.
+ */
+ZS_API zs_status zs_check_timeouts(void);
 
 #ifdef __cplusplus
 }

@@ -30,8 +30,11 @@ def run_gpu(w, *, backward=True):
     if backward:
         g = dev(w.grad_out)
         d_coup, d_rad = zs.zs_backward(g, coup, rad, dst, w.N)
-        res.update(d_coup=d_coup.cpu().numpy(), d_rad=d_rad.cpu().numpy())
+        c_coup, c_rad = zs.zs_backward_csr(g, coup, rad, row_ptr, perm, w.N)
+        res.update(d_coup=d_coup.cpu().numpy(), d_rad=d_rad.cpu().numpy(),
+                   csr_d_coup=c_coup.cpu().numpy(), csr_d_rad=c_rad.cpu().numpy())
     torch.cuda.synchronize()
+    zs.zs_check_timeouts()
     return res
 
 
@@ -63,9 +66,14 @@ def check_forward(w, res, row_ptr, perm, nodes=None):
 
 
 def check_backward(w, res, edges=None):
+    """Both backward entry points against the oracle (on the sampled edges)."""
     dc, dr, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N, edges=edges)
-    gdc = res["d_coup"] if edges is None else res["d_coup"][edges]
-    gdr = res["d_rad"] if edges is None else res["d_rad"][edges]
-    e1 = assert_close(gdc, dc, adc, "d_coup")
-    e2 = assert_close(gdr, dr, adr, "d_rad")
-    return e1, e2
+    errs = []
+    for pre in ("", "csr_"):
+        if pre + "d_coup" not in res:
+            continue
+        gdc = res[pre + "d_coup"] if edges is None else res[pre + "d_coup"][edges]
+        gdr = res[pre + "d_rad"] if edges is None else res[pre + "d_rad"][edges]
+        errs.append(assert_close(gdc, dc, adc, pre + "d_coup"))
+        errs.append(assert_close(gdr, dr, adr, pre + "d_rad"))
+    return errs

@@ -19,8 +19,9 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = zs.declared_functions()
-    for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_build_csr_workspace_bytes",
-               "zs_forward_workspace_bytes", "zs_status_string", "zs_last_error", "zs_version"):
+    for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_backward_csr", "zs_build_csr_workspace_bytes",
+               "zs_forward_workspace_bytes", "zs_status_string", "zs_last_error", "zs_version",
+               "zs_check_timeouts"):
         assert fn in names
 
 
@@ -82,6 +83,16 @@ def test_backward_argument_checks(lib):
     assert lib.zs_backward(None, None, None, None, 0, 10, 32, 3, None, None, None) == 0
 
 
+def test_backward_csr_argument_checks(lib):
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 1, FAKE, FAKE, None) == UNSUPPORTED
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, None, FAKE, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, None, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward_csr(None, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, None, None) == INVALID
+    assert lib.zs_backward_csr(None, None, None, FAKE, None, 0, 10, 32, 3, None, None, None) == 0
+
+
 def test_build_csr_argument_checks(lib):
     ws = lib.zs_build_csr_workspace_bytes(5000, 100)
     assert lib.zs_build_csr(FAKE, -1, 100, FAKE, FAKE, None, FAKE, ws, None) == INVALID
@@ -101,9 +112,9 @@ def test_workspace_sizes(lib):
     tiles = -(-E // 2048)
     want = 4 * (-(-E * 4 // 256) * 256) + (-(-256 * tiles * 4 // 256) * 256) + 1024
     assert lib.zs_build_csr_workspace_bytes(E, 4096) == want
-    # forward: a pair of 15 x C partials per 256 CSR positions
-    assert lib.zs_forward_workspace_bytes(E, 4096, 32) == -(-(-(-E // 256) * 2 * 15 * 32 * 4) // 256) * 256
-    assert lib.zs_forward_workspace_bytes(0, 4096, 32) == 2 * 15 * 32 * 4
+    # forward: a pair of 15 x C partials per window of at least 224 CSR positions, plus one
+    assert lib.zs_forward_workspace_bytes(E, 4096, 32) == -(-((-(-E // 224) + 1) * 2 * 15 * 32 * 4) // 256) * 256
+    assert lib.zs_forward_workspace_bytes(0, 4096, 32) == 2 * 2 * 15 * 32 * 4
     assert lib.zs_forward_workspace_bytes(10, 4096, 0) == 0
 
 

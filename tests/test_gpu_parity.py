@@ -204,7 +204,8 @@ def test_bitwise_deterministic(name):
         row_ptr, perm, _ = zs.zs_build_csr(dst, w.N)
         out = zs.zs_forward(coup, rad, row_ptr, perm, w.N)
         d_coup, d_rad = zs.zs_backward(g, coup, rad, dst, w.N)
-        cur = [t.clone() for t in (row_ptr, perm, out, d_coup, d_rad)]
+        c_coup, c_rad = zs.zs_backward_csr(g, coup, rad, row_ptr, perm, w.N)
+        cur = [t.clone() for t in (row_ptr, perm, out, d_coup, d_rad, c_coup, c_rad)]
         if ref is None:
             ref = cur
         else:
@@ -218,7 +219,7 @@ def test_inputs_untouched_and_guard_bands(C):
     w = workloads.make_workload("zipf") if C == 32 else workloads.make_random(500, 60000, C, seed=12)
     E, N = w.E, w.N
     G = 4096
-    canary = -7.25e33
+    canary = -1.75 * 2.0 ** 100   # exactly representable in fp32
 
     def banded(n, dtype):
         buf = torch.full((n + 2 * G,), canary, device="cuda").to(dtype) if dtype == torch.float32 else \
@@ -279,3 +280,16 @@ def test_streams_are_honoured():
     rp, pm = check_csr(w, res)
     check_forward(w, res, rp, pm)
     check_backward(w, res)
+
+
+@pytest.mark.parametrize("name", ["n4096", "zipf"])
+def test_backward_variants_bitwise_equal(name):
+    # the edge-order and CSR-order backward do the same per-edge arithmetic
+    w = workloads.make_workload(name)
+    dst, coup, rad, g = dev(w.dst), dev(w.coup), dev(w.rad), dev(w.grad_out)
+    row_ptr, perm, _ = zs.zs_build_csr(dst, w.N)
+    a = zs.zs_backward(g, coup, rad, dst, w.N)
+    b = zs.zs_backward_csr(g, coup, rad, row_ptr, perm, w.N)
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    zs.zs_check_timeouts()
