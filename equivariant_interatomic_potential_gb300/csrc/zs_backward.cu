@@ -15,6 +15,16 @@ namespace zs {
 namespace {
 
 constexpr int kBwdWarps = 8;
+// CSR-order C == 32 path: warps per CTA (one CTA per SM), ring stages, edges per tile.
+#ifndef ZS_BWD_WARPS
+#define ZS_BWD_WARPS 14
+#endif
+#ifndef ZS_BWD_STAGES
+#define ZS_BWD_STAGES 2
+#endif
+#ifndef ZS_BWD_TILE
+#define ZS_BWD_TILE 16
+#endif
 constexpr int kBwdThreads = kBwdWarps * 32;
 constexpr int kC32 = 32;
 constexpr unsigned kFull = 0xffffffffu;
@@ -39,6 +49,8 @@ bwd_c32(const float* __restrict__ g, const float* __restrict__ coup, const float
     const bool row_writer = (lane & 1) == 0 && my_row < 15;
     cs[warp][lane][15] = 0.f;
     __syncwarp();
+    pdl_wait();
+    pdl_trigger();
 
     const int64_t nbatch = (E + 31) / 32;
     for (int64_t bt = (int64_t)blockIdx.x * kBwdWarps + warp; bt < nbatch; bt += (int64_t)gridDim.x * kBwdWarps) {
@@ -177,6 +189,8 @@ bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float
         const int32_t* __restrict__ dst, int64_t E, int32_t N, int C,
         float* __restrict__ d_coup, float* __restrict__ d_rad) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     for (int64_t e = (int64_t)blockIdx.x * kBwdWarps + warp; e < E; e += (int64_t)gridDim.x * kBwdWarps) {
         const int d = __ldg(dst + e);
         bwd_gen_edge(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad);
@@ -199,99 +213,124 @@ __device__ __forceinline__ int first_node_b(const int32_t* __restrict__ row_ptr,
     return n_lb;
 }
 
-template <int W, int S>
+// Gradients of the edge at tile slot j, whose node's cotangent rows are in
+// gr (rows 4g..4g+3 of this lane's group, channels 4q..4q+3).
+struct BwdLane {
+    int lane, gq, q, slo, shi, my_row;
+    bool b2, b1, row_writer;
+    __device__ __forceinline__ explicit BwdLane(int l) : lane(l), gq(l >> 3), q(l & 7) {
+        slo = gq == 0 ? 0 : (gq == 1 ? 1 : 2);
+        shi = gq == 0 ? 1 : slo;
+        b2 = (lane & 4) != 0;
+        b1 = (lane & 2) != 0;
+        my_row = 4 * gq + (b2 ? 2 : 0) + (b1 ? 1 : 0);
+        row_writer = (lane & 1) == 0 && my_row < 15;
+    }
+};
+
+template <int S, int T>
+__device__ __forceinline__ void bwd_edge32(const TileRing<S, T>& ring, int st, int j, const float4 gr[4],
+                                           const BwdLane& B, float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    const int2 m = ring.meta[st * T + j];
+    const float* rrow = ring.rad + (st * T + j) * 96;
+    const float4 a = *reinterpret_cast<const float4*>(rrow + B.slo * kC32 + 4 * B.q);
+    const float4 bb = *reinterpret_cast<const float4*>(rrow + B.shi * kC32 + 4 * B.q);
+    const float* crow = ring.coup + (st * T + j) * kCoupSlotFloats + m.y + 4 * B.gq;
+    const float4 c4 = make_float4(crow[0], crow[1], crow[2], B.gq == 3 ? 0.f : crow[3]);
+    // d_coup: four row dot products over this lane's 4 channels, then a
+    // transposed butterfly over the 8 lanes of the group
+    const float p0v = f4_dot(gr[0], a);
+    const float p1v = f4_dot(gr[1], a);
+    const float p2v = f4_dot(gr[2], a);
+    const float p3v = f4_dot(gr[3], bb);
+    const float x0 = B.b2 ? p0v : p2v, x1 = B.b2 ? p1v : p3v;
+    const float k0 = (B.b2 ? p2v : p0v) + __shfl_xor_sync(kFull, x0, 4);
+    const float k1 = (B.b2 ? p3v : p1v) + __shfl_xor_sync(kFull, x1, 4);
+    float mm = (B.b1 ? k1 : k0) + __shfl_xor_sync(kFull, B.b1 ? k0 : k1, 2);
+    mm += __shfl_xor_sync(kFull, mm, 1);
+    // d_rad: the group's rows weighted by their coupling; the degree-2 slot
+    // adds group 0's row 3, the degree-3 slot adds group 3's rows
+    float4 lo = make_float4(c4.x * gr[0].x, c4.x * gr[0].y, c4.x * gr[0].z, c4.x * gr[0].w);
+    lo = f4_fma(c4.y, gr[1], lo);
+    lo = f4_fma(c4.z, gr[2], lo);
+    const float4 hi = make_float4(c4.w * gr[3].x, c4.w * gr[3].y, c4.w * gr[3].z, c4.w * gr[3].w);
+    const float4 both = f4_add(lo, hi);
+    const float4 y = f4_shfl_xor(B.gq == 0 ? hi : both, 8);
+    if (m.x < 0) return;
+    const int64_t e = m.x;
+    if (B.row_writer) st_stream(d_coup + e * 15 + B.my_row, mm);
+    if (B.gq < 3) {
+        const float4 res = B.gq == 0 ? lo : (B.gq == 1 ? f4_add(y, both) : f4_add(both, y));
+        st_stream4(d_rad + e * (3 * kC32) + B.gq * kC32 + 4 * B.q, res);
+    }
+}
+
+template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
                 const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-                int64_t E, int32_t N, int64_t KW, int Wtot,
+                int E, int32_t N, int KW, int Wtot,
                 float* __restrict__ d_coup, float* __restrict__ d_rad) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 3, q = lane & 7;
-    const int slo = gq == 0 ? 0 : (gq == 1 ? 1 : 2);
-    const int shi = gq == 0 ? 1 : slo;
-    const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0;
-    const int my_row = 4 * gq + (b2 ? 2 : 0) + (b1 ? 1 : 0);
-    const bool row_writer = (lane & 1) == 0 && my_row < 15;
+    const int warp = threadIdx.x >> 5;
+    const BwdLane B(threadIdx.x & 31);
     const int gw = blockIdx.x * W + warp;
-    const int64_t p0 = gw < Wtot ? (int64_t)gw * KW : E;
-    const int64_t p1 = gw < Wtot ? imin<int64_t>(p0 + KW, E) : E;
-    TileRing<S> ring;
-    ring.init(smem + (size_t)warp * RingLayout<S>::kBytes, p0, p1, lane);
-    if (gw < Wtot) {
-        ring.prefetch_perm(perm, lane);
+    const bool active = gw < Wtot;
+    pdl_wait();
+    pdl_trigger();
+    const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
+    const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
+    TileRing<S, T> ring;
+    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, B.lane);
+    if (active) {
+        ring.prefetch_perm(perm, B.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, lane);
-        const int64_t vend = __ldg(row_ptr + N);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, B.lane);
+        const int vend = __ldg(row_ptr + N);
         int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
-        int cur = -1, st = 0;
-        int64_t pos = p0;
-        while (pos < p1) {
-            const bool has_node = pos < vend;
-            int64_t t = p1;
-            float4 gr[4];
-            if (has_node) {
-                while ((int64_t)__ldg(row_ptr + n + 1) <= pos) ++n;
-                t = imin<int64_t>(__ldg(row_ptr + n + 1), p1);
-                const float* gn = g + (int64_t)n * (16 * kC32) + 4 * q;
+        int b = 0;
+        float4 gr[4] = {};
+        auto enter = [&](int pos) {   // make node n the one holding position pos < vend
+            while ((b = __ldg(row_ptr + n + 1)) <= pos) ++n;
+            const float* gn = g + (int64_t)n * (16 * kC32) + 4 * B.q;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 4 * gq + i;
-                    gr[i] = r < 15 ? ld_ro4(gn + (1 + r) * kC32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * B.gq + i;
+                gr[i] = r < 15 ? ld_ro4(gn + (1 + r) * kC32) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            while (pos < t) {
-                const int k = (int)((pos - p0) / kTileEdges);
-                if (k != cur) {
-                    if (cur >= 0) ring.refill(perm, coup, rad, E, lane);
-                    st = ring.acquire();
-                    cur = k;
+        };
+        if (p0 < vend) enter(p0);
+        for (int k = 0; k < ring.ntiles; ++k) {
+            const int st = ring.acquire();
+            const int tb = p0 + k * T;
+            const int jt = imin(T, p1 - tb);
+            int j = 0;
+            while (j < jt) {
+                if (tb + j >= vend) {              // edges without a node: zero gradients
+                    for (int jj = j; jj < jt; ++jj) {
+                        const int e = ring.meta[st * T + jj].x;
+                        if (e < 0) continue;
+                        if (B.lane < 24) st_stream4(d_rad + (int64_t)e * (3 * kC32) + 4 * B.lane,
+                                                    make_float4(0.f, 0.f, 0.f, 0.f));
+                        if (B.lane < 15) st_stream(d_coup + (int64_t)e * 15 + B.lane, 0.f);
+                    }
+                    break;
                 }
-                const int64_t tb = p0 + (int64_t)k * kTileEdges;
-                const int64_t tend = imin<int64_t>(t, tb + kTileEdges);
-                const float* radst = ring.rad + (size_t)st * kTileEdges * 96;
-                const float* coupst = ring.coup + (size_t)st * kTileEdges * kCoupSlotFloats;
-                const int2* metast = ring.meta + st * kTileEdges;
-                const int j1 = (int)(tend - tb);
+                if (tb + j >= b) {
+                    ++n;
+                    enter(tb + j);
+                }
+                const int stop = imin(b - tb, jt);
+                if (j == 0 && stop == T) {
+#pragma unroll
+                    for (int jj = 0; jj < T; ++jj) bwd_edge32(ring, st, jj, gr, B, d_coup, d_rad);
+                } else {
 #pragma unroll 2
-                for (int j = (int)(pos - tb); j < j1; ++j) {
-                    const int2 m = metast[j];
-                    if (m.x < 0) continue;
-                    const int64_t e = m.x;
-                    if (!has_node) {
-                        if (lane < 24) st_stream4(d_rad + e * (3 * kC32) + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
-                        if (lane < 15) st_stream(d_coup + e * 15 + lane, 0.f);
-                        continue;
-                    }
-                    const float* rrow = radst + j * 96;
-                    const float4 a = *reinterpret_cast<const float4*>(rrow + slo * kC32 + 4 * q);
-                    const float4 bb = *reinterpret_cast<const float4*>(rrow + shi * kC32 + 4 * q);
-                    const float* crow = coupst + j * kCoupSlotFloats + m.y + 4 * gq;
-                    const float4 c4 = make_float4(crow[0], crow[1], crow[2], gq == 3 ? 0.f : crow[3]);
-                    const float p0v = f4_dot(gr[0], a);
-                    const float p1v = f4_dot(gr[1], a);
-                    const float p2v = f4_dot(gr[2], a);
-                    const float p3v = f4_dot(gr[3], bb);
-                    const float x0 = b2 ? p0v : p2v, x1 = b2 ? p1v : p3v;
-                    const float k0 = (b2 ? p2v : p0v) + __shfl_xor_sync(kFull, x0, 4);
-                    const float k1 = (b2 ? p3v : p1v) + __shfl_xor_sync(kFull, x1, 4);
-                    float mm = (b1 ? k1 : k0) + __shfl_xor_sync(kFull, b1 ? k0 : k1, 2);
-                    mm += __shfl_xor_sync(kFull, mm, 1);
-                    if (row_writer) st_stream(d_coup + e * 15 + my_row, mm);
-                    float4 lo = make_float4(c4.x * gr[0].x, c4.x * gr[0].y, c4.x * gr[0].z, c4.x * gr[0].w);
-                    lo = f4_fma(c4.y, gr[1], lo);
-                    lo = f4_fma(c4.z, gr[2], lo);
-                    const float4 hi = make_float4(c4.w * gr[3].x, c4.w * gr[3].y, c4.w * gr[3].z, c4.w * gr[3].w);
-                    const float4 both = f4_add(lo, hi);
-                    const float4 y = f4_shfl_xor(gq == 0 ? hi : both, 8);
-                    if (gq < 3) {
-                        const float4 res = gq == 0 ? lo : (gq == 1 ? f4_add(y, both) : f4_add(both, y));
-                        st_stream4(d_rad + e * (3 * kC32) + gq * kC32 + 4 * q, res);
-                    }
+                    for (int jj = j; jj < stop; ++jj) bwd_edge32(ring, st, jj, gr, B, d_coup, d_rad);
                 }
-                pos = tend;
+                j = stop;
             }
-            if (has_node) ++n;
+            ring.refill(perm, coup, rad, E, B.lane);
         }
     }
     ring.drain();
@@ -305,6 +344,8 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
             float* __restrict__ d_coup, float* __restrict__ d_rad) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kBwdWarps + warp;
+    pdl_wait();
+    pdl_trigger();
     if (gw >= Wtot) return;
     const int64_t p0 = (int64_t)gw * KW;
     const int64_t p1 = imin<int64_t>(p0 + KW, E);
@@ -345,11 +386,11 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
     if (fast) {
         const int64_t want = (nbatch + kBwdWarps - 1) / kBwdWarps;
         const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 2);
-        bwd_c32<4><<<grid, kBwdThreads, 0, s>>>(g, coup, rad, dst, E, N, d_coup, d_rad);
+        launch(bwd_c32<4>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, d_coup, d_rad);
     } else {
         const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
         const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
-        bwd_gen<<<grid, kBwdThreads, 0, s>>>(g, coup, rad, dst, E, N, C, d_coup, d_rad);
+        launch(bwd_gen, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad);
     }
     return check_launch("zs_backward");
 }
@@ -368,24 +409,24 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
-        constexpr int W = 7, S = 2;
+        constexpr int W = ZS_BWD_WARPS, S = ZS_BWD_STAGES, T = ZS_BWD_TILE;
         const int64_t warps_max = (int64_t)num_sms() * W;
-        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max, kTileEdges);
+        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max, T);
         const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
         const int64_t ctas = (Wtot + W - 1) / W;
-        const int smem = W * RingLayout<S>::kBytes;
+        const int smem = W * RingLayout<S, T>::kBytes;
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(bwd_csr_c32_tma<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(bwd_csr_c32_tma<W, S, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             attr_set = true;
         }
-        bwd_csr_c32_tma<W, S><<<(unsigned)ctas, W * 32, smem, s>>>(g, coup, rad, row_ptr, perm, E, N, KW, (int)Wtot,
-                                                                     d_coup, d_rad);
+        launch(bwd_csr_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
+               (int)KW, (int)Wtot, d_coup, d_rad);
     } else {
         const int64_t KW = 64;
         const int64_t Wtot = (E + KW - 1) / KW;
         const int64_t ctas = (Wtot + kBwdWarps - 1) / kBwdWarps;
-        bwd_csr_gen<<<(unsigned)ctas, kBwdThreads, 0, s>>>(g, coup, rad, row_ptr, perm, E, N, C, KW, (int)Wtot,
+        launch(bwd_csr_gen, (unsigned)ctas, kBwdThreads, 0, s, g, coup, rad, row_ptr, perm, E, N, C, KW, (int)Wtot,
                                                             d_coup, d_rad);
     }
     return check_launch("zs_backward_csr");

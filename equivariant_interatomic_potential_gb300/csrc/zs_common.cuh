@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "zs.h"
 
 namespace zs {
@@ -108,5 +110,31 @@ template <class T>
 __host__ __device__ __forceinline__ constexpr T imax(T a, T b) { return a < b ? b : a; }
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialisation, so it may be scheduled while the
+// previous kernel in the stream is still finishing; pdl_wait() blocks until
+// that kernel has completed and its memory is visible, and must come before
+// the first global-memory access (read or write).  pdl_trigger() lets the
+// next kernel start being scheduled.  Both are no-ops when the kernel was
+// not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace zs

@@ -5,7 +5,7 @@
 // order ("stable-sort CSR order", section "What").  Built here as an LSD
 // radix sort of destination keys with 8-bit digits, each pass in three
 // launches with no inter-CTA waiting:
-//   upsweep   -- per tile of 2048 keys, a 256-bin digit histogram
+//   upsweep   -- per tile of 2048 keys, a 256-bin digit histogram (shared atomics)
 //   scan      -- per digit, exclusive scan of its histogram row over tiles
 //   downsweep -- per tile, stable rank of every key among equal digits
 //                (warp match + per-warp running counts), then scatter
@@ -40,27 +40,20 @@ template <bool kFirst>
 __global__ void __launch_bounds__(kCsrThreads)
 csr_upsweep(const int32_t* __restrict__ keys_in, int64_t E, int32_t N, int shift,
             int32_t* __restrict__ hist, int T) {
-    __shared__ int cnt[kCsrWarps][kRadix];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < kCsrWarps * kRadix; i += kCsrThreads) (&cnt[0][0])[i] = 0;
+    __shared__ int cnt[kRadix];
+    const int tid = threadIdx.x;
+    cnt[tid] = 0;   // kCsrThreads == kRadix
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
-    const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)warp * kCsrItems * 32;
-#pragma unroll
-    for (int i = 0; i < kCsrItems; ++i) {
-        const int64_t idx = base + i * 32 + lane;
-        const bool valid = idx < E;
-        const int digit = valid ? ((key_of(keys_in, idx, N, kFirst) >> shift) & (kRadix - 1)) : kRadix;
-        const unsigned peers = __match_any_sync(0xffffffffu, digit);
-        if (valid && lane == __ffs(peers) - 1) cnt[warp][digit] += __popc(peers);
-        __syncwarp();
+    // counts do not depend on the order of the increments
+    const int64_t base = (int64_t)blockIdx.x * kTile;
+    for (int i = tid; i < kTile; i += kCsrThreads) {
+        const int64_t idx = base + i;
+        if (idx < E) atomicAdd(&cnt[(key_of(keys_in, idx, N, kFirst) >> shift) & (kRadix - 1)], 1);
     }
     __syncthreads();
-    for (int d = tid; d < kRadix; d += kCsrThreads) {
-        int s = 0;
-#pragma unroll
-        for (int w = 0; w < kCsrWarps; ++w) s += cnt[w][d];
-        hist[(int64_t)d * T + blockIdx.x] = s;
-    }
+    hist[(int64_t)tid * T + blockIdx.x] = cnt[tid];
 }
 
 // One warp per digit: exclusive scan of hist[d, 0..T) in place, total to tot[d].
@@ -69,6 +62,8 @@ csr_scan(int32_t* __restrict__ hist, int T, int32_t* __restrict__ tot) {
     constexpr int R = 8;
     const int lane = threadIdx.x & 31;
     const int d = blockIdx.x * kCsrWarps + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
     if (d >= kRadix) return;
     int32_t* row = hist + (int64_t)d * T;
     int carry = 0;
@@ -110,6 +105,8 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
     __shared__ int dbase[kRadix];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < kCsrWarps * kRadix; i += kCsrThreads) (&cnt[0][0])[i] = 0;
+    pdl_wait();
+    pdl_trigger();
 
     // Exclusive scan of the 256 digit totals (kCsrThreads == kRadix).
     {
@@ -173,6 +170,8 @@ __global__ void __launch_bounds__(256)
 csr_row_ptr(const int32_t* __restrict__ sorted, int64_t E, int32_t N,
             int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (j > E) return;
     const int64_t kprev = j > 0 ? (int64_t)sorted[j - 1] : -1;
     const int64_t kcur = j < E ? (int64_t)sorted[j] : (int64_t)N + 1;
@@ -242,17 +241,17 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
             const int shift = 8 * pass;
             int32_t* kout = reinterpret_cast<int32_t*>(ws + p.off_k[pass & 1]);
             int32_t* vout = last ? perm : reinterpret_cast<int32_t*>(ws + p.off_v[pass & 1]);
-            if (first) csr_upsweep<true><<<p.T, kCsrThreads, 0, s>>>(kin, E, N, shift, hist, p.T);
-            else csr_upsweep<false><<<p.T, kCsrThreads, 0, s>>>(kin, E, N, shift, hist, p.T);
-            csr_scan<<<kRadix / kCsrWarps, kCsrThreads, 0, s>>>(hist, p.T, tot);
-            if (first) csr_downsweep<true><<<p.T, kCsrThreads, 0, s>>>(kin, vin, E, N, shift, hist, tot, p.T, kout, vout);
-            else csr_downsweep<false><<<p.T, kCsrThreads, 0, s>>>(kin, vin, E, N, shift, hist, tot, p.T, kout, vout);
+            if (first) launch(csr_upsweep<true>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
+            else launch(csr_upsweep<false>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
+            launch(csr_scan, kRadix / kCsrWarps, kCsrThreads, 0, s, hist, p.T, tot);
+            if (first) launch(csr_downsweep<true>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
+            else launch(csr_downsweep<false>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
             kin = kout;
             vin = vout;
         }
         sorted = kin;
     }
     const int64_t threads = E + 1;
-    csr_row_ptr<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(sorted, E, N, row_ptr, bad_dst_count);
+    launch(csr_row_ptr, (unsigned)((threads + 255) / 256), 256, 0, s, sorted, E, N, row_ptr, bad_dst_count);
     return check_launch("zs_build_csr");
 }

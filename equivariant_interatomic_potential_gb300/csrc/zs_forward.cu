@@ -27,8 +27,19 @@ namespace {
 
 constexpr int kFwdWarps = 8;
 constexpr int kFwdThreads = kFwdWarps * 32;
-constexpr int kTmaWarps = 7;                   // warps per CTA of the C == 32 path (one CTA per SM)
-constexpr int kTmaStages = 2;                  // tiles of 32 edges per warp ring
+// C == 32 path: warps per CTA (one CTA per SM), ring stages and edges per tile.
+#ifndef ZS_FWD_WARPS
+#define ZS_FWD_WARPS 14
+#endif
+#ifndef ZS_FWD_STAGES
+#define ZS_FWD_STAGES 2
+#endif
+#ifndef ZS_FWD_TILE
+#define ZS_FWD_TILE 16
+#endif
+constexpr int kTmaWarps = ZS_FWD_WARPS;
+constexpr int kTmaStages = ZS_FWD_STAGES;
+constexpr int kTile = ZS_FWD_TILE;
 constexpr int kGenWin = 256;                   // CSR positions per warp (per-channel path)
 constexpr int kC32 = 32;
 constexpr int kNodeFloats32 = kD * kC32;       // 512 floats per node at C = 32
@@ -38,15 +49,15 @@ constexpr unsigned kFull = 0xffffffffu;
 // --------------------------------------------------------------------------
 // C == 32 path.  Lane layout: group g = lane/8 owns zonal rows 4g..4g+3 (row
 // 15 is padding), quad q = lane%8 owns channels 4q..4q+3.  Rows 4g..4g+2
-// share one radial slot; row 4g+3 uses the slot of lane+8 for g == 0 (row 3
-// is the first degree-2 row) and the lane's own slot otherwise.
+// share one radial slot; row 4g+3 uses slot 1 for g == 0 (row 3 is the first
+// degree-2 row) and the group's own slot otherwise.
 // --------------------------------------------------------------------------
 
 struct Lane32 {
-    int lane, g, q, slo, src_hi;
+    int lane, g, q, slo, shi;
     __device__ __forceinline__ explicit Lane32(int l) : lane(l), g(l >> 3), q(l & 7) {
         slo = g == 0 ? 0 : (g == 1 ? 1 : 2);
-        src_hi = g == 0 ? lane + 8 : lane;
+        shi = g == 0 ? 1 : slo;
     }
 };
 
@@ -83,90 +94,118 @@ __device__ __forceinline__ void zero_node32(float* __restrict__ node, int lane) 
         *reinterpret_cast<float4*>(node + 4 * (lane + 32 * k)) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Add the messages of the edges at tile positions [j0, j1) of stage st.
-template <int S>
-__device__ __forceinline__ void accumulate_tile32(const TileRing<S>& ring, int st, int j0, int j1,
-                                                  const Lane32& L, int shi, float4 acc[4]) {
-    const float* radst = ring.rad + (size_t)st * kTileEdges * 96;
-    const float* coupst = ring.coup + (size_t)st * kTileEdges * kCoupSlotFloats;
-    const int2* metast = ring.meta + st * kTileEdges;
-#pragma unroll 4
-    for (int j = j0; j < j1; ++j) {
-        const int2 m = metast[j];
-        if (m.x < 0) continue;
-        const float* rrow = radst + j * 96;
-        const float4 a = *reinterpret_cast<const float4*>(rrow + L.slo * kC32 + 4 * L.q);
-        const float4 b = *reinterpret_cast<const float4*>(rrow + shi * kC32 + 4 * L.q);
-        const float* crow = coupst + j * kCoupSlotFloats + m.y + 4 * L.g;
-        acc[0] = f4_fma(crow[0], a, acc[0]);
-        acc[1] = f4_fma(crow[1], a, acc[1]);
-        acc[2] = f4_fma(crow[2], a, acc[2]);
-        acc[3] = f4_fma(crow[3], b, acc[3]);   // row 15 of group 3 is padding, never stored
-    }
+// Add the message of the edge at tile slot j of stage st.  Rows of
+// positions without an edge are zero in the ring, so there is no branch.
+struct TileView {
+    const float* ra;    // radial quad of slot slo of edge 0
+    const float* rb;    // radial quad of slot shi of edge 0
+    const float* cp;    // coupling span of edge 0, offset to this group's rows
+    const int2* mt;     // (edge id, row offset in span) per edge
+};
+
+__device__ __forceinline__ void add_edge32(const TileView& v, int j, float4 acc[4]) {
+    const float4 a = *reinterpret_cast<const float4*>(v.ra + j * 96);
+    const float4 b = *reinterpret_cast<const float4*>(v.rb + j * 96);
+    const float* crow = v.cp + j * kCoupSlotFloats + v.mt[j].y;
+    acc[0] = f4_fma(crow[0], a, acc[0]);
+    acc[1] = f4_fma(crow[1], a, acc[1]);
+    acc[2] = f4_fma(crow[2], a, acc[2]);
+    acc[3] = f4_fma(crow[3], b, acc[3]);   // row 15 of group 3 is padding, never stored
 }
 
-// First node to visit for window [p0, ...): the node containing p0 when it
-// starts before p0, else the first node starting at or after p0.
+// First node to visit for a window starting at p0: the node containing p0
+// when it starts before p0, else the first node starting at or after p0.
 __device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
     const int n_lb = lower_bound_i32(row_ptr, N + 1, p0);
     if (n_lb >= 1 && n_lb <= N && (int64_t)__ldg(row_ptr + n_lb) > p0) return n_lb - 1;
     return n_lb;
 }
 
-// C == 32 forward with TMA-fed warps.  W warps per CTA, one CTA per SM, each
-// warp owns the window [gw*KW, gw*KW + KW) of CSR positions.
-template <int W, int S>
+// C == 32 forward with TMA-fed warps.  W warps per CTA, one CTA per SM; warp
+// gw owns the window [gw*KW, gw*KW + KW) of CSR positions and walks it in
+// position order, closing a node when its last position is reached.
+template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-            int64_t E, int32_t N, int64_t KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
+            int E, int32_t N, int KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
     const int warp = threadIdx.x >> 5;
     const Lane32 L(threadIdx.x & 31);
-    const int shi = L.g == 0 ? 1 : L.slo;
     const int gw = blockIdx.x * W + warp;
-    const int64_t p0 = gw < Wtot ? (int64_t)gw * KW : E;
-    const int64_t p1 = gw < Wtot ? imin<int64_t>(p0 + KW, E) : E;
-    TileRing<S> ring;
-    ring.init(smem + (size_t)warp * RingLayout<S>::kBytes, p0, p1, L.lane);
+    const bool active = gw < Wtot;
+    pdl_wait();
+    pdl_trigger();
+    const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
+    const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
+    const bool is_last = gw == Wtot - 1;
+    const int vend = __ldg(row_ptr + N);              // positions from vend on hold no node
+    const int pe = imax(p0, imin(p1, vend));
+    TileRing<S, T> ring;
+    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, active ? pe : p0, L.lane);
     if (L.lane < 2) sp_node[warp][L.lane] = -1;
     __syncwarp();
 
     float4 acc0[4] = {}, acc[4] = {};
     bool have0 = false, have1 = false;
-    if (gw < Wtot) {
+    if (active) {
         ring.prefetch_perm(perm, L.lane);
 #pragma unroll
         for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, L.lane);
-        const bool is_last = gw == Wtot - 1;
-        int cur = -1, st = 0;
-        for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
-            const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
-            if (a >= p1 && !(is_last && a == b)) break;
-            if (a == b) {
+        // current node n covers positions [a, b); empty nodes this window owns
+        // (those starting in it, or all trailing ones for the last window) are zeroed
+        int n = first_node(row_ptr, N, p0), a = 0, b = 0;
+        auto advance = [&]() {
+            for (; n < N; ++n) {
+                a = __ldg(row_ptr + n);
+                b = __ldg(row_ptr + n + 1);
+                if (a != b) break;
+                if (a >= p1 && !is_last) break;
                 zero_node32(out + (int64_t)n * kNodeFloats32, L.lane);
-                continue;
             }
+        };
+        advance();
+        const float* rbase = ring.rad + L.slo * kC32 + 4 * L.q;
+        const float* hbase = ring.rad + L.shi * kC32 + 4 * L.q;
+        const float* cbase = ring.coup + 4 * L.g;
+        for (int k = 0; k < ring.ntiles; ++k) {
+            const int st = ring.acquire();
+            const TileView v{rbase + st * T * 96, hbase + st * T * 96, cbase + st * T * kCoupSlotFloats,
+                             ring.meta + st * T};
+            const int tb = p0 + k * T;
+            const int jt = imin(T, pe - tb);
+            int j = 0;
+            while (j < jt) {
+                const int stop = imin(b - tb, jt);   // the current node covers position tb + j
+                if (j == 0 && stop == T) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            int64_t pos = imax<int64_t>(a, p0);
-            const int64_t t = imin<int64_t>(b, p1);
-            while (pos < t) {
-                const int k = (int)((pos - p0) / kTileEdges);
-                if (k != cur) {
-                    if (cur >= 0) ring.refill(perm, coup, rad, E, L.lane);
-                    st = ring.acquire();
-                    cur = k;
+                    for (int jj = 0; jj < T; ++jj) add_edge32(v, jj, acc);
+                } else {
+#pragma unroll 4
+                    for (int jj = j; jj < stop; ++jj) add_edge32(v, jj, acc);
                 }
-                const int64_t tb = p0 + (int64_t)k * kTileEdges;
-                const int64_t tend = imin<int64_t>(t, tb + kTileEdges);
-                accumulate_tile32(ring, st, (int)(pos - tb), (int)(tend - tb), L, shi, acc);
-                pos = tend;
+                j = stop;
+                if (tb + j == b) {                   // node n ends inside this window
+                    if (a >= p0) {
+                        store_node32(out + (int64_t)n * kNodeFloats32, acc, L);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
+                        have0 = true;
+                        if (L.lane == 0) sp_node[warp][0] = n;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    ++n;
+                    advance();
+                }
             }
-            if (a >= p0 && b <= p1) {
-                store_node32(out + (int64_t)n * kNodeFloats32, acc, L);
-            } else if (a < p0) {
+            ring.refill(perm, coup, rad, E, L.lane);
+        }
+        // a node still open at the end runs past p1
+        if (n < N && a < pe && b > pe) {
+            if (a < p0) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
                 have0 = true;
@@ -175,7 +214,6 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
                 have1 = true;
                 if (L.lane == 0) sp_node[warp][1] = n;
             }
-            if (b > p1) break;
         }
     }
     ring.drain();
@@ -198,16 +236,15 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
         load_part32(part + slot * kPartFloats32, sum, L);
         for (int w2 = warp + 1; w2 < W && sp_node[w2][0] == m; ++w2) {
             float4 t4[4];
-            load_part32(reinterpret_cast<const float*>(smem + (size_t)w2 * RingLayout<S>::kBytes), t4, L);
+            load_part32(reinterpret_cast<const float*>(smem + (size_t)w2 * RingLayout<S, T>::kBytes), t4, L);
 #pragma unroll
             for (int i = 0; i < 4; ++i) sum[i] = f4_add(sum[i], t4[i]);
         }
-        const int a = __ldg(row_ptr + m), b = __ldg(row_ptr + m + 1);
-        if (a >= P0 && b <= P1) {
+        const int ma = __ldg(row_ptr + m), mb = __ldg(row_ptr + m + 1);
+        if (ma >= P0 && mb <= P1) {
             store_node32(out + (int64_t)m * kNodeFloats32, sum, L);
         } else {
-            const int cslot = a < P0 ? 0 : 1;
-            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + cslot) * kPartFloats32, sum, L);
+            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * kPartFloats32, sum, L);
         }
     }
 }
@@ -262,6 +299,8 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
     __shared__ float cs[kFwdWarps][32][16];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kFwdWarps + warp;
+    pdl_wait();
+    pdl_trigger();
     if (gw >= Wtot) return;
     const int64_t V = (int64_t)kRows * C;
     const int64_t p0 = (int64_t)gw * kGenWin;
@@ -313,6 +352,8 @@ fwd_fixup(const int32_t* __restrict__ row_ptr, int32_t N, int C, int win,
     __shared__ float red[kFwdWarps][kFixVals];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t V = (int64_t)kRows * C;
+    pdl_wait();
+    pdl_trigger();
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
         if (a >= b) continue;
@@ -366,8 +407,8 @@ extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
     (void)N;
     // One pair of (15 x C) partials per window: per warp window of kGenWin
     // positions on the per-channel path, per CTA window of at least
-    // kTmaWarps * 32 positions on the C == 32 path.
-    const int64_t windows = ceil_div(E > 0 ? E : 1, imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTileEdges)) + 1;
+    // kTmaWarps * kTile positions on the C == 32 path.
+    const int64_t windows = ceil_div(E > 0 ? E : 1, imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile)) + 1;
     return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256);
 }
 
@@ -395,23 +436,23 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
         // the same number of CSR positions (at least one tile).
         const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
-        const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTileEdges);
+        const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
         const int64_t Wtot = imax<int64_t>(ceil_div(E, KW), 1);
         const int64_t ctas = ceil_div(Wtot, kTmaWarps);
-        const int smem = kTmaWarps * RingLayout<kTmaStages>::kBytes;
+        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             attr_set = true;
         }
-        fwd_c32_tma<kTmaWarps, kTmaStages><<<(unsigned)ctas, kTmaWarps * 32, smem, s>>>(
-            coup, rad, row_ptr, perm, E, N, KW, (int)Wtot, out, part);
-        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, (int)(KW * kTmaWarps), part, out);
+        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part);
+        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, (int)(KW * kTmaWarps), (const float*)part, out);
     } else {
         const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
         const int64_t ctas = ceil_div(Wtot, kFwdWarps);
-        fwd_gen_main<<<(unsigned)ctas, kFwdThreads, 0, s>>>(coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
-        fwd_fixup<<<fix_grid, kFwdThreads, 0, s>>>(row_ptr, N, C, kGenWin, part, out);
+        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
+        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, kGenWin, (const float*)part, out);
     }
     return check_launch("zs_forward");
 }

@@ -1,17 +1,20 @@
-// Per-warp TMA ring over a window of CSR positions (sm_90+ bulk copies,
-// used here on sm_103a).
+// Per-warp ring of asynchronous copies over a window of CSR positions.
 //
-// A warp streams the edges at CSR positions [p0, p1) in tiles of 32.  For
-// each edge e = perm[j] of a tile, one lane issues two cp.async.bulk copies
-// into the tile's shared-memory stage: the radial row rad[e] (3*32 floats,
-// 384 bytes) and the 16-byte-aligned span holding the coupling row coup[e]
-// (60 bytes inside 64 or 80 bytes).  Completion is counted in bytes on one
-// mbarrier per stage.  Tiles are issued kStages - 1 ahead of the one being
-// consumed, so each warp keeps about 15 KB of HBM reads in flight with no
-// registers held for them.
+// A warp streams the edges at CSR positions [p0, pe) in tiles of T edges
+// (T <= 32, one lane per edge).  For edge e = perm[j] its lane issues
+//   - one cp.async.bulk (TMA) copy of the radial row rad[e] (3*32 floats,
+//     384 bytes, 16-byte aligned), completion counted in bytes on the
+//     stage's mbarrier, and
+//   - four or five 16-byte cp.async copies of the aligned span holding the
+//     coupling row coup[e] (60 bytes at byte offset 60e), completion signalled
+//     to the same mbarrier by cp.async.mbarrier.arrive.
+// Tiles are issued S - 1 ahead of the one being consumed, so a warp keeps
+// (S - 1) * T * ~450 bytes of HBM reads in flight without holding registers
+// for them.  A position whose perm entry is not a valid edge id gets zero
+// rows, so consumers need no branch.
 //
-// Every wait is bounded: after kMaxSpins unsuccessful tries the wait records
-// a timeout in g_zs_timeouts and returns, so a lost completion can never hang
+// Every wait is bounded: after kMaxSpins unsuccessful tries the wait counts a
+// timeout in g_zs_timeouts and returns, so a lost completion can never hang
 // the GPU; zs_check_timeouts() reports it.
 #pragma once
 
@@ -30,10 +33,10 @@ static inline unsigned int take_timeouts_local() {
     return v;
 }
 
-constexpr int kTileEdges = 32;
 constexpr int kRadRowBytes = 3 * 32 * 4;    // 384
 constexpr int kCoupSlotFloats = 20;         // 80 bytes: the widest aligned span of one coupling row
 constexpr uint32_t kMaxSpins = 1u << 22;
+constexpr uint32_t kRingArrivals = 33;      // the expect-tx arrival plus one cp.async arrival per lane
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,102 +71,120 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on bar once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
-// Shared-memory layout of one warp's ring.
-template <int S>
+// Shared-memory layout of one warp's ring of S stages of T edges.
+template <int S, int T>
 struct RingLayout {
-    static constexpr int kRad = S * kTileEdges * kRadRowBytes;              // radial rows
-    static constexpr int kCoup = S * kTileEdges * kCoupSlotFloats * 4;      // coupling spans
-    static constexpr int kMeta = S * kTileEdges * 8;                        // (edge id, coupling offset)
+    static constexpr int kRad = S * T * kRadRowBytes;              // radial rows
+    static constexpr int kCoup = S * T * kCoupSlotFloats * 4;      // coupling spans
+    static constexpr int kMeta = S * T * 8;                        // (edge id, coupling offset)
     static constexpr int kBars = S * 8;
     static constexpr int kBytes = (kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
 };
 
-// One warp's stream of tiles over [p0, p1).
-template <int S>
+// One warp's stream of tiles over [p0, pe).
+template <int S, int T>
 struct TileRing {
-    float* rad;        // [S][32][96]
-    float* coup;       // [S][32][20]
-    int2* meta;        // [S][32]: x = edge id (-1 if none), y = float offset of the row in its span
+    static_assert(T >= 1 && T <= 32, "a tile is at most one edge per lane");
+    float* rad;        // [S][T][96]
+    float* coup;       // [S][T][20]
+    int2* meta;        // [S][T]: x = edge id (-1 if none), y = float offset of the row in its span
     uint32_t bar0;     // shared address of the first mbarrier
-    int64_t p0, p1;
-    int ntiles;        // tiles covering [p0, p1)
+    int p0, pe;
+    int ntiles;        // tiles covering [p0, pe)
     int issued;        // tiles issued so far
     int consumed;      // tiles waited for so far
     int pf;            // this lane's perm entry for tile `issued` (prefetched)
 
-    __device__ __forceinline__ void init(unsigned char* base, int64_t p0_, int64_t p1_, int lane) {
+    __device__ __forceinline__ void init(unsigned char* base, int p0_, int pe_, int lane) {
         rad = reinterpret_cast<float*>(base);
-        coup = reinterpret_cast<float*>(base + RingLayout<S>::kRad);
-        meta = reinterpret_cast<int2*>(base + RingLayout<S>::kRad + RingLayout<S>::kCoup);
-        bar0 = smem_u32(base + RingLayout<S>::kRad + RingLayout<S>::kCoup + RingLayout<S>::kMeta);
+        coup = reinterpret_cast<float*>(base + RingLayout<S, T>::kRad);
+        meta = reinterpret_cast<int2*>(base + RingLayout<S, T>::kRad + RingLayout<S, T>::kCoup);
+        bar0 = smem_u32(base + RingLayout<S, T>::kRad + RingLayout<S, T>::kCoup + RingLayout<S, T>::kMeta);
         p0 = p0_;
-        p1 = p1_;
-        ntiles = p1 > p0 ? (int)((p1 - p0 + kTileEdges - 1) / kTileEdges) : 0;
+        pe = pe_;
+        ntiles = pe > p0 ? (pe - p0 + T - 1) / T : 0;
         issued = 0;
         consumed = 0;
-        if (lane < S) mbar_init(bar0 + 8 * lane, 1);
+        if (lane < S) mbar_init(bar0 + 8 * lane, kRingArrivals);
         mbar_fence_init();
         __syncwarp();
     }
 
     __device__ __forceinline__ void prefetch_perm(const int32_t* __restrict__ perm, int lane) {
-        const int64_t j = p0 + (int64_t)issued * kTileEdges + lane;
-        pf = (issued < ntiles && j < p1) ? ld_stream_i(perm + j) : -1;
+        const int j = p0 + issued * T + lane;
+        pf = (issued < ntiles && lane < T && j < pe) ? ld_stream_i(perm + j) : -1;
     }
 
     // Issue the next tile into its stage (its previous tile must be consumed).
     __device__ __forceinline__ void issue(const int32_t* __restrict__ perm, const float* __restrict__ coup_g,
-                                          const float* __restrict__ rad_g, int64_t E, int lane) {
+                                          const float* __restrict__ rad_g, int E, int lane) {
         if (issued >= ntiles) return;
-        const int k = issued;
-        const int st = k % S;
-        const int64_t j = p0 + (int64_t)k * kTileEdges + lane;
-        int e = pf;
-        if ((uint32_t)e >= (uint64_t)E) e = -1;
-        // next tile's perm entries, consumed at the next issue
+        const int st = issued % S;
+        const int e = pf;
         ++issued;
-        prefetch_perm(perm, lane);
-        int off = 0;
-        uint32_t cbytes = 0;
+        prefetch_perm(perm, lane);   // the next tile's entries, used at the next issue
+        const bool valid = (uint32_t)e < (uint32_t)E;
         int64_t cstart = 0;
-        bool plain = false;
-        if (e >= 0 && j < p1) {
+        int off = 0, nch = 0;
+        bool tail = false;
+        if (valid) {
             const int64_t b0 = (int64_t)e * 60;
             cstart = b0 & ~(int64_t)15;
-            const int64_t cend = (b0 + 60 + 15) & ~(int64_t)15;
-            off = (int)((b0 - cstart) >> 2);
-            if (cend <= E * 60) {
-                cbytes = (uint32_t)(cend - cstart);
-            } else {
-                plain = true;   // span would run past the end of coup: load the row directly
-            }
-        } else {
-            e = -1;
+            off = (int)(b0 - cstart) >> 2;          // 0..3
+            nch = (off * 4 + 75) >> 4;              // 16-byte pieces covering the row: 4 or 5
+            tail = cstart + 16 * nch > (int64_t)E * 60;
         }
-        const uint32_t mine = (e >= 0 ? (uint32_t)kRadRowBytes : 0u) + cbytes;
-        const uint32_t total = __reduce_add_sync(0xffffffffu, mine);
         const uint32_t bar = bar0 + 8 * st;
-        float* cslot = coup + ((size_t)st * kTileEdges + lane) * kCoupSlotFloats;
-        if (plain) {
-            off = 0;
-            const float* src = coup_g + (int64_t)e * 15;
+        float* cslot = coup + (st * T + lane) * kCoupSlotFloats;
+        float* rslot = rad + (st * T + lane) * 96;
+        if (lane < T) {
+            if (!valid || tail) {
+                // rare: no edge here, or the span would run past the end of coup.
+                // Generic-proxy writes, ordered before the consumer by the
+                // syncwarps below and after the consumer's wait.
+                if (valid) {
+                    const float* src = coup_g + (int64_t)e * 15;
 #pragma unroll
-            for (int r = 0; r < 15; ++r) cslot[r] = __ldg(src + r);
+                    for (int r = 0; r < 15; ++r) cslot[r] = __ldg(src + r);
+                } else {
+                    for (int r = 0; r < kCoupSlotFloats; ++r) cslot[r] = 0.f;
+                    for (int c = 0; c < 96; ++c) rslot[c] = 0.f;
+                }
+                off = 0;
+            }
+            meta[st * T + lane] = make_int2(valid ? e : -1, off);
         }
-        meta[st * kTileEdges + lane] = make_int2(e, off);
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, total);
+        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadRowBytes);
         __syncwarp();
-        if (e >= 0) {
-            bulk_g2s(smem_u32(rad + ((size_t)st * kTileEdges + lane) * 96), rad_g + (int64_t)e * 96,
-                     kRadRowBytes, bar);
-            if (cbytes) bulk_g2s(smem_u32(cslot), reinterpret_cast<const char*>(coup_g) + cstart, cbytes, bar);
+        if (valid) {
+            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * 96, kRadRowBytes, bar);
+            if (!tail) {
+                const char* src = reinterpret_cast<const char*>(coup_g) + cstart;
+                const uint32_t dst = smem_u32(cslot);
+                cp_async16(dst, src);
+                cp_async16(dst + 16, src + 16);
+                cp_async16(dst + 32, src + 32);
+                cp_async16(dst + 48, src + 48);
+                if (nch == 5) cp_async16(dst + 64, src + 64);
+            }
         }
+        cp_async_arrive(bar);
     }
 
     // Wait for the next tile in order; returns its stage.
@@ -177,7 +198,7 @@ struct TileRing {
 
     // The last acquired tile is finished: reuse its stage for the next tile.
     __device__ __forceinline__ void refill(const int32_t* __restrict__ perm, const float* __restrict__ coup_g,
-                                           const float* __restrict__ rad_g, int64_t E, int lane) {
+                                           const float* __restrict__ rad_g, int E, int lane) {
         __syncwarp();
         issue(perm, coup_g, rad_g, E, lane);
     }
