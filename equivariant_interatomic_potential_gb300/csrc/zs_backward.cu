@@ -17,13 +17,13 @@ namespace {
 constexpr int kBwdWarps = 8;
 // CSR-order C == 32 path: warps per CTA (one CTA per SM), ring stages, edges per tile.
 #ifndef ZS_BWD_WARPS
-#define ZS_BWD_WARPS 14
+#define ZS_BWD_WARPS 16
 #endif
 #ifndef ZS_BWD_STAGES
 #define ZS_BWD_STAGES 2
 #endif
 #ifndef ZS_BWD_TILE
-#define ZS_BWD_TILE 16
+#define ZS_BWD_TILE 8
 #endif
 constexpr int kBwdThreads = kBwdWarps * 32;
 constexpr int kC32 = 32;
@@ -213,55 +213,40 @@ __device__ __forceinline__ int first_node_b(const int32_t* __restrict__ row_ptr,
     return n_lb;
 }
 
-// Gradients of the edge at tile slot j, whose node's cotangent rows are in
-// gr (rows 4g..4g+3 of this lane's group, channels 4q..4q+3).
-struct BwdLane {
-    int lane, gq, q, slo, shi, my_row;
-    bool b2, b1, row_writer;
-    __device__ __forceinline__ explicit BwdLane(int l) : lane(l), gq(l >> 3), q(l & 7) {
-        slo = gq == 0 ? 0 : (gq == 1 ? 1 : 2);
-        shi = gq == 0 ? 1 : slo;
-        b2 = (lane & 4) != 0;
-        b1 = (lane & 2) != 0;
-        my_row = 4 * gq + (b2 ? 2 : 0) + (b1 ? 1 : 0);
-        row_writer = (lane & 1) == 0 && my_row < 15;
-    }
+// Lane layout of the CSR-order C == 32 backward: the 8 lanes of group
+// grp = lane/8 own one edge of every 4 consecutive positions, lane q = lane%8
+// owns channels 4q..4q+3 of ALL 15 rows.  One warp instruction therefore
+// advances four edges; the radial gradient needs no cross-lane traffic and
+// the coupling gradient is one transposed butterfly over the group's 8 lanes.
+struct QuadLane {
+    int lane, grp, q;
+    bool b2, b1, b0;
+    __device__ __forceinline__ explicit QuadLane(int l)
+        : lane(l), grp(l >> 3), q(l & 7), b2((l & 4) != 0), b1((l & 2) != 0), b0((l & 1) != 0) {}
 };
 
-template <int S, int T>
-__device__ __forceinline__ void bwd_edge32(const TileRing<S, T>& ring, int st, int j, const float4 gr[4],
-                                           const BwdLane& B, float* __restrict__ d_coup, float* __restrict__ d_rad) {
-    const int2 m = ring.meta[st * T + j];
-    const float* rrow = ring.rad + (st * T + j) * 96;
-    const float4 a = *reinterpret_cast<const float4*>(rrow + B.slo * kC32 + 4 * B.q);
-    const float4 bb = *reinterpret_cast<const float4*>(rrow + B.shi * kC32 + 4 * B.q);
-    const float* crow = ring.coup + (st * T + j) * kCoupSlotFloats + m.y + 4 * B.gq;
-    const float4 c4 = make_float4(crow[0], crow[1], crow[2], B.gq == 3 ? 0.f : crow[3]);
-    // d_coup: four row dot products over this lane's 4 channels, then a
-    // transposed butterfly over the 8 lanes of the group
-    const float p0v = f4_dot(gr[0], a);
-    const float p1v = f4_dot(gr[1], a);
-    const float p2v = f4_dot(gr[2], a);
-    const float p3v = f4_dot(gr[3], bb);
-    const float x0 = B.b2 ? p0v : p2v, x1 = B.b2 ? p1v : p3v;
-    const float k0 = (B.b2 ? p2v : p0v) + __shfl_xor_sync(kFull, x0, 4);
-    const float k1 = (B.b2 ? p3v : p1v) + __shfl_xor_sync(kFull, x1, 4);
-    float mm = (B.b1 ? k1 : k0) + __shfl_xor_sync(kFull, B.b1 ? k0 : k1, 2);
-    mm += __shfl_xor_sync(kFull, mm, 1);
-    // d_rad: the group's rows weighted by their coupling; the degree-2 slot
-    // adds group 0's row 3, the degree-3 slot adds group 3's rows
-    float4 lo = make_float4(c4.x * gr[0].x, c4.x * gr[0].y, c4.x * gr[0].z, c4.x * gr[0].w);
-    lo = f4_fma(c4.y, gr[1], lo);
-    lo = f4_fma(c4.z, gr[2], lo);
-    const float4 hi = make_float4(c4.w * gr[3].x, c4.w * gr[3].y, c4.w * gr[3].z, c4.w * gr[3].w);
-    const float4 both = f4_add(lo, hi);
-    const float4 y = f4_shfl_xor(B.gq == 0 ? hi : both, 8);
-    if (m.x < 0) return;
-    const int64_t e = m.x;
-    if (B.row_writer) st_stream(d_coup + e * 15 + B.my_row, mm);
-    if (B.gq < 3) {
-        const float4 res = B.gq == 0 ? lo : (B.gq == 1 ? f4_add(y, both) : f4_add(both, y));
-        st_stream4(d_rad + e * (3 * kC32) + B.gq * kC32 + 4 * B.q, res);
+// Sum of v over the 8 lanes of the group for 16 values at once: each lane
+// ends with the totals of rows 8*b2 + 4*b1 + 2*b0 + {0, 1}.
+__device__ __forceinline__ void group_reduce16(float v[16], const QuadLane& Q, float& r0, float& r1) {
+    float w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float keep = Q.b2 ? v[k + 8] : v[k];
+        const float send = Q.b2 ? v[k] : v[k + 8];
+        w[k] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    float x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float keep = Q.b1 ? w[k + 4] : w[k];
+        const float send = Q.b1 ? w[k] : w[k + 4];
+        x[k] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float keep = Q.b0 ? x[k + 2] : x[k];
+        const float send = Q.b0 ? x[k] : x[k + 2];
+        (k == 0 ? r0 : r1) = keep + __shfl_xor_sync(kFull, send, 1);
     }
 }
 
@@ -271,9 +256,10 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
                 const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
                 int E, int32_t N, int KW, int Wtot,
                 float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    static_assert(T % 4 == 0, "tiles hold whole groups of four edges");
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
-    const BwdLane B(threadIdx.x & 31);
+    const QuadLane Q(threadIdx.x & 31);
     const int gw = blockIdx.x * W + warp;
     const bool active = gw < Wtot;
     pdl_wait();
@@ -281,56 +267,87 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
     TileRing<S, T> ring;
-    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, B.lane);
+    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, Q.lane);
     if (active) {
-        ring.prefetch_perm(perm, B.lane);
+        ring.prefetch_perm(perm, Q.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, B.lane);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, Q.lane);
         const int vend = __ldg(row_ptr + N);
+        // this group's node: n covers positions [.., b); G holds its rows 1..15
         int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
-        int b = 0;
-        float4 gr[4] = {};
-        auto enter = [&](int pos) {   // make node n the one holding position pos < vend
-            while ((b = __ldg(row_ptr + n + 1)) <= pos) ++n;
-            const float* gn = g + (int64_t)n * (16 * kC32) + 4 * B.q;
+        int b = n < N ? __ldg(row_ptr + n + 1) : 0;
+        float4 G[15];
+        const float* gq = g + 4 * Q.q;
+        auto load_g = [&]() {
+            const float* gn = gq + (int64_t)n * (16 * kC32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = 4 * B.gq + i;
-                gr[i] = r < 15 ? ld_ro4(gn + (1 + r) * kC32) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            for (int r = 0; r < 15; ++r) G[r] = ld_ro4(gn + (1 + r) * kC32);
         };
-        if (p0 < vend) enter(p0);
+        if (p0 < vend) {
+            while (b <= p0) b = __ldg(row_ptr + (++n) + 1);
+            load_g();
+        } else {
+#pragma unroll
+            for (int r = 0; r < 15; ++r) G[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
             const int tb = p0 + k * T;
             const int jt = imin(T, p1 - tb);
-            int j = 0;
-            while (j < jt) {
-                if (tb + j >= vend) {              // edges without a node: zero gradients
-                    for (int jj = j; jj < jt; ++jj) {
-                        const int e = ring.meta[st * T + jj].x;
-                        if (e < 0) continue;
-                        if (B.lane < 24) st_stream4(d_rad + (int64_t)e * (3 * kC32) + 4 * B.lane,
-                                                    make_float4(0.f, 0.f, 0.f, 0.f));
-                        if (B.lane < 15) st_stream(d_coup + (int64_t)e * 15 + B.lane, 0.f);
-                    }
-                    break;
+            const float* radst = ring.rad + st * T * 96 + 4 * Q.q;
+            const float* coupst = ring.coup + st * T * kCoupSlotFloats;
+            const int2* metast = ring.meta + st * T;
+#pragma unroll 1
+            for (int i = 0; i < T / 4; ++i) {
+                const int j = 4 * i + Q.grp;
+                const int pos = tb + j;
+                const bool in = j < jt;
+                const bool has_node = in && pos < vend;
+                if (has_node && pos >= b) {        // this group's edge starts a later node
+                    do { b = __ldg(row_ptr + (++n) + 1); } while (b <= pos);
+                    load_g();
                 }
-                if (tb + j >= b) {
-                    ++n;
-                    enter(tb + j);
-                }
-                const int stop = imin(b - tb, jt);
-                if (j == 0 && stop == T) {
+                const int2 m = metast[j];
+                const float* rrow = radst + j * 96;
+                const float4 a0 = *reinterpret_cast<const float4*>(rrow);
+                const float4 a1 = *reinterpret_cast<const float4*>(rrow + kC32);
+                const float4 a2 = *reinterpret_cast<const float4*>(rrow + 2 * kC32);
+                const float* crow = coupst + j * kCoupSlotFloats + m.y;
+                float c[15];
 #pragma unroll
-                    for (int jj = 0; jj < T; ++jj) bwd_edge32(ring, st, jj, gr, B, d_coup, d_rad);
-                } else {
-#pragma unroll 2
-                    for (int jj = j; jj < stop; ++jj) bwd_edge32(ring, st, jj, gr, B, d_coup, d_rad);
+                for (int r = 0; r < 15; ++r) c[r] = crow[r];
+                // radial gradient, one slot per degree group of rows
+                float4 s0 = make_float4(c[0] * G[0].x, c[0] * G[0].y, c[0] * G[0].z, c[0] * G[0].w);
+                s0 = f4_fma(c[1], G[1], s0);
+                s0 = f4_fma(c[2], G[2], s0);
+                float4 s1 = make_float4(c[3] * G[3].x, c[3] * G[3].y, c[3] * G[3].z, c[3] * G[3].w);
+#pragma unroll
+                for (int r = 4; r < 8; ++r) s1 = f4_fma(c[r], G[r], s1);
+                float4 s2 = make_float4(c[8] * G[8].x, c[8] * G[8].y, c[8] * G[8].z, c[8] * G[8].w);
+#pragma unroll
+                for (int r = 9; r < 15; ++r) s2 = f4_fma(c[r], G[r], s2);
+                // coupling gradient: per-row dot products over this lane's channels,
+                // then summed over the group's 8 lanes
+                float pr[16];
+#pragma unroll
+                for (int r = 0; r < 15; ++r) pr[r] = f4_dot(G[r], r < 3 ? a0 : (r < 8 ? a1 : a2));
+                pr[15] = 0.f;
+                float t0, t1;
+                group_reduce16(pr, Q, t0, t1);
+                const int e = m.x;
+                if (in && e >= 0) {
+                    const int row = 8 * Q.b2 + 4 * Q.b1 + 2 * Q.b0;
+                    float* dc = d_coup + (int64_t)e * 15 + row;
+                    float* dr = d_rad + (int64_t)e * (3 * kC32) + 4 * Q.q;
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    st_stream4(dr, has_node ? s0 : z);
+                    st_stream4(dr + kC32, has_node ? s1 : z);
+                    st_stream4(dr + 2 * kC32, has_node ? s2 : z);
+                    st_stream(dc, has_node ? t0 : 0.f);
+                    if (row + 1 < 15) st_stream(dc + 1, has_node ? t1 : 0.f);
                 }
-                j = stop;
             }
-            ring.refill(perm, coup, rad, E, B.lane);
+            ring.refill(perm, coup, rad, E, Q.lane);
         }
     }
     ring.drain();

@@ -154,8 +154,8 @@ ZS_API zs_status zs_backward(const float* g, const float* coup, const float* rad
  *   d_coup (E,15), d_rad (E,3,C)          outputs, fully written; edges at
  *                                         positions >= row_ptr[N] (no node)
  *                                         get zero gradients
- * Needs no workspace.  The per-edge arithmetic is the same as zs_backward's,
- * so both entry points return bitwise-equal gradients on the C == 32 path.
+ * Needs no workspace.  Gradients agree with zs_backward's to fp32 rounding
+ * (each is bitwise reproducible run to run).
  */
 ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float* rad,
                                  const int32_t* row_ptr, const int32_t* perm,

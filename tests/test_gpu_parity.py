@@ -283,13 +283,17 @@ def test_streams_are_honoured():
 
 
 @pytest.mark.parametrize("name", ["n4096", "zipf"])
-def test_backward_variants_bitwise_equal(name):
-    # the edge-order and CSR-order backward do the same per-edge arithmetic
+def test_backward_variants_agree(name):
+    # the edge-order and CSR-order backward sum in different orders: both
+    # within the tolerance of each other, each bitwise reproducible
     w = workloads.make_workload(name)
     dst, coup, rad, g = dev(w.dst), dev(w.coup), dev(w.rad), dev(w.grad_out)
     row_ptr, perm, _ = zs.zs_build_csr(dst, w.N)
     a = zs.zs_backward(g, coup, rad, dst, w.N)
     b = zs.zs_backward_csr(g, coup, rad, row_ptr, perm, w.N)
-    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
-    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    b2 = zs.zs_backward_csr(g, coup, rad, row_ptr, perm, w.N)
+    assert torch.equal(b[0], b2[0]) and torch.equal(b[1], b2[1])
+    _, _, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
+    assert_close(a[0].cpu().numpy(), b[0].cpu().numpy(), adc, "d_coup edge vs csr", tol=2 * TOL)
+    assert_close(a[1].cpu().numpy(), b[1].cpu().numpy(), adr, "d_rad edge vs csr", tol=2 * TOL)
     zs.zs_check_timeouts()
