@@ -29,13 +29,13 @@ constexpr int kFwdWarps = 8;
 constexpr int kFwdThreads = kFwdWarps * 32;
 // C == 32 path: warps per CTA (one CTA per SM), ring stages and edges per tile.
 #ifndef ZS_FWD_WARPS
-#define ZS_FWD_WARPS 14
+#define ZS_FWD_WARPS 16
 #endif
 #ifndef ZS_FWD_STAGES
 #define ZS_FWD_STAGES 2
 #endif
 #ifndef ZS_FWD_TILE
-#define ZS_FWD_TILE 16
+#define ZS_FWD_TILE 8
 #endif
 constexpr int kTmaWarps = ZS_FWD_WARPS;
 constexpr int kTmaStages = ZS_FWD_STAGES;
