@@ -19,6 +19,8 @@
 //     small kernel adds in CTA order.
 // Every sum is therefore formed in one fixed order: run to run bitwise
 // deterministic, no floating-point atomics.
+#include <mutex>
+
 #include "zs_common.cuh"
 #include "zs_tma.cuh"
 
@@ -455,4 +457,93 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, kGenWin, (const float*)part, out);
     }
     return check_launch("zs_forward");
+}
+
+// --------------------------------------------------------------------------
+// zs_forward_noalloc: zs_forward for callers that cannot allocate device
+// memory (for example code that runs where cudaMalloc is not allowed, such
+// as inside a region that must not touch the allocator, or a host framework
+// that owns all device memory and hands out only the tensors themselves).
+// The partial sums the forward keeps between its two kernels live in a
+// fixed, file-scope device array instead of a caller workspace.
+// --------------------------------------------------------------------------
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB, held by every GPU that loads the library
+static __device__ __align__(256) unsigned char g_forward_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_forward_scratch on the current device, looked up once per
+// device.  In host code the array's name is only a stand-in for the symbol.
+zs_status forward_scratch_address(float** out_ptr) {
+    static std::mutex mu;
+    static void* cached[128] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return fail(ZS_ERR_CUDA, "zs_forward_noalloc: cudaGetDevice: %s", cudaGetErrorString(err));
+    if (dev < 0 || dev >= 128) return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_forward_scratch);
+        if (err != cudaSuccess || !p)
+            return fail(ZS_ERR_CUDA, "zs_forward_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(err));
+        cached[dev] = p;
+    }
+    *out_ptr = static_cast<float*>(cached[dev]);
+    return ZS_OK;
+}
+
+}  // namespace
+
+extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
+                                        const int32_t* row_ptr, const int32_t* perm,
+                                        int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                        float* out, zs_stream_t stream) {
+    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: lmax=%d, only lmax=3 is supported", lmax);
+    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: E=%lld exceeds the int32 index range", (long long)E);
+    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: row_ptr is NULL");
+    if (N > 0 && !out) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: out is NULL");
+    if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: coup, rad or perm is NULL with E > 0");
+    if (N == 0) return ZS_OK;
+    const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
+    // the same split as zs_forward; the scratch holds one pair of partials per window
+    int64_t KW = 0, Wtot = 0, ctas = 0, windows = 0;
+    if (fast) {
+        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
+        KW = imax<int64_t>(ceil_div(E, warps_max), kTile);
+        Wtot = imax<int64_t>(ceil_div(E, KW), 1);
+        ctas = ceil_div(Wtot, kTmaWarps);
+        windows = ctas;
+    } else {
+        Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
+        ctas = ceil_div(Wtot, kFwdWarps);
+        windows = Wtot;
+    }
+    const size_t need = (size_t)windows * 2 * kRows * (size_t)C * sizeof(float);
+    if (need > kNoAllocScratchBytes)
+        return fail(ZS_ERR_INVALID_ARG,
+                    "zs_forward_noalloc: this call needs %zu bytes of scratch but the library's static scratch holds "
+                    "%zu; use zs_forward with a caller workspace", need, kNoAllocScratchBytes);
+    float* part = nullptr;
+    const zs_status st = forward_scratch_address(&part);
+    if (st != ZS_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int fix_grid = (int)imin<int64_t>(N, (int64_t)num_sms() * 8);
+    if (fast) {
+        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
+        static bool attr_set = false;
+        if (!attr_set) {
+            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            attr_set = true;
+        }
+        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part);
+        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, (int)(KW * kTmaWarps), (const float*)part, out);
+    } else {
+        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
+        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, kGenWin, (const float*)part, out);
+    }
+    return check_launch("zs_forward_noalloc");
 }

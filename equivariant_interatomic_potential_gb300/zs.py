@@ -63,6 +63,8 @@ def load(build_if_missing: bool = True):
         lib.zs_backward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P]
         lib.zs_backward_csr.restype = ctypes.c_int
         lib.zs_backward_csr.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P]
+        lib.zs_forward_noalloc.restype = ctypes.c_int
+        lib.zs_forward_noalloc.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P]
         lib.zs_check_timeouts.restype = ctypes.c_int
         lib.zs_check_timeouts.argtypes = []
         _lib = lib
@@ -206,3 +208,23 @@ def zs_backward_csr(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, row_
 def zs_check_timeouts() -> None:
     """Raise ZsError if a bounded device wait ran out since the last check (synchronises)."""
     _check("zs_check_timeouts", load().zs_check_timeouts())
+
+
+def zs_forward_noalloc(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,
+                       out: torch.Tensor, stream=None, lmax: int = 3):
+    """zs_forward with the library's static device scratch instead of a workspace.
+
+    For callers that cannot allocate device memory: ``out`` must be given,
+    nothing is allocated.  See include/zs.h for the size limit and the rule
+    that overlapping calls race.
+    """
+    E = coup.shape[0]
+    C = rad.shape[2]
+    _need(coup, "coup", torch.float32, (E, 15))
+    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    _need(out, "out", torch.float32, (N, 16, C))
+    _check("zs_forward_noalloc", load().zs_forward_noalloc(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm),
+                                                           E, N, C, lmax, _ptr(out), _stream(stream)))
+    return out

@@ -163,6 +163,31 @@ ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float*
                                  float* d_coup, float* d_rad, zs_stream_t stream);
 
 /*
+ * zs_forward without a workspace argument, for callers that cannot allocate
+ * device memory: code that must not call cudaMalloc or a caching allocator
+ * (for instance inside a region where allocation is forbidden or would
+ * synchronise, or a host framework that owns all device memory and passes
+ * in only the tensors).  The pages have no counterpart; this is a
+ * convenience of this library.
+ *   Arguments, results and errors as zs_forward (caller still passes the
+ *   inputs and out).  The partial sums zs_forward keeps in its workspace
+ *   live instead in one static device array of 4 MiB that every GPU
+ *   loading the library holds until the process exits.  C == 32 with
+ *   16-byte aligned rad, out and coup needs 3840 bytes per SM whatever E
+ *   is; other channel counts need 120*C bytes per 128 edges.  A call that
+ *   would need more returns ZS_ERR_INVALID_ARG and enqueues nothing.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the array: calls whose kernels overlap on the GPU
+ *   (other streams, other host threads) race and give wrong results.
+ *   Nothing in the array needs to start at zero.
+ */
+ZS_API zs_status zs_forward_noalloc(const float* coup, const float* rad,
+                                    const int32_t* row_ptr, const int32_t* perm,
+                                    int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                    float* out, zs_stream_t stream);
+
+/*
  * Reads and clears the device-side count of bounded waits that ran out.
  * The kernels that stream operands with asynchronous bulk copies wait for
  * them with an iteration limit; a wait that reaches its limit is counted
