@@ -276,6 +276,7 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
         // this group's node: n covers positions [.., b); G holds its rows 1..15
         int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
         int b = n < N ? __ldg(row_ptr + n + 1) : 0;
+        int c = 0;   // row_ptr[n + 2], fetched one node ahead
         float4 G[15];
         const float* gq = g + 4 * Q.q;
         auto load_g = [&]() {
@@ -285,6 +286,7 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
         };
         if (p0 < vend) {
             while (b <= p0) b = __ldg(row_ptr + (++n) + 1);
+            c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
             load_g();
         } else {
 #pragma unroll
@@ -304,7 +306,11 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
                 const bool in = j < jt;
                 const bool has_node = in && pos < vend;
                 if (has_node && pos >= b) {        // this group's edge starts a later node
-                    do { b = __ldg(row_ptr + (++n) + 1); } while (b <= pos);
+                    do {
+                        ++n;
+                        b = c;
+                        c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
+                    } while (b <= pos);
                     load_g();
                 }
                 const int2 m = metast[j];

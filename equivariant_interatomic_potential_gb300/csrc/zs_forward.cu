@@ -130,13 +130,16 @@ template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-            int E, int32_t N, int KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part) {
+            int E, int32_t N, int KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part,
+            int32_t* __restrict__ cross) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
+    __shared__ int cross_node;
     const int warp = threadIdx.x >> 5;
     const Lane32 L(threadIdx.x & 31);
     const int gw = blockIdx.x * W + warp;
     const bool active = gw < Wtot;
+    if (threadIdx.x == 0) cross_node = -1;
     pdl_wait();
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
@@ -157,14 +160,21 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
         for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, L.lane);
         // current node n covers positions [a, b); empty nodes this window owns
         // (those starting in it, or all trailing ones for the last window) are zeroed
-        int n = first_node(row_ptr, N, p0), a = 0, b = 0;
+        // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead
+        int n = first_node(row_ptr, N, p0);
+        int a = n < N ? __ldg(row_ptr + n) : 0;
+        int b = n < N ? __ldg(row_ptr + n + 1) : 0;
+        int c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
+        auto step = [&]() {
+            ++n;
+            a = b;
+            b = c;
+            c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
+        };
         auto advance = [&]() {
-            for (; n < N; ++n) {
-                a = __ldg(row_ptr + n);
-                b = __ldg(row_ptr + n + 1);
-                if (a != b) break;
-                if (a >= p1 && !is_last) break;
+            while (n < N && a == b && (a < p1 || is_last)) {
                 zero_node32(out + (int64_t)n * kNodeFloats32, L.lane);
+                step();
             }
         };
         advance();
@@ -199,7 +209,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    ++n;
+                    step();
                     advance();
                 }
             }
@@ -247,8 +257,11 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
             store_node32(out + (int64_t)m * kNodeFloats32, sum, L);
         } else {
             store_part32(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * kPartFloats32, sum, L);
+            if (ma >= P0 && L.lane == 0) cross_node = m;   // starts here, continues past this CTA
         }
     }
+    __syncthreads();
+    if (threadIdx.x == 0) cross[blockIdx.x] = cross_node;
 }
 
 // --------------------------------------------------------------------------
@@ -297,7 +310,8 @@ __device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, c
 __global__ void __launch_bounds__(kFwdThreads)
 fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
              const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-             int64_t E, int32_t N, int C, int Wtot, float* __restrict__ out, float* __restrict__ part) {
+             int64_t E, int32_t N, int C, int Wtot, float* __restrict__ out, float* __restrict__ part,
+             int32_t* __restrict__ cross) {
     __shared__ float cs[kFwdWarps][32][16];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kFwdWarps + warp;
@@ -308,6 +322,7 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
     const int64_t p0 = (int64_t)gw * kGenWin;
     const int64_t p1 = min(p0 + kGenWin, E);
     const bool is_last = gw == Wtot - 1;
+    int crossing = -1;   // the node that starts in this window and continues past it
     for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
         const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
         if (a >= p1 && !(is_last && a == b)) break;
@@ -332,65 +347,65 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
                 for (int r = 0; r < kRows; ++r) dstp[(int64_t)r * C + c] = acc[r];
             }
         }
+        if (!full && a >= p0) crossing = n;
         if (b > p1) break;
     }
+    if (lane == 0) cross[gw] = crossing;
 }
 
 // --------------------------------------------------------------------------
-// Cross-window fix-up: for each node whose positions span more than one
-// window of `win` positions, add its window partials in window order and
-// write rows 1..15 and the zero scalar row.  Partial k of a node is the one
-// of window floor(a/win) + k, slot 1 for k == 0 (the node starts inside it)
-// and slot 0 after (the node runs in from the previous window).
-// Warp w adds partials k = w, w+8, ...; the eight warp sums are then added
-// in warp order.
+// Cross-window fix-up, one CTA per window: window c's main kernel recorded in
+// cross[c] the node (if any) that starts in it and runs past its end.  That
+// node's partials are those of windows c, c+1, ..., floor((b-1)/win): slot 1
+// of window c (the node starts inside it), slot 0 of the later ones (it runs
+// in from the previous window).  Warp w adds partials k = w, w+8, ... in
+// order; the eight warp sums are then added in warp order, and rows 1..15 and
+// the zero scalar row are written.
 // --------------------------------------------------------------------------
 
 constexpr int kFixVals = 256;   // values per chunk: 8 per lane
 
 __global__ void __launch_bounds__(kFwdThreads)
-fwd_fixup(const int32_t* __restrict__ row_ptr, int32_t N, int C, int win,
+fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross, int C, int win,
           const float* __restrict__ part, float* __restrict__ out) {
     __shared__ float red[kFwdWarps][kFixVals];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t V = (int64_t)kRows * C;
+    const int wa = blockIdx.x;
     pdl_wait();
     pdl_trigger();
-    for (int n = blockIdx.x; n < N; n += gridDim.x) {
-        const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
-        if (a >= b) continue;
-        const int wa = a / win, wb = (b - 1) / win;
-        if (wa == wb) continue;
-        const int np = wb - wa + 1;
-        float* node = out + (int64_t)n * kD * C;
-        for (int c = threadIdx.x; c < C; c += kFwdThreads) node[c] = 0.f;
-        for (int64_t v0 = 0; v0 < V; v0 += kFixVals) {
-            float s[kFixVals / 32];
+    const int n = __ldg(cross + wa);
+    if (n < 0) return;
+    const int b = __ldg(row_ptr + n + 1);
+    const int np = (b - 1) / win - wa + 1;
+    float* node = out + (int64_t)n * kD * C;
+    for (int c = threadIdx.x; c < C; c += kFwdThreads) node[c] = 0.f;
+    for (int64_t v0 = 0; v0 < V; v0 += kFixVals) {
+        float sacc[kFixVals / 32];
 #pragma unroll
-            for (int i = 0; i < kFixVals / 32; ++i) s[i] = 0.f;
-            for (int k = warp; k < np; k += kFwdWarps) {
-                const float* p = part + ((int64_t)(wa + k) * 2 + (k == 0 ? 1 : 0)) * V + v0;
+        for (int i = 0; i < kFixVals / 32; ++i) sacc[i] = 0.f;
+        for (int k = warp; k < np; k += kFwdWarps) {
+            const float* p = part + ((int64_t)(wa + k) * 2 + (k == 0 ? 1 : 0)) * V + v0;
 #pragma unroll
-                for (int i = 0; i < kFixVals / 32; ++i) {
-                    const int64_t v = v0 + lane + 32 * i;
-                    if (v < V) s[i] += __ldg(p + lane + 32 * i);
-                }
+            for (int i = 0; i < kFixVals / 32; ++i) {
+                const int64_t v = v0 + lane + 32 * i;
+                if (v < V) sacc[i] += __ldg(p + lane + 32 * i);
             }
-#pragma unroll
-            for (int i = 0; i < kFixVals / 32; ++i) red[warp][lane + 32 * i] = s[i];
-            __syncthreads();
-            {
-                const int vl = threadIdx.x;   // kFwdThreads == kFixVals
-                const int64_t v = v0 + vl;
-                if (v < V) {
-                    float t = red[0][vl];
-#pragma unroll
-                    for (int w = 1; w < kFwdWarps; ++w) t += red[w][vl];
-                    node[C + v] = t;
-                }
-            }
-            __syncthreads();
         }
+#pragma unroll
+        for (int i = 0; i < kFixVals / 32; ++i) red[warp][lane + 32 * i] = sacc[i];
+        __syncthreads();
+        {
+            const int vl = threadIdx.x;   // kFwdThreads == kFixVals
+            const int64_t v = v0 + vl;
+            if (v < V) {
+                float t = red[0][vl];
+#pragma unroll
+                for (int w = 1; w < kFwdWarps; ++w) t += red[w][vl];
+                node[C + v] = t;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -404,14 +419,21 @@ unsigned int take_timeouts_forward() { return take_timeouts_local(); }
 
 using namespace zs;
 
+// Bytes of scratch for `windows` windows: a pair of (15 x C) partials and
+// one crossing-node entry per window.
+static size_t scratch_bytes(int64_t windows, int C) {
+    return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256) +
+           align_up((size_t)windows * sizeof(int32_t), 256);
+}
+
 extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
     if (E < 0 || N < 0 || C < 1) return 0;
     (void)N;
-    // One pair of (15 x C) partials per window: per warp window of kGenWin
-    // positions on the per-channel path, per CTA window of at least
-    // kTmaWarps * kTile positions on the C == 32 path.
+    // Sized for the smaller of the two window lengths: kGenWin positions per
+    // warp on the per-channel path, at least kTmaWarps * kTile per CTA on the
+    // C == 32 path.
     const int64_t windows = ceil_div(E > 0 ? E : 1, imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile)) + 1;
-    return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256);
+    return scratch_bytes(windows, C);
 }
 
 extern "C" zs_status zs_forward(const float* coup, const float* rad,
@@ -433,7 +455,6 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float* part = static_cast<float*>(workspace);
     const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
-    const int fix_grid = (int)imin<int64_t>(N, (int64_t)num_sms() * 8);
     if (fast) {
         // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
         // the same number of CSR positions (at least one tile).
@@ -441,6 +462,8 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
         const int64_t Wtot = imax<int64_t>(ceil_div(E, KW), 1);
         const int64_t ctas = ceil_div(Wtot, kTmaWarps);
+        int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
+                                                    align_up((size_t)ctas * 2 * kRows * C * sizeof(float), 256));
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static bool attr_set = false;
         if (!attr_set) {
@@ -448,13 +471,18 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
             attr_set = true;
         }
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part);
-        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, (int)(KW * kTmaWarps), (const float*)part, out);
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
+        launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
+               (int)(KW * kTmaWarps), (const float*)part, out);
     } else {
         const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
         const int64_t ctas = ceil_div(Wtot, kFwdWarps);
-        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
-        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, kGenWin, (const float*)part, out);
+        int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
+                                                    align_up((size_t)Wtot * 2 * kRows * C * sizeof(float), 256));
+        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
+               part, cross);
+        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C, kGenWin,
+               (const float*)part, out);
     }
     return check_launch("zs_forward");
 }
@@ -521,7 +549,7 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
         ctas = ceil_div(Wtot, kFwdWarps);
         windows = Wtot;
     }
-    const size_t need = (size_t)windows * 2 * kRows * (size_t)C * sizeof(float);
+    const size_t need = scratch_bytes(windows, C);
     if (need > kNoAllocScratchBytes)
         return fail(ZS_ERR_INVALID_ARG,
                     "zs_forward_noalloc: this call needs %zu bytes of scratch but the library's static scratch holds "
@@ -529,8 +557,9 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     float* part = nullptr;
     const zs_status st = forward_scratch_address(&part);
     if (st != ZS_OK) return st;
+    int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(part) +
+                                                align_up((size_t)windows * 2 * kRows * C * sizeof(float), 256));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int fix_grid = (int)imin<int64_t>(N, (int64_t)num_sms() * 8);
     if (fast) {
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static bool attr_set = false;
@@ -539,11 +568,14 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
             attr_set = true;
         }
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part);
-        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, (int)(KW * kTmaWarps), (const float*)part, out);
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
+        launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
+               (int)(KW * kTmaWarps), (const float*)part, out);
     } else {
-        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out, part);
-        launch(fwd_fixup, fix_grid, kFwdThreads, 0, s, row_ptr, N, C, kGenWin, (const float*)part, out);
+        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
+               part, cross);
+        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C, kGenWin,
+               (const float*)part, out);
     }
     return check_launch("zs_forward_noalloc");
 }

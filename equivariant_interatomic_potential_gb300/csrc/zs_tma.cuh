@@ -98,7 +98,7 @@ struct RingLayout {
 // One warp's stream of tiles over [p0, pe).
 template <int S, int T>
 struct TileRing {
-    static_assert(T >= 1 && T <= 32, "a tile is at most one edge per lane");
+    static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
     float* rad;        // [S][T][96]
     float* coup;       // [S][T][20]
     int2* meta;        // [S][T]: x = edge id (-1 if none), y = float offset of the row in its span
@@ -107,7 +107,10 @@ struct TileRing {
     int ntiles;        // tiles covering [p0, pe)
     int issued;        // tiles issued so far
     int consumed;      // tiles waited for so far
-    int pf;            // this lane's perm entry for tile `issued` (prefetched)
+    // perm entries are fetched 32 positions (kPB tiles) at a time, one block
+    // ahead: blk_cur holds the block of tile `issued`, blk_next the one after
+    static constexpr int kPB = 32 / T;
+    int blk_cur, blk_next;
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int pe_, int lane) {
         rad = reinterpret_cast<float*>(base);
@@ -124,9 +127,14 @@ struct TileRing {
         __syncwarp();
     }
 
+    __device__ __forceinline__ int load_block(const int32_t* __restrict__ perm, int blk, int lane) const {
+        const int j = p0 + blk * 32 + lane;
+        return (blk * kPB < ntiles && j < pe) ? ld_stream_i(perm + j) : -1;
+    }
+
     __device__ __forceinline__ void prefetch_perm(const int32_t* __restrict__ perm, int lane) {
-        const int j = p0 + issued * T + lane;
-        pf = (issued < ntiles && lane < T && j < pe) ? ld_stream_i(perm + j) : -1;
+        blk_cur = load_block(perm, 0, lane);
+        blk_next = load_block(perm, 1, lane);
     }
 
     // Issue the next tile into its stage (its previous tile must be consumed).
@@ -134,10 +142,14 @@ struct TileRing {
                                           const float* __restrict__ rad_g, int E, int lane) {
         if (issued >= ntiles) return;
         const int st = issued % S;
-        const int e = pf;
+        const int sub = issued % kPB;
+        const int e = __shfl_sync(0xffffffffu, blk_cur, (sub * T + lane) & 31);
         ++issued;
-        prefetch_perm(perm, lane);   // the next tile's entries, used at the next issue
-        const bool valid = (uint32_t)e < (uint32_t)E;
+        if (sub == kPB - 1) {        // last tile of this block: move on, fetch the block after next
+            blk_cur = blk_next;
+            blk_next = load_block(perm, issued / kPB + 1, lane);
+        }
+        const bool valid = lane < T && (uint32_t)e < (uint32_t)E;
         int64_t cstart = 0;
         int off = 0, nch = 0;
         bool tail = false;

@@ -173,9 +173,9 @@ ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float*
  *   inputs and out).  The partial sums zs_forward keeps in its workspace
  *   live instead in one static device array of 4 MiB that every GPU
  *   loading the library holds until the process exits.  C == 32 with
- *   16-byte aligned rad, out and coup needs 3840 bytes per SM whatever E
- *   is; other channel counts need 120*C bytes per 128 edges.  A call that
- *   would need more returns ZS_ERR_INVALID_ARG and enqueues nothing.
+ *   16-byte aligned rad, out and coup needs about 3.8 KB per SM whatever E
+ *   is; other channel counts need 120*C + 4 bytes per 256 edges.  A call
+ *   that would need more returns ZS_ERR_INVALID_ARG and enqueues nothing.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   Every call shares the array: calls whose kernels overlap on the GPU

@@ -112,9 +112,14 @@ def test_workspace_sizes(lib):
     tiles = -(-E // 2048)
     want = 4 * (-(-E * 4 // 256) * 256) + (-(-256 * tiles * 4 // 256) * 256) + 1024
     assert lib.zs_build_csr_workspace_bytes(E, 4096) == want
-    # forward: a pair of 15 x C partials per window of at least 128 CSR positions, plus one
-    assert lib.zs_forward_workspace_bytes(E, 4096, 32) == -(-((-(-E // 128) + 1) * 2 * 15 * 32 * 4) // 256) * 256
-    assert lib.zs_forward_workspace_bytes(0, 4096, 32) == 2 * 2 * 15 * 32 * 4
+    # forward: per window of at least 128 CSR positions (plus one), a pair of 15 x C
+    # partials and one crossing-node entry, each array 256-byte aligned
+    def ws(E, C):
+        w = -(-max(E, 1) // 128) + 1
+        return -(-(w * 2 * 15 * C * 4) // 256) * 256 + -(-(w * 4) // 256) * 256
+    assert lib.zs_forward_workspace_bytes(E, 4096, 32) == ws(E, 32)
+    assert lib.zs_forward_workspace_bytes(0, 4096, 32) == ws(0, 32)
+    assert lib.zs_forward_workspace_bytes(1000, 10, 40) == ws(1000, 40)
     assert lib.zs_forward_workspace_bytes(10, 4096, 0) == 0
 
 
