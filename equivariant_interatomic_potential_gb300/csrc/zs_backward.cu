@@ -266,8 +266,9 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
-    TileRing<S, T> ring;
+    TileRing<S, T, true> ring;
     ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, Q.lane);
+    const uint64_t pol_first = l2_evict_first(), pol_last = l2_evict_last();
     if (active) {
         ring.prefetch_perm(perm, Q.lane);
 #pragma unroll
@@ -346,11 +347,13 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
                     float* dc = d_coup + (int64_t)e * 15 + row;
                     float* dr = d_rad + (int64_t)e * (3 * kC32) + 4 * Q.q;
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    st_stream4(dr, has_node ? s0 : z);
-                    st_stream4(dr + kC32, has_node ? s1 : z);
-                    st_stream4(dr + 2 * kC32, has_node ? s2 : z);
-                    st_stream(dc, has_node ? t0 : 0.f);
-                    if (row + 1 < 15) st_stream(dc + 1, has_node ? t1 : 0.f);
+                    // d_rad rows are whole lines: stream them out.  d_coup rows are 60 bytes in
+                    // random order: keep their lines in L2 until neighbouring rows fill them
+                    st_hint4(dr, has_node ? s0 : z, pol_first);
+                    st_hint4(dr + kC32, has_node ? s1 : z, pol_first);
+                    st_hint4(dr + 2 * kC32, has_node ? s2 : z, pol_first);
+                    st_hint(dc, has_node ? t0 : 0.f, pol_last);
+                    if (row + 1 < 15) st_hint(dc + 1, has_node ? t1 : 0.f, pol_last);
                 }
             }
             ring.refill(perm, coup, rad, E, Q.lane);

@@ -5,7 +5,7 @@
 // order ("stable-sort CSR order", section "What").  Built here as an LSD
 // radix sort of destination keys with 8-bit digits, each pass in three
 // launches with no inter-CTA waiting:
-//   upsweep   -- per tile of 2048 keys, a 256-bin digit histogram (shared atomics)
+//   upsweep   -- per tile of keys, a 256-bin digit histogram (shared atomics)
 //   scan      -- per digit, exclusive scan of its histogram row over tiles
 //   downsweep -- per tile, stable rank of every key among equal digits
 //                (warp match + per-warp running counts), then scatter
@@ -20,8 +20,11 @@ namespace {
 
 constexpr int kCsrWarps = 8;
 constexpr int kCsrThreads = kCsrWarps * 32;
-constexpr int kCsrItems = 8;
-constexpr int kTile = kCsrWarps * kCsrItems * 32;  // 2048 keys per tile
+#ifndef ZS_CSR_ITEMS
+#define ZS_CSR_ITEMS 8
+#endif
+constexpr int kCsrItems = ZS_CSR_ITEMS;
+constexpr int kTile = kCsrWarps * kCsrItems * 32;  // keys per tile
 constexpr int kRadix = 256;
 
 __device__ __forceinline__ int32_t key_of(const int32_t* keys_in, int64_t idx, int32_t N, bool first) {
@@ -166,19 +169,28 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
 
 // row_ptr from sorted keys: position j is the first of every node in
 // (key[j-1], key[j]]; the count of keys equal to N (invalid) is E - row_ptr[N].
+// Each thread looks at kRowPtrPer consecutive positions.
+constexpr int kRowPtrPer = 4;
+
 __global__ void __launch_bounds__(256)
 csr_row_ptr(const int32_t* __restrict__ sorted, int64_t E, int32_t N,
             int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kRowPtrPer;
     pdl_wait();
     pdl_trigger();
-    if (j > E) return;
-    const int64_t kprev = j > 0 ? (int64_t)sorted[j - 1] : -1;
-    const int64_t kcur = j < E ? (int64_t)sorted[j] : (int64_t)N + 1;
-    const int64_t hi = kcur < (int64_t)N ? kcur : (int64_t)N;
-    for (int64_t n = kprev + 1; n <= hi; ++n) {
-        row_ptr[n] = (int32_t)j;
-        if (n == N && bad) *bad = (int32_t)(E - j);
+    if (j0 > E) return;
+    int64_t kprev = j0 > 0 ? (int64_t)__ldg(sorted + j0 - 1) : -1;
+#pragma unroll
+    for (int i = 0; i < kRowPtrPer; ++i) {
+        const int64_t j = j0 + i;
+        if (j > E) break;
+        const int64_t kcur = j < E ? (int64_t)__ldg(sorted + j) : (int64_t)N + 1;
+        const int64_t hi = kcur < (int64_t)N ? kcur : (int64_t)N;
+        for (int64_t n = kprev + 1; n <= hi; ++n) {
+            row_ptr[n] = (int32_t)j;
+            if (n == N && bad) *bad = (int32_t)(E - j);
+        }
+        kprev = kcur;
     }
 }
 
@@ -251,7 +263,7 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
         }
         sorted = kin;
     }
-    const int64_t threads = E + 1;
+    const int64_t threads = (E + 1 + kRowPtrPer - 1) / kRowPtrPer;
     launch(csr_row_ptr, (unsigned)((threads + 255) / 256), 256, 0, s, sorted, E, N, row_ptr, bad_dst_count);
     return check_launch("zs_build_csr");
 }

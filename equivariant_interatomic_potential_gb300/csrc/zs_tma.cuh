@@ -71,8 +71,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "l"(pol) : "memory");
 }
 
 // Arrive on bar once every cp.async this thread issued so far has landed.
@@ -80,9 +80,9 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
 }
 
 // Shared-memory layout of one warp's ring of S stages of T edges.
@@ -95,8 +95,9 @@ struct RingLayout {
     static constexpr int kBytes = (kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
 };
 
-// One warp's stream of tiles over [p0, pe).
-template <int S, int T>
+// One warp's stream of tiles over [p0, pe).  kEvictFirst marks every byte
+// the ring brings in as evict-first in L2 (it is read exactly once).
+template <int S, int T, bool kEvictFirst = false>
 struct TileRing {
     static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
     float* rad;        // [S][T][96]
@@ -111,6 +112,7 @@ struct TileRing {
     // ahead: blk_cur holds the block of tile `issued`, blk_next the one after
     static constexpr int kPB = 32 / T;
     int blk_cur, blk_next;
+    uint64_t pol;      // L2 policy of the ring's copies
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int pe_, int lane) {
         rad = reinterpret_cast<float*>(base);
@@ -122,6 +124,7 @@ struct TileRing {
         ntiles = pe > p0 ? (pe - p0 + T - 1) / T : 0;
         issued = 0;
         consumed = 0;
+        pol = kEvictFirst ? l2_evict_first() : l2_evict_normal();
         if (lane < S) mbar_init(bar0 + 8 * lane, kRingArrivals);
         mbar_fence_init();
         __syncwarp();
@@ -129,7 +132,7 @@ struct TileRing {
 
     __device__ __forceinline__ int load_block(const int32_t* __restrict__ perm, int blk, int lane) const {
         const int j = p0 + blk * 32 + lane;
-        return (blk * kPB < ntiles && j < pe) ? ld_stream_i(perm + j) : -1;
+        return (blk * kPB < ntiles && j < pe) ? ld_hint_i(perm + j, pol) : -1;
     }
 
     __device__ __forceinline__ void prefetch_perm(const int32_t* __restrict__ perm, int lane) {
@@ -185,15 +188,15 @@ struct TileRing {
         if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadRowBytes);
         __syncwarp();
         if (valid) {
-            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * 96, kRadRowBytes, bar);
+            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * 96, kRadRowBytes, bar, pol);
             if (!tail) {
                 const char* src = reinterpret_cast<const char*>(coup_g) + cstart;
                 const uint32_t dst = smem_u32(cslot);
-                cp_async16(dst, src);
-                cp_async16(dst + 16, src + 16);
-                cp_async16(dst + 32, src + 32);
-                cp_async16(dst + 48, src + 48);
-                if (nch == 5) cp_async16(dst + 64, src + 64);
+                cp_async16(dst, src, pol);
+                cp_async16(dst + 16, src + 16, pol);
+                cp_async16(dst + 32, src + 32, pol);
+                cp_async16(dst + 48, src + 48, pol);
+                if (nch == 5) cp_async16(dst + 64, src + 64, pol);
             }
         }
         cp_async_arrive(bar);
