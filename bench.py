@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "zonal-scatter fwd+bwd edges/s at N=4096,E=647170,C=32; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = {
     "fwd": "equivariant_interatomic_potential_gb300/csrc/zs_forward.cu",
     "bwd_csr": "equivariant_interatomic_potential_gb300/csrc/zs_backward.cu",
@@ -84,6 +85,32 @@ def ncu_traffic(kernel_key: str, workload: str):
         return int(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+# ---------------------------------------------------------------- ranks
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Maximum of a per-rank scalar over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return world * units_per_rank * steps / (max_ms / 1e3)
+
+
+def workload_config(w, backward: str) -> dict:
+    entry = "zs_backward_csr" if backward == "csr" else "zs_backward"
+    return {"workload": f"{w.name}: N={w.N}, E={w.E}, C={w.C}, lmax=3 (rows 3/5/7), fp32, seed {w.seed}",
+            "step": "zs_build_csr + zs_forward + " + entry,
+            "l2": ("inputs larger than L2" if w.coup.nbytes + w.rad.nbytes > L2_BYTES else
+                   "inputs smaller than L2, no flush") + " (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6)}
 
 
 # ---------------------------------------------------------------- clocks
@@ -286,21 +313,14 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         b.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (h_dst, h_coup, h_rad, h_g))
         d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dc, h_dr))
-        e2e = {"value": world * E * args.steps / (e2e_ms / 1e3), "unit": "edges/s",
+        e2e = {"value": job_throughput(E, args.steps, e2e_ms, world), "unit": "edges/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps}
 
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = reduce_max(total_ms, world, dev)
     if rank != 0:
         return None
 
@@ -325,7 +345,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
     res = {
         "metric": METRIC,
-        "value": world * E * args.steps / (total_ms / 1e3),
+        "value": job_throughput(E, args.steps, total_ms, world),
         "unit": "edges/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -336,10 +356,8 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{args.config}: N={N}, E={E}, C={C}, lmax=3 (rows 3/5/7), fp32, seed {w.seed}",
-                   "step": "zs_build_csr + zs_forward + " + bwd_entry,
-                   "l2": "inputs larger than L2 (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": dict(workload_config(w, args.backward),
+                       parallelism="replicas" if world > 1 else "single GPU"),
         "fwd_bwd_edges_per_s": E / (fwd_bwd_us * 1e-6),
         "kernels": kernels,
         "roofline": roof,
@@ -352,13 +370,13 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def run_oracle(config: str, min_seconds: float) -> dict:
+def run_oracle(config: str, min_seconds: float, w=None) -> dict:
     """The fp64 oracle (single-threaded C) on the full graph, repeated until
     min_seconds of CPU work has been timed."""
     import oracle
     from equivariant_interatomic_potential_gb300 import workloads
 
-    w = workloads.make_workload(config)
+    w = workloads.make_workload(config) if w is None else w
     oracle.build()
     reps, t_csr, t_fwd, t_bwd = 0, 0.0, 0.0, 0.0
     while reps == 0 or (t_csr + t_fwd + t_bwd) < min_seconds:
@@ -406,23 +424,23 @@ def main():
         # the oracle on the host cores, rank 0 only
         if rank != 0:
             return
+        from equivariant_interatomic_potential_gb300 import workloads
+        w = workloads.make_workload(args.config)
         t0 = time.perf_counter()
         steps = []
-        base = None
         for i in range(args.warmup + args.steps):
-            r = run_oracle(args.config, 0.0)
+            r = run_oracle(args.config, 0.0, w)
             if i >= args.warmup:
                 steps.append(r["ms_per_step"])
-            base = r
-        E = {"tiny": 2048, "n1000": 158002, "n4096": 647170, "zipf": 647170, "large": 5177344}[args.config]
         ms = statistics.mean(steps)
-        val = E / (ms / 1e3)
+        val = w.E / (ms / 1e3)
+        sample = (f"full {w.name} graph (N={w.N}, E={w.E}, C={w.C}) per step: csr build, forward, backward, "
+                  f"fp64 sequential C, {args.steps} timed steps after {args.warmup} warm-up")
         res = {"impl": "reference", "metric": METRIC, "value": val, "unit": "edges/s", "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-               "config": {"workload": f"{args.config}", "step": "csr_build + forward + backward"},
-               "cpu_baseline": {"value": val, "unit": "edges/s", "cores": 1, "kind": "oracle",
-                                "sample": base["sample"].split(",")[0] + ", one repetition per step"},
+               "config": dict(workload_config(w, args.backward), parallelism="replicas" if world > 1 else "single GPU"),
+               "cpu_baseline": {"value": val, "unit": "edges/s", "cores": 1, "kind": "oracle", "sample": sample},
                "e2e": {"value": val, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                "wall_s": time.perf_counter() - t0}
         print(json.dumps(res))
