@@ -441,11 +441,8 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
         const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
         const int64_t ctas = (Wtot + W - 1) / W;
         const int smem = W * RingLayout<S, T>::kBytes;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaFuncSetAttribute(bwd_csr_c32_tma<W, S, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            attr_set = true;
-        }
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_csr_c32_tma<W, S, T>, smem, attr_done);
         launch(bwd_csr_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
                (int)KW, (int)Wtot, d_coup, d_rad);
     } else {

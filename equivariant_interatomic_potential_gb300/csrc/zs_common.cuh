@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "zs.h"
@@ -122,16 +123,35 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int64_t 
     return lo;
 }
 
+constexpr int kMaxDevices = 128;
+
+inline int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return (dev >= 0 && dev < kMaxDevices) ? dev : 0;
+}
+
+// Number of SMs of the current device (looked up once per device).
 inline int num_sms() {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int v = 0;
+    static std::atomic<int> cached[kMaxDevices];
+    const int dev = current_device();
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached = v > 0 ? v : 1;
+        if (v <= 0) v = 1;
+        cached[dev].store(v, std::memory_order_relaxed);
     }
-    return cached;
+    return v;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+inline void set_smem_limit_once(K kernel, int bytes, std::atomic<bool>* done) {
+    const int dev = current_device();
+    if (!done[dev].load(std::memory_order_acquire)) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        done[dev].store(true, std::memory_order_release);
+    }
 }
 
 template <class T>

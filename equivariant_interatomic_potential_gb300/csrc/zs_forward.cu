@@ -465,11 +465,8 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
                                                     align_up((size_t)ctas * 2 * kRows * C * sizeof(float), 256));
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            attr_set = true;
-        }
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
                coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
         launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
@@ -562,11 +559,8 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fast) {
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaFuncSetAttribute(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            attr_set = true;
-        }
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
                coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
         launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
