@@ -8,7 +8,7 @@
 //   upsweep   -- per tile of keys, a 256-bin digit histogram (shared atomics)
 //   scan      -- per digit, exclusive scan of its histogram row over tiles
 //   downsweep -- per tile, stable rank of every key among equal digits
-//                (warp match + per-warp running counts), then scatter
+//                (warp ballots + per-warp running counts), then scatter
 // and a final pass that reads the sorted keys to write row_ptr.
 // Every step is integer arithmetic in a fixed order, so perm is unique and
 // bit-identical to a sequential counting sort.  Keys outside [0, N) sort as
@@ -31,6 +31,19 @@ __device__ __forceinline__ int32_t key_of(const int32_t* keys_in, int64_t idx, i
     int32_t k = __ldg(keys_in + idx);
     if (first) k = (k >= 0 && k < N) ? k : N;
     return k;
+}
+
+// Lanes of the warp holding the same 8-bit digit as this lane (valid lanes
+// only), from one ballot per digit bit (cheaper here than a match instruction).
+__device__ __forceinline__ unsigned digit_peers(int dig, bool valid) {
+    unsigned peers = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const bool bit = (dig >> b) & 1;
+        const unsigned bal = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? bal : ~bal;
+    }
+    return peers;
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -139,7 +152,7 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
         key[i] = valid ? key_of(keys_in, idx, N, kFirst) : 0;
         val[i] = valid ? (kFirst ? (int32_t)idx : __ldg(vals_in + idx)) : 0;
         dig[i] = valid ? ((key[i] >> shift) & (kRadix - 1)) : kRadix;
-        const unsigned peers = __match_any_sync(0xffffffffu, dig[i]);
+        const unsigned peers = digit_peers(dig[i] & (kRadix - 1), valid);
         rank[i] = valid ? cnt[warp][dig[i]] + __popc(peers & lt) : 0;
         __syncwarp();
         if (valid && lane == __ffs(peers) - 1) cnt[warp][dig[i]] += __popc(peers);
