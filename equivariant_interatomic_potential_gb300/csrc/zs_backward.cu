@@ -5,9 +5,10 @@
 // section "What", backward bullet: both operand gradients in a single
 // edge-parallel kernel, no materialised message gradient).
 //
-// Edges are taken in their own order, 32 consecutive edges per warp step, so
-// coup, rad, dst, d_coup and d_rad stream through HBM contiguously; the only
-// gathered operand is g (N x 16 x C, a few MB, resident in L2).
+// zs_backward takes the edges in their own order, so coup, rad, dst, d_coup
+// and d_rad stream through HBM contiguously and the only gathered operand is
+// g (N x 16 x C, a few MB, resident in L2).  zs_backward_csr visits them in
+// destination order instead and reads each node's g once per run of edges.
 #include "zs_common.cuh"
 #include "zs_tma.cuh"
 
@@ -16,6 +17,16 @@ namespace {
 
 constexpr int kBwdWarps = 8;
 // CSR-order C == 32 path: warps per CTA (one CTA per SM), ring stages, edges per tile.
+// Edge-order C == 32 path: warps per CTA, stages, edges per tile.
+#ifndef ZS_BWDE_WARPS
+#define ZS_BWDE_WARPS 8
+#endif
+#ifndef ZS_BWDE_STAGES
+#define ZS_BWDE_STAGES 3
+#endif
+#ifndef ZS_BWDE_TILE
+#define ZS_BWDE_TILE 4
+#endif
 #ifndef ZS_BWD_WARPS
 #define ZS_BWD_WARPS 16
 #endif
@@ -28,109 +39,6 @@ constexpr int kBwdWarps = 8;
 constexpr int kBwdThreads = kBwdWarps * 32;
 constexpr int kC32 = 32;
 constexpr unsigned kFull = 0xffffffffu;
-
-// --------------------------------------------------------------------------
-// C == 32 path.  Lane layout as in the forward: group g = lane/8 owns zonal
-// rows 4g..4g+3 (row 15 padding), quad q = lane%8 owns channels 4q..4q+3.
-// --------------------------------------------------------------------------
-template <int U>
-__global__ void __launch_bounds__(kBwdThreads, 2)
-bwd_c32(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
-        const int32_t* __restrict__ dst, int64_t E, int32_t N,
-        float* __restrict__ d_coup, float* __restrict__ d_rad) {
-    __shared__ __align__(16) float cs[kBwdWarps][32][16];
-    __shared__ float dcs[kBwdWarps][32 * 15];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 3, q = lane & 7;
-    const int slo = gq == 0 ? 0 : (gq == 1 ? 1 : 2);
-    const int src_hi = gq == 0 ? lane + 8 : lane;
-    const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0;
-    const int my_row = 4 * gq + (b2 ? 2 : 0) + (b1 ? 1 : 0);   // row this lane holds after the reduction
-    const bool row_writer = (lane & 1) == 0 && my_row < 15;
-    cs[warp][lane][15] = 0.f;
-    __syncwarp();
-    pdl_wait();
-    pdl_trigger();
-
-    const int64_t nbatch = (E + 31) / 32;
-    for (int64_t bt = (int64_t)blockIdx.x * kBwdWarps + warp; bt < nbatch; bt += (int64_t)gridDim.x * kBwdWarps) {
-        const int64_t e0 = bt * 32;
-        const int cnt = (int)imin<int64_t>(32, E - e0);
-        int d_l = -1;
-        if (lane < cnt) {
-            d_l = ld_stream_i(dst + e0 + lane);
-            if (d_l < 0 || d_l >= N) d_l = -1;
-        }
-        const float* cblk = coup + e0 * 15;
-#pragma unroll
-        for (int it = 0; it < 15; ++it) {
-            const int v = it * 32 + lane;
-            const int j = v / 15;
-            cs[warp][j][v - j * 15] = v < cnt * 15 ? ld_stream(cblk + v) : 0.f;
-        }
-        __syncwarp();
-
-        for (int j0 = 0; j0 < cnt; j0 += U) {
-            float4 gr[U][4], a[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u;
-                const int d = __shfl_sync(kFull, d_l, j & 31);
-                const bool in = j < cnt;
-                const float* gn = g + (int64_t)(d < 0 ? 0 : d) * (16 * kC32) + 4 * q;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 4 * gq + i;
-                    gr[u][i] = (in && d >= 0 && r < 15) ? ld_ro4(gn + (1 + r) * kC32)
-                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                a[u] = in ? ld_stream4(rad + (e0 + j) * (3 * kC32) + slo * kC32 + 4 * q)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u;
-                const int d = __shfl_sync(kFull, d_l, j & 31);
-                const bool ok = j < cnt && d >= 0;
-                const float4 bb = f4_shfl(a[u], src_hi);
-                const float4 c4 = *reinterpret_cast<const float4*>(&cs[warp][j & 31][4 * gq]);
-                // d_coup: four row dot products over this lane's 4 channels,
-                // then a transposed butterfly over the 8 lanes of the group.
-                const float p0 = f4_dot(gr[u][0], a[u]);
-                const float p1 = f4_dot(gr[u][1], a[u]);
-                const float p2 = f4_dot(gr[u][2], a[u]);
-                const float p3 = f4_dot(gr[u][3], bb);
-                const float x0 = b2 ? p0 : p2, x1 = b2 ? p1 : p3;
-                const float k0 = (b2 ? p2 : p0) + __shfl_xor_sync(kFull, x0, 4);
-                const float k1 = (b2 ? p3 : p1) + __shfl_xor_sync(kFull, x1, 4);
-                float m = (b1 ? k1 : k0) + __shfl_xor_sync(kFull, b1 ? k0 : k1, 2);
-                m += __shfl_xor_sync(kFull, m, 1);
-                if (row_writer && j < cnt) dcs[warp][(j & 31) * 15 + my_row] = ok ? m : 0.f;
-                // d_rad: rows of the group weighted by their coupling, then the
-                // degree-2 slot adds group 0's row 3 and the degree-3 slot adds group 3.
-                float4 lo = make_float4(c4.x * gr[u][0].x, c4.x * gr[u][0].y, c4.x * gr[u][0].z, c4.x * gr[u][0].w);
-                lo = f4_fma(c4.y, gr[u][1], lo);
-                lo = f4_fma(c4.z, gr[u][2], lo);
-                const float4 hi = make_float4(c4.w * gr[u][3].x, c4.w * gr[u][3].y, c4.w * gr[u][3].z, c4.w * gr[u][3].w);
-                const float4 both = f4_add(lo, hi);
-                const float4 y = f4_shfl_xor(gq == 0 ? hi : both, 8);
-                if (gq < 3 && j < cnt) {
-                    float4 res = gq == 0 ? lo : (gq == 1 ? f4_add(y, both) : f4_add(both, y));
-                    if (!ok) res = make_float4(0.f, 0.f, 0.f, 0.f);
-                    st_stream4(d_rad + (e0 + j) * (3 * kC32) + gq * kC32 + 4 * q, res);
-                }
-            }
-        }
-        __syncwarp();
-        float* dblk = d_coup + e0 * 15;
-#pragma unroll
-        for (int it = 0; it < 15; ++it) {
-            const int v = it * 32 + lane;
-            if (v < cnt * 15) st_stream(dblk + v, dcs[warp][v]);
-        }
-        __syncwarp();
-    }
-}
 
 // --------------------------------------------------------------------------
 // Per-channel path (any C, any alignment): lane = channel within a chunk of
@@ -362,6 +270,203 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     ring.drain();
 }
 
+// --------------------------------------------------------------------------
+// Edge-order C == 32 backward fed by bulk copies.  A warp owns a window of
+// consecutive edges and streams it in tiles of T edges (T a multiple of 4,
+// tiles start at multiples of 4 so every block below is 16-byte aligned):
+// per tile one bulk copy of the T radial rows, one of the T coupling rows,
+// and per edge one bulk copy of its destination's cotangent rows 1..15
+// (1920 bytes, gathered from L2).  dst is read ahead with plain loads, 32
+// edges at a time, since the gathers need it.  The lane layout is the one of
+// the CSR-order kernel: one edge per 8-lane group, all 15 rows per lane.
+// --------------------------------------------------------------------------
+
+template <int S, int T>
+struct EdgeRingLayout {
+    static constexpr int kG = S * T * 15 * kC32 * 4;   // cotangent rows 1..15 per edge
+    static constexpr int kRad = S * T * 3 * kC32 * 4;
+    static constexpr int kCoup = S * T * 15 * 4;
+    static constexpr int kMeta = S * T * 4;
+    static constexpr int kBars = S * 8;
+    static constexpr int kBytes = (kG + kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
+};
+
+template <int S, int T>
+struct EdgeRing {
+    static_assert(T % 4 == 0 && 32 % T == 0, "tiles of whole quads that divide 32");
+    static constexpr int kPB = 32 / T;
+    float* gs;      // [S][T][15*32]
+    float* rads;    // [S][T][96]
+    float* coups;   // [S][T*15]
+    int* meta;      // [S][T]: destination, -1 for an edge without a node, -2 past the window
+    uint32_t bar0;
+    int p0, p1, ntiles, issued, consumed;
+    int blk_cur, blk_next;   // dst of the 32 edges of the current / next block
+    uint64_t pol_stream, pol_g;
+
+    __device__ __forceinline__ void init(unsigned char* base, int p0_, int p1_, int lane) {
+        gs = reinterpret_cast<float*>(base);
+        rads = reinterpret_cast<float*>(base + EdgeRingLayout<S, T>::kG);
+        coups = reinterpret_cast<float*>(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad);
+        meta = reinterpret_cast<int*>(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad +
+                                      EdgeRingLayout<S, T>::kCoup);
+        bar0 = smem_u32(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad + EdgeRingLayout<S, T>::kCoup +
+                        EdgeRingLayout<S, T>::kMeta);
+        p0 = p0_;
+        p1 = p1_;
+        ntiles = p1 > p0 ? (p1 - p0 + T - 1) / T : 0;
+        issued = 0;
+        consumed = 0;
+        pol_stream = l2_evict_first();
+        pol_g = l2_evict_last();
+        if (lane < S) mbar_init(bar0 + 8 * lane, 1);
+        mbar_fence_init();
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ int load_block(const int32_t* __restrict__ dst, int blk, int lane) const {
+        const int j = p0 + blk * 32 + lane;
+        return (blk * kPB < ntiles && j < p1) ? ld_hint_i(dst + j, pol_stream) : -1;
+    }
+
+    __device__ __forceinline__ void prefetch(const int32_t* __restrict__ dst, int lane) {
+        blk_cur = load_block(dst, 0, lane);
+        blk_next = load_block(dst, 1, lane);
+    }
+
+    __device__ __forceinline__ void issue(const int32_t* __restrict__ dst, const float* __restrict__ coup_g,
+                                          const float* __restrict__ rad_g, const float* __restrict__ g_g,
+                                          int N, int lane) {
+        if (issued >= ntiles) return;
+        const int k = issued;
+        const int st = k % S;
+        const int sub = k % kPB;
+        const int d = __shfl_sync(0xffffffffu, blk_cur, (sub * T + lane) & 31);
+        ++issued;
+        if (sub == kPB - 1) {
+            blk_cur = blk_next;
+            blk_next = load_block(dst, issued / kPB + 1, lane);
+        }
+        const int e0 = p0 + k * T;
+        const int cnt = imin(T, p1 - e0);
+        const bool in = lane < cnt;
+        const bool valid = in && d >= 0 && d < N;
+        const bool full = cnt == T;
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        const uint32_t bytes = (uint32_t)cnt * 384u + (full ? (uint32_t)T * 60u : 0u) + nvalid * 1920u;
+        const uint32_t bar = bar0 + 8 * st;
+        float* cst = coups + st * T * 15;
+        if (lane < T) meta[st * T + lane] = valid ? d : (in ? -1 : -2);
+        if (!full && in) {   // ragged last tile: its coupling block is not a whole number of 16-byte pieces
+            const float* src = coup_g + (int64_t)(e0 + lane) * 15;
+#pragma unroll
+            for (int r = 0; r < 15; ++r) cst[lane * 15 + r] = __ldg(src + r);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(rads + st * T * 96), rad_g + (int64_t)e0 * 96, (uint32_t)cnt * 384u, bar, pol_stream);
+            if (full) bulk_g2s(smem_u32(cst), coup_g + (int64_t)e0 * 15, (uint32_t)T * 60u, bar, pol_stream);
+        }
+        __syncwarp();
+        if (valid)
+            bulk_g2s(smem_u32(gs + (st * T + lane) * (15 * kC32)), g_g + (int64_t)d * (16 * kC32) + kC32, 1920u,
+                     bar, pol_g);
+    }
+
+    __device__ __forceinline__ int acquire() {
+        const int k = consumed++;
+        const int st = k % S;
+        mbar_wait(bar0 + 8 * st, (uint32_t)((k / S) & 1));
+        __syncwarp();
+        return st;
+    }
+
+    __device__ __forceinline__ void drain() {
+        while (consumed < issued) {
+            const int st = consumed % S;
+            mbar_wait(bar0 + 8 * st, (uint32_t)((consumed / S) & 1));
+            ++consumed;
+        }
+        __syncwarp();
+    }
+};
+
+template <int W, int S, int T>
+__global__ void __launch_bounds__(W * 32, 1)
+bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+                 const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
+                 float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const QuadLane Q(threadIdx.x & 31);
+    const int gw = blockIdx.x * W + warp;
+    const bool active = gw < Wtot;
+    pdl_wait();
+    pdl_trigger();
+    const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
+    const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
+    EdgeRing<S, T> ring;
+    ring.init(smem + (size_t)warp * EdgeRingLayout<S, T>::kBytes, p0, p1, Q.lane);
+    const uint64_t pol_out = l2_evict_first();
+    if (active) {
+        ring.prefetch(dst, Q.lane);
+#pragma unroll
+        for (int i = 0; i < S; ++i) ring.issue(dst, coup, rad, g, N, Q.lane);
+        for (int k = 0; k < ring.ntiles; ++k) {
+            const int st = ring.acquire();
+            const int e0 = p0 + k * T;
+#pragma unroll
+            for (int i = 0; i < T / 4; ++i) {
+                const int j = 4 * i + Q.grp;
+                const int m = ring.meta[st * T + j];
+                const float* gj = ring.gs + (st * T + j) * (15 * kC32) + 4 * Q.q;
+                float4 G[15];
+#pragma unroll
+                for (int r = 0; r < 15; ++r) G[r] = *reinterpret_cast<const float4*>(gj + r * kC32);
+                const float* rrow = ring.rads + (st * T + j) * 96 + 4 * Q.q;
+                const float4 a0 = *reinterpret_cast<const float4*>(rrow);
+                const float4 a1 = *reinterpret_cast<const float4*>(rrow + kC32);
+                const float4 a2 = *reinterpret_cast<const float4*>(rrow + 2 * kC32);
+                const float* crow = ring.coups + st * T * 15 + j * 15;
+                float c[15];
+#pragma unroll
+                for (int r = 0; r < 15; ++r) c[r] = crow[r];
+                float4 s0 = make_float4(c[0] * G[0].x, c[0] * G[0].y, c[0] * G[0].z, c[0] * G[0].w);
+                s0 = f4_fma(c[1], G[1], s0);
+                s0 = f4_fma(c[2], G[2], s0);
+                float4 s1 = make_float4(c[3] * G[3].x, c[3] * G[3].y, c[3] * G[3].z, c[3] * G[3].w);
+#pragma unroll
+                for (int r = 4; r < 8; ++r) s1 = f4_fma(c[r], G[r], s1);
+                float4 s2 = make_float4(c[8] * G[8].x, c[8] * G[8].y, c[8] * G[8].z, c[8] * G[8].w);
+#pragma unroll
+                for (int r = 9; r < 15; ++r) s2 = f4_fma(c[r], G[r], s2);
+                float pr[16];
+#pragma unroll
+                for (int r = 0; r < 15; ++r) pr[r] = f4_dot(G[r], r < 3 ? a0 : (r < 8 ? a1 : a2));
+                pr[15] = 0.f;
+                float t0, t1;
+                group_reduce16(pr, Q, t0, t1);
+                if (m == -2) continue;
+                const bool ok = m >= 0;
+                const int64_t e = e0 + j;
+                const int row = 8 * Q.b2 + 4 * Q.b1 + 2 * Q.b0;
+                float* dc = d_coup + e * 15 + row;
+                float* dr = d_rad + e * (3 * kC32) + 4 * Q.q;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                st_hint4(dr, ok ? s0 : z, pol_out);
+                st_hint4(dr + kC32, ok ? s1 : z, pol_out);
+                st_hint4(dr + 2 * kC32, ok ? s2 : z, pol_out);
+                st_stream(dc, ok ? t0 : 0.f);
+                if (row + 1 < 15) st_stream(dc + 1, ok ? t1 : 0.f);
+            }
+            __syncwarp();
+            ring.issue(dst, coup, rad, g, N, Q.lane);
+        }
+    }
+    ring.drain();
+}
+
 // Per-channel CSR-order backward (any C, any alignment): same walk, no TMA.
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
@@ -407,12 +512,18 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
     if (!coup || !rad || !dst || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward: NULL array with E > 0");
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward: g is NULL with N > 0");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad);
-    const int64_t nbatch = (E + 31) / 32;
+    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
-        const int64_t want = (nbatch + kBwdWarps - 1) / kBwdWarps;
-        const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 2);
-        launch(bwd_c32<4>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, d_coup, d_rad);
+        constexpr int W = ZS_BWDE_WARPS, S = ZS_BWDE_STAGES, T = ZS_BWDE_TILE;
+        const int64_t warps_max = (int64_t)num_sms() * W;
+        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
+        const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
+        const int64_t ctas = (Wtot + W - 1) / W;
+        const int smem = W * EdgeRingLayout<S, T>::kBytes;
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_edge_c32_tma<W, S, T>, smem, attr_done);
+        launch(bwd_edge_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
+               (int)Wtot, d_coup, d_rad);
     } else {
         const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
         const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
