@@ -408,7 +408,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--config", default="n4096")
     ap.add_argument("--impl", default="zs", choices=["zs", "reference"])
-    ap.add_argument("--backward", default="csr", choices=["csr", "edge"],
+    ap.add_argument("--backward", default="edge", choices=["csr", "edge"],
                     help="backward entry point timed in the step (the other is timed alongside)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -17,16 +17,6 @@ namespace {
 
 constexpr int kBwdWarps = 8;
 // CSR-order C == 32 path: warps per CTA (one CTA per SM), ring stages, edges per tile.
-// Edge-order C == 32 path: warps per CTA, stages, edges per tile.
-#ifndef ZS_BWDE_WARPS
-#define ZS_BWDE_WARPS 8
-#endif
-#ifndef ZS_BWDE_STAGES
-#define ZS_BWDE_STAGES 3
-#endif
-#ifndef ZS_BWDE_TILE
-#define ZS_BWDE_TILE 4
-#endif
 #ifndef ZS_BWD_WARPS
 #define ZS_BWD_WARPS 16
 #endif
@@ -494,6 +484,24 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
     }
 }
 
+constexpr int64_t kSmallCotangentBytes = int64_t(16) << 20;   // 16 MiB
+constexpr int kEdgeWarpsSmall = 12;   // 2-stage rings of 4 edges: 12 warps fit one SM's shared memory
+constexpr int kEdgeWarpsLarge = 8;    // 3-stage rings of 4 edges: 8 warps
+
+template <int W, int S, int T>
+void launch_edge_tma(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
+                     float* d_coup, float* d_rad, cudaStream_t s) {
+    const int64_t warps_max = (int64_t)num_sms() * W;
+    const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
+    const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
+    const int64_t ctas = (Wtot + W - 1) / W;
+    const int smem = W * EdgeRingLayout<S, T>::kBytes;
+    static std::atomic<bool> attr_done[kMaxDevices];
+    set_smem_limit_once(bwd_edge_c32_tma<W, S, T>, smem, attr_done);
+    launch(bwd_edge_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
+           (int)Wtot, d_coup, d_rad);
+}
+
 }  // namespace
 
 unsigned int take_timeouts_backward() { return take_timeouts_local(); }
@@ -514,16 +522,13 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
-        constexpr int W = ZS_BWDE_WARPS, S = ZS_BWDE_STAGES, T = ZS_BWDE_TILE;
-        const int64_t warps_max = (int64_t)num_sms() * W;
-        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
-        const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
-        const int64_t ctas = (Wtot + W - 1) / W;
-        const int smem = W * EdgeRingLayout<S, T>::kBytes;
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(bwd_edge_c32_tma<W, S, T>, smem, attr_done);
-        launch(bwd_edge_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
-               (int)Wtot, d_coup, d_rad);
+        // While the cotangent block is small enough to stay in L2 next to the
+        // streams, more warps with one tile in flight each hide the gather
+        // latency best; a larger block misses L2 more often and wants more
+        // tiles in flight per warp.
+        const bool small_g = (int64_t)N * 16 * kC32 * 4 <= kSmallCotangentBytes;
+        if (small_g) launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
+        else launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
     } else {
         const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
         const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
