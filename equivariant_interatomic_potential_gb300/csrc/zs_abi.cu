@@ -28,6 +28,7 @@ zs_status check_launch(const char* what) {
 
 unsigned int take_timeouts_forward();
 unsigned int take_timeouts_backward();
+zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s);
 
 }  // namespace zs
 
@@ -42,6 +43,12 @@ zs_status zs_check_timeouts(void) {
     return ZS_OK;
 }
 
+
+zs_status zs_selftest_bounded_wait(uint32_t max_spins, zs_stream_t stream) {
+    if (max_spins == 0 || max_spins > (1u << 16))
+        return zs::fail(ZS_ERR_INVALID_ARG, "zs_selftest_bounded_wait: max_spins=%u outside [1, 2^16]", max_spins);
+    return zs::selftest_bounded_wait(max_spins, reinterpret_cast<cudaStream_t>(stream));
+}
 
 const char* zs_status_string(int status) {
     switch (status) {

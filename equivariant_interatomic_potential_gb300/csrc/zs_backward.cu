@@ -502,9 +502,26 @@ void launch_edge_tma(const float* g, const float* coup, const float* rad, const 
            (int)Wtot, d_coup, d_rad);
 }
 
+// One warp waits on an mbarrier that nothing arrives on, with a limit of
+// max_spins tries: the wait gives up, counts a timeout and the kernel ends.
+__global__ void __launch_bounds__(32) selftest_wait(uint32_t max_spins) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) mbar_init(b, 1);
+    mbar_fence_init();
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_wait(b, 0, max_spins);
+    __syncwarp();
+}
+
 }  // namespace
 
 unsigned int take_timeouts_backward() { return take_timeouts_local(); }
+
+zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s) {
+    selftest_wait<<<1, 32, 0, s>>>(max_spins);
+    return check_launch("zs_selftest_bounded_wait");
+}
 
 }  // namespace zs
 

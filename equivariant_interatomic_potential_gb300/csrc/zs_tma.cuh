@@ -63,9 +63,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxSpins; ++i)
+// Bounded wait for the phase with the given parity; false (and one count in
+// g_zs_timeouts) when max_spins tries all fail.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t max_spins = kMaxSpins) {
+    for (uint32_t i = 0; i < max_spins; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicAdd(&g_zs_timeouts, 1u);
     return false;

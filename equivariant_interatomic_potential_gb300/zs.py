@@ -65,6 +65,8 @@ def load(build_if_missing: bool = True):
         lib.zs_backward_csr.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P]
         lib.zs_forward_noalloc.restype = ctypes.c_int
         lib.zs_forward_noalloc.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P]
+        lib.zs_selftest_bounded_wait.restype = ctypes.c_int
+        lib.zs_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
         lib.zs_check_timeouts.restype = ctypes.c_int
         lib.zs_check_timeouts.argtypes = []
         _lib = lib

@@ -197,6 +197,15 @@ ZS_API zs_status zs_forward_noalloc(const float* coup, const float* rad,
  */
 ZS_API zs_status zs_check_timeouts(void);
 
+/*
+ * Self-test of the bounded waits (the pages have no counterpart): enqueues a
+ * one-warp kernel that waits on an mbarrier nothing completes, giving up
+ * after max_spins tries (1 <= max_spins <= 2^16).  The wait records one
+ * timeout, which the next
+ * zs_check_timeouts() reports as ZS_ERR_TIMEOUT.  Nothing faults or hangs.
+ */
+ZS_API zs_status zs_selftest_bounded_wait(uint32_t max_spins, zs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ def test_header_declares_the_boundary():
     names = zs.declared_functions()
     for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_backward_csr", "zs_build_csr_workspace_bytes",
                "zs_forward_workspace_bytes", "zs_status_string", "zs_last_error", "zs_version",
-               "zs_check_timeouts"):
+               "zs_check_timeouts", "zs_selftest_bounded_wait", "zs_forward_noalloc"):
         assert fn in names
 
 
@@ -91,6 +91,11 @@ def test_backward_csr_argument_checks(lib):
     assert lib.zs_backward_csr(None, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
     assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 3, FAKE, None, None) == INVALID
     assert lib.zs_backward_csr(None, None, None, FAKE, None, 0, 10, 32, 3, None, None, None) == 0
+
+
+def test_selftest_argument_checks(lib):
+    assert lib.zs_selftest_bounded_wait(0, None) == INVALID
+    assert lib.zs_selftest_bounded_wait((1 << 16) + 1, None) == INVALID
 
 
 def test_build_csr_argument_checks(lib):

@@ -193,6 +193,24 @@ def test_misaligned_views_take_the_channel_path():
     check_backward(w, res)
 
 
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_reports_timeout():
+    lib = zs.load()
+    zs.zs_check_timeouts()                      # nothing pending
+    for spins in (1, 1000):
+        assert lib.zs_selftest_bounded_wait(spins, torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        assert lib.zs_check_timeouts() == 4     # ZS_ERR_TIMEOUT, counter cleared
+        assert b"bounded waits ran out" in lib.zs_last_error()
+        assert lib.zs_check_timeouts() == 0
+    # the context is still usable afterwards
+    w = workloads.make_workload("tiny")
+    res = run_gpu(w)
+    row_ptr, perm = check_csr(w, res)
+    check_forward(w, res, row_ptr, perm)
+
+
 # ------------------------------------------------------------------ determinism and ownership
 
 @pytest.mark.parametrize("name", ["n4096", "zipf"])
