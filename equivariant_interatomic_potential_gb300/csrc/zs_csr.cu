@@ -8,7 +8,8 @@
 //   upsweep   -- per tile of keys, a 256-bin digit histogram (shared atomics)
 //   scan      -- per digit, exclusive scan of its histogram row over tiles
 //   downsweep -- per tile, stable rank of every key among equal digits
-//                (warp ballots + per-warp running counts), then scatter
+//                (warp ballots + per-warp running counts), staged in shared
+//                memory in digit order and written out run by run
 // and a final pass that reads the sorted keys to write row_ptr.
 // Every step is integer arithmetic in a fixed order, so perm is unique and
 // bit-identical to a sequential counting sort.  Keys outside [0, N) sort as
@@ -119,6 +120,7 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
     __shared__ int cnt[kCsrWarps][kRadix];
     __shared__ int wsum[kCsrWarps];
     __shared__ int dbase[kRadix];
+    __shared__ int32_t skey[kTile], sval[kTile];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < kCsrWarps * kRadix; i += kCsrThreads) (&cnt[0][0])[i] = 0;
     pdl_wait();
@@ -160,23 +162,50 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
     }
     __syncthreads();
     {
-        const int d = tid;  // one thread per digit
-        int run = dbase[d] + hist[(int64_t)d * T + blockIdx.x];
+        // one thread per digit: per-warp offsets inside the tile, the tile's
+        // count of the digit, and where the digit's run starts in the tile
+        const int d = tid;
+        int own = 0;
 #pragma unroll
         for (int w = 0; w < kCsrWarps; ++w) {
             const int c = cnt[w][d];
-            cnt[w][d] = run;
-            run += c;
+            cnt[w][d] = own;
+            own += c;
         }
+        int incl = own;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        __syncthreads();                     // wsum is reused from the digit-total scan
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int pre = 0;
+        for (int w = 0; w < warp; ++w) pre += wsum[w];
+        const int local = pre + incl - own;  // first tile slot of digit d
+        // global position of the tile's first key of digit d, minus its tile slot
+        dbase[d] = dbase[d] + hist[(int64_t)d * T + blockIdx.x] - local;
+#pragma unroll
+        for (int w = 0; w < kCsrWarps; ++w) cnt[w][d] += local;
     }
     __syncthreads();
+    // stage the tile in digit order, then write each digit's run contiguously
 #pragma unroll
     for (int i = 0; i < kCsrItems; ++i) {
         if (dig[i] < kRadix) {
-            const int pos = cnt[warp][dig[i]] + rank[i];
-            keys_out[pos] = key[i];
-            vals_out[pos] = val[i];
+            const int slot = cnt[warp][dig[i]] + rank[i];
+            skey[slot] = key[i];
+            sval[slot] = val[i];
         }
+    }
+    __syncthreads();
+    const int n_in_tile = (int)imin<int64_t>(kTile, E - (int64_t)blockIdx.x * kTile);
+    for (int slot = tid; slot < n_in_tile; slot += kCsrThreads) {
+        const int32_t k = skey[slot];
+        const int pos = dbase[(k >> shift) & (kRadix - 1)] + slot;
+        keys_out[pos] = k;
+        vals_out[pos] = sval[slot];
     }
 }
 
