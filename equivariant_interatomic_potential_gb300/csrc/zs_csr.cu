@@ -2,18 +2,28 @@
 //
 // The forward of the deepmd-kit pull request "fused Triton zonal scatter for
 // the GIE head" walks a destination CSR whose within-node order is the edge
-// order ("stable-sort CSR order", section "What").  Built here as an LSD
-// radix sort of destination keys with 8-bit digits, each pass in three
-// launches with no inter-CTA waiting:
+// order ("stable-sort CSR order", section "What").  Two constructions, both
+// integer-only in a fixed order, so perm is unique and bit-identical to a
+// sequential counting sort; keys outside [0, N) count as key N, after all
+// valid ones.
+//
+// Counting path (N + 1 <= kCntMaxKeys, every bench-sized graph): one pass,
+// three launches with no inter-CTA waiting:
+//   count_rank    -- per tile of edges, each edge's stable rank among the
+//                    tile's edges of the same node (warp match + per-warp
+//                    running counts in shared memory, then a prefix over
+//                    warps), and the tile's per-node counts M[tile][n]
+//   scan_cols     -- per node, exclusive scan of M[.][n] over tiles
+//   count_scatter -- per tile, node bases from a block scan of the node
+//                    totals; perm[base[n] + M[tile][n] + rank] = edge
+// Radix path (larger N): LSD radix sort with 8-bit digits, each pass in
+// three launches:
 //   upsweep   -- per tile of keys, a 256-bin digit histogram (shared atomics)
 //   scan      -- per digit, exclusive scan of its histogram row over tiles
 //   downsweep -- per tile, stable rank of every key among equal digits
 //                (warp ballots + per-warp running counts), staged in shared
 //                memory in digit order and written out run by run
 // and a final pass that reads the sorted keys to write row_ptr.
-// Every step is integer arithmetic in a fixed order, so perm is unique and
-// bit-identical to a sequential counting sort.  Keys outside [0, N) sort as
-// key N, after all valid ones.
 #include "zs_common.cuh"
 
 namespace zs {
@@ -73,15 +83,16 @@ csr_upsweep(const int32_t* __restrict__ keys_in, int64_t E, int32_t N, int shift
     hist[(int64_t)tid * T + blockIdx.x] = cnt[tid];
 }
 
-// One warp per digit: exclusive scan of hist[d, 0..T) in place, total to tot[d].
+// One warp per row: exclusive scan of hist[d, 0..T) in place, total to tot[d],
+// for rows d < rows (digits of the radix path, nodes of the counting path).
 __global__ void __launch_bounds__(kCsrThreads)
-csr_scan(int32_t* __restrict__ hist, int T, int32_t* __restrict__ tot) {
+csr_scan(int32_t* __restrict__ hist, int T, int rows, int32_t* __restrict__ tot) {
     constexpr int R = 8;
     const int lane = threadIdx.x & 31;
     const int d = blockIdx.x * kCsrWarps + (threadIdx.x >> 5);
     pdl_wait();
     pdl_trigger();
-    if (d >= kRadix) return;
+    if (d >= rows) return;
     int32_t* row = hist + (int64_t)d * T;
     int carry = 0;
     for (int base = 0; base < T; base += 32 * R) {
@@ -236,21 +247,286 @@ csr_row_ptr(const int32_t* __restrict__ sorted, int64_t E, int32_t N,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Counting path.  A tile is kCntWarps warps x `rounds` rounds of 32 edges;
+// warp w of tile t owns the edges [t*TS + w*TW, t*TS + (w+1)*TW), TW = 32*rounds.
+constexpr int kCntWarps = 16;
+constexpr int kCntThreads = kCntWarps * 32;
+#ifndef ZS_CNT_MAX_KEYS
+#define ZS_CNT_MAX_KEYS 5120
+#endif
+constexpr int kCntMaxKeys = ZS_CNT_MAX_KEYS;   // N + 1 up to this takes the counting path
+constexpr int kCntMaxRounds = 16;       // tile of at most 8192 edges
+constexpr int kCntTargetTiles = 152;    // tiles sized so one wave covers 152 SMs
+
+constexpr int kCntMaxPer = (kCntMaxKeys + kCntThreads - 1) / kCntThreads;   // keys per thread in a block scan
+
+// Keys rounded up to even, so two keys' 16-bit counters share a 32-bit word.
+__host__ __device__ __forceinline__ int count_pairs(int nkeys) { return (nkeys + 1) >> 1; }
+
+// Shared memory of csr_count_rank: 16-bit counters [kCntWarps][keys, padded
+// to even], then one 32-bit word per edge of the tile.
+inline int count_rank_smem(int nkeys, int rounds) { return count_pairs(nkeys) * 4 * kCntWarps + rounds * kCntThreads * 4; }
+
+// 4-byte asynchronous copy global -> shared (cp.async): a CTA issues all of
+// a tile's copies, then waits once (cp_async_wait_all + a barrier).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                 :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ int32_t clamp_key(int32_t k, int32_t N) { return (uint32_t)k < (uint32_t)N ? k : N; }
+
+// Per tile: each edge's stable rank among the tile's edges of the same key
+// (to rank[]), and the tile's count of every key (to row `tile` of M, whose
+// rows hold 2 * count_pairs(N + 1) counts).
+__global__ void __launch_bounds__(kCntThreads, 1)
+csr_count_rank(const int32_t* __restrict__ dst, int64_t E, int32_t N, int rounds,
+               int32_t* __restrict__ M, uint16_t* __restrict__ rank) {
+    extern __shared__ uint32_t cnt_words[];
+    const int nkeys = N + 1;
+    const int npairs = count_pairs(nkeys);
+    // warp w's counter of key k is the 16-bit half (k & 1) of word w * npairs + k / 2
+    uint16_t* cnt = reinterpret_cast<uint16_t*>(cnt_words);
+    uint32_t* packed = cnt_words + kCntWarps * npairs;      // [TS]: key << 16 | rank in warp
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int TW = rounds * 32;
+    const int64_t tbase = (int64_t)blockIdx.x * rounds * kCntThreads;
+    const int n_in_tile = (int)imin<int64_t>((int64_t)rounds * kCntThreads, E - tbase);
+    pdl_wait();
+    pdl_trigger();
+    // the tile's keys land in packed[] while the counters are cleared
+    for (int i = tid; i < n_in_tile; i += kCntThreads) cp_async4(packed + i, dst + tbase + i);
+    // kCntWarps * npairs words, a multiple of four
+    for (int i = tid; i < kCntWarps * npairs / 4; i += kCntThreads) reinterpret_cast<uint4*>(cnt_words)[i] = make_uint4(0u, 0u, 0u, 0u);
+    cp_async_wait_all();
+    __syncthreads();
+
+    const unsigned lt = lanemask_lt();
+    uint16_t* wcnt = cnt + 2 * warp * npairs;
+    // Per round of 32 edges: the lanes holding each key (peers), found by
+    // claim and verify -- every lane writes its lane id into bits 10..14 of
+    // its key's counter (count < 1024 stays in bits 0..9), reads the slot
+    // back, and lanes that lost the claim are grouped with the winner by one
+    // ballot per contested key.  Uncontested rounds cost no ballot loop.
+    for (int r = 0; r < rounds; ++r) {
+        const int i = warp * TW + r * 32 + lane;
+        const bool valid = i < n_in_tile;
+        const int key = valid ? clamp_key((int32_t)packed[i], N) : 0;
+        const uint32_t before = valid ? wcnt[key] : 0u;          // count so far, owner bits clear
+        __syncwarp();
+        if (valid) wcnt[key] = (uint16_t)(before | ((uint32_t)lane << 10));
+        __syncwarp();
+        const int owner = valid ? (int)(wcnt[key] >> 10) : lane;
+        unsigned lost = __ballot_sync(0xffffffffu, valid && owner != lane);
+        unsigned peers = 1u << lane;
+        while (lost) {
+            const int w = __shfl_sync(0xffffffffu, owner, __ffs(lost) - 1);
+            const unsigned group = __ballot_sync(0xffffffffu, valid && owner == w);
+            if (group & (1u << lane)) peers = group;
+            lost &= ~group;
+        }
+        __syncwarp();
+        if (valid) {
+            if (lane == __ffs(peers) - 1) wcnt[key] = (uint16_t)(before + __popc(peers));
+            packed[i] = ((uint32_t)key << 16) | (before + __popc(peers & lt));
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // per pair of keys: exclusive prefix of the counters over the warps (both
+    // halves at once: every partial sum is below 2^16), tile counts to M
+    for (int q = tid; q < npairs; q += kCntThreads) {
+        uint32_t c[kCntWarps];
+#pragma unroll
+        for (int w = 0; w < kCntWarps; ++w) c[w] = cnt_words[w * npairs + q];
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kCntWarps; ++w) {
+            cnt_words[w * npairs + q] = run;
+            run += c[w];
+        }
+        reinterpret_cast<int2*>(M + (int64_t)blockIdx.x * 2 * npairs)[q] = make_int2((int)(run & 0xffffu), (int)(run >> 16));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kCntMaxRounds; ++u) {
+        const int i = tid + u * kCntThreads;
+        if (i >= n_in_tile) break;
+        const uint32_t p = packed[i];
+        const int w = i / TW;
+        rank[tbase + i] = (uint16_t)((p & 0xffffu) + cnt[2 * w * npairs + (p >> 16)]);
+    }
+}
+
+// Per key: exclusive scan over the tiles of its column of M (rows of S
+// counts) in place, total to tot[key].  A CTA takes 32 keys, one per lane;
+// its warps split the tiles into chunks and combine through shared memory.
+__global__ void __launch_bounds__(kCntThreads)
+csr_scan_cols(int32_t* __restrict__ M, int T, int S, int nkeys, int32_t* __restrict__ tot) {
+    __shared__ int32_t part[kCntWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int key = blockIdx.x * 32 + lane;
+    const int chunk = (T + kCntWarps - 1) / kCntWarps;
+    const int t0 = imin(T, warp * chunk), t1 = imin(T, t0 + chunk);
+    pdl_wait();
+    pdl_trigger();
+    constexpr int kRegs = 16;
+    __shared__ int32_t stage[kCntWarps][kRegs][32];
+    int32_t c[kRegs];
+    int32_t sum = 0;
+    const bool in_regs = chunk <= kRegs;
+    if (in_regs) {
+        // one batch of copies per lane, then the lane's own values from shared memory
+        if (key < nkeys)
+            for (int j = 0; j < t1 - t0; ++j) cp_async4(&stage[warp][j][lane], M + (int64_t)(t0 + j) * S + key);
+        cp_async_wait_all();
+#pragma unroll
+        for (int j = 0; j < kRegs; ++j) {
+            c[j] = (key < nkeys && j < t1 - t0) ? stage[warp][j][lane] : 0;
+            sum += c[j];
+        }
+    } else if (key < nkeys) {
+#pragma unroll 8
+        for (int t = t0; t < t1; ++t) sum += M[(int64_t)t * S + key];
+    }
+    part[warp][lane] = sum;
+    __syncthreads();
+    int32_t run = 0;
+    for (int w = 0; w < warp; ++w) run += part[w][lane];
+    if (key >= nkeys) return;
+    if (warp == kCntWarps - 1) tot[key] = run + sum;
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kRegs; ++j) {
+            if (t0 + j < t1) M[(int64_t)(t0 + j) * S + key] = run;
+            run += c[j];
+        }
+        return;
+    }
+    for (int t = t0; t < t1; ++t) {
+        const int64_t i = (int64_t)t * S + key;
+        const int32_t v = M[i];
+        M[i] = run;
+        run += v;
+    }
+}
+
+// Shared memory of csr_count_scatter: the tile's row of M, the node totals,
+// kCntWarps warp sums, the tile's keys, its ranks (two per word).
+inline int count_scatter_smem(int nkeys, int rounds) {
+    return (2 * count_pairs(nkeys) + nkeys + kCntWarps + rounds * kCntThreads + rounds * kCntThreads / 2) * 4;
+}
+
+// Dynamic shared memory requested so that no two CTAs of a kernel share an SM
+// (a kernel launched early behind its predecessor otherwise lands two CTAs
+// on one SM while others idle, doubling the slowest CTA's time).
+constexpr int kOneCtaPerSmSmem = 120 * 1024;
+
+// Per tile: node bases from an exclusive scan of the key totals plus the
+// tile's offset within each key, then every edge to its CSR position.  Tile 0
+// also writes row_ptr and the count of invalid keys.
+__global__ void __launch_bounds__(kCntThreads)
+csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ rank,
+                  const int32_t* __restrict__ M, const int32_t* __restrict__ tot,
+                  int64_t E, int32_t N, int rounds,
+                  int32_t* __restrict__ perm, int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
+    extern __shared__ int32_t kbase[];
+    const int nkeys = N + 1;
+    const int S = 2 * count_pairs(nkeys);
+    int32_t* ktot = kbase + S;
+    int32_t* wsum = ktot + nkeys;
+    int32_t* skey = wsum + kCntWarps;
+    uint32_t* srank = reinterpret_cast<uint32_t*>(skey + rounds * kCntThreads);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t tbase = (int64_t)blockIdx.x * rounds * kCntThreads;
+    const int n_in_tile = (int)imin<int64_t>((int64_t)rounds * kCntThreads, E - tbase);
+    pdl_wait();
+    pdl_trigger();
+    // every input of the tile in one batch of asynchronous copies: the tile's
+    // row of M, the node totals, the tile's keys and its ranks (in pairs; the
+    // tile starts on an even edge, an odd last edge is read directly)
+    for (int k = tid; k < nkeys; k += kCntThreads) {
+        cp_async4(kbase + k, M + (int64_t)blockIdx.x * S + k);
+        cp_async4(ktot + k, tot + k);
+    }
+    for (int i = tid; i < n_in_tile; i += kCntThreads) cp_async4(skey + i, dst + tbase + i);
+    for (int j = tid; j < n_in_tile / 2; j += kCntThreads) cp_async4(srank + j, rank + tbase + 2 * j);
+    if ((n_in_tile & 1) && tid == 0) srank[n_in_tile / 2] = __ldg(rank + tbase + n_in_tile - 1);
+    cp_async_wait_all();
+    __syncthreads();
+    // thread tid scans keys [k0, k0 + per)
+    const int per = (nkeys + kCntThreads - 1) / kCntThreads;
+    const int k0 = tid * per;
+    int32_t v[kCntMaxPer];
+    int32_t own = 0;
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        v[j] = (j < per && k0 + j < nkeys) ? ktot[k0 + j] : 0;
+        own += v[j];
+    }
+    int32_t incl = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t run = incl - own;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        const int k = k0 + j;
+        if (j < per && k < nkeys) {
+            if (blockIdx.x == 0) {
+                row_ptr[k] = run;
+                if (k == N && bad) *bad = v[j];
+            }
+            kbase[k] += run;
+            run += v[j];
+        }
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < n_in_tile; i += kCntThreads) {
+        const uint32_t rk = (srank[i >> 1] >> (16 * (i & 1))) & 0xffffu;
+        perm[kbase[clamp_key(skey[i], N)] + (int32_t)rk] = (int32_t)(tbase + i);
+    }
+}
+
 struct CsrPlan {
+    bool counting = false;
     int T = 0;
     int passes = 0;
-    size_t off_k[2] = {0, 0}, off_v[2] = {0, 0}, off_hist = 0, off_tot = 0, bytes = 0;
+    int rounds = 0;     // counting path: rounds of 32 edges per warp in a tile
+    size_t off_k[2] = {0, 0}, off_v[2] = {0, 0}, off_hist = 0, off_tot = 0, off_rank = 0, bytes = 0;
 };
 
 CsrPlan csr_plan(int64_t E, int32_t N) {
     CsrPlan p;
     if (E <= 0) return p;
+    const size_t ebytes = align_up((size_t)E * 4, 256);
+    size_t off = 0;
+    if ((int64_t)N + 1 <= kCntMaxKeys) {
+        p.counting = true;
+        const int64_t per_tile = (E + kCntTargetTiles - 1) / kCntTargetTiles;
+        p.rounds = (int)imax<int64_t>(1, imin<int64_t>(kCntMaxRounds, (per_tile + kCntThreads - 1) / kCntThreads));
+        const int64_t ts = (int64_t)p.rounds * kCntThreads;
+        p.T = (int)((E + ts - 1) / ts);
+        const int nkeys = N + 1;
+        p.off_hist = off; off += align_up((size_t)2 * count_pairs(nkeys) * p.T * 4, 256);
+        p.off_tot = off; off += align_up((size_t)nkeys * 4, 256);
+        p.off_rank = off; off += align_up((size_t)E * 2, 256);
+        p.bytes = off;
+        return p;
+    }
     p.T = (int)((E + kTile - 1) / kTile);
     const uint32_t maxkey = (uint32_t)N;
     const int bits = maxkey == 0 ? 1 : 32 - __builtin_clz(maxkey);
     p.passes = (bits + 7) / 8;
-    const size_t ebytes = align_up((size_t)E * 4, 256);
-    size_t off = 0;
     p.off_k[0] = off; off += ebytes;
     p.off_v[0] = off; off += ebytes;
     p.off_k[1] = off; off += ebytes;
@@ -284,6 +560,24 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
         return fail(ZS_ERR_INVALID_ARG, "zs_build_csr: workspace NULL or not 256-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
+    if (p.counting) {
+        static std::atomic<bool> rank_smem_set[kMaxDevices];
+        int32_t* M = reinterpret_cast<int32_t*>(ws + p.off_hist);
+        int32_t* tot = reinterpret_cast<int32_t*>(ws + p.off_tot);
+        uint16_t* rank = reinterpret_cast<uint16_t*>(ws + p.off_rank);
+        const int smem = count_rank_smem(kCntMaxKeys, kCntMaxRounds);
+        set_smem_limit_once(csr_count_rank, smem, rank_smem_set);
+        const int S = 2 * count_pairs(N + 1);
+        launch(csr_count_rank, p.T, kCntThreads, count_rank_smem(N + 1, p.rounds), s, dst, E, N, p.rounds, M, rank);
+        static std::atomic<bool> scan_smem_set[kMaxDevices];
+        set_smem_limit_once(csr_scan_cols, kOneCtaPerSmSmem, scan_smem_set);
+        launch(csr_scan_cols, (N + 1 + 31) / 32, kCntThreads, kOneCtaPerSmSmem, s, M, p.T, S, N + 1, tot);
+        static std::atomic<bool> scatter_smem_set[kMaxDevices];
+        set_smem_limit_once(csr_count_scatter, imax(kOneCtaPerSmSmem, count_scatter_smem(kCntMaxKeys, kCntMaxRounds)), scatter_smem_set);
+        launch(csr_count_scatter, p.T, kCntThreads, imax(kOneCtaPerSmSmem, count_scatter_smem(N + 1, p.rounds)), s, dst, (const uint16_t*)rank,
+               (const int32_t*)M, (const int32_t*)tot, E, N, p.rounds, perm, row_ptr, bad_dst_count);
+        return check_launch("zs_build_csr");
+    }
     const int32_t* sorted = nullptr;
     if (E > 0) {
         int32_t* hist = reinterpret_cast<int32_t*>(ws + p.off_hist);
@@ -297,7 +591,7 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
             int32_t* vout = last ? perm : reinterpret_cast<int32_t*>(ws + p.off_v[pass & 1]);
             if (first) launch(csr_upsweep<true>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
             else launch(csr_upsweep<false>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
-            launch(csr_scan, kRadix / kCsrWarps, kCsrThreads, 0, s, hist, p.T, tot);
+            launch(csr_scan, kRadix / kCsrWarps, kCsrThreads, 0, s, hist, p.T, kRadix, tot);
             if (first) launch(csr_downsweep<true>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
             else launch(csr_downsweep<false>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
             kin = kout;

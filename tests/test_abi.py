@@ -112,10 +112,23 @@ def test_build_csr_argument_checks(lib):
 def test_workspace_sizes(lib):
     assert lib.zs_build_csr_workspace_bytes(0, 10) == 0
     assert lib.zs_build_csr_workspace_bytes(-1, 10) == 0
-    # four int32 arrays of E plus a 256 x tiles histogram, 256-byte aligned pieces
+    al = lambda x: -(-x // 256) * 256
+    # counting path (N + 1 <= 5120): per tile of 512 x rounds edges (rounds so
+    # that about 152 tiles cover E, 1..16) one count per key, the key totals,
+    # and a 16-bit rank per edge
+    def counting(E, N):
+        rounds = max(1, min(16, -(-(-(-E // 152)) // 512)))
+        T = -(-E // (512 * rounds))
+        return al(T * 2 * -(-(N + 1) // 2) * 4) + al((N + 1) * 4) + al(E * 2)
+    # radix path: four int32 arrays of E plus a 256 x tiles histogram
+    def radix(E):
+        return 4 * al(E * 4) + al(256 * -(-E // 2048) * 4) + 1024
     E = 647170
-    tiles = -(-E // 2048)
-    want = 4 * (-(-E * 4 // 256) * 256) + (-(-256 * tiles * 4 // 256) * 256) + 1024
+    want = counting(E, 4096)
+    for e, n in [(1, 0), (5000, 5119), (2_000_000, 3000), (50, 1)]:
+        assert lib.zs_build_csr_workspace_bytes(e, n) == counting(e, n)
+    for e, n in [(5000, 5120), (E, 32768), (1, 1 << 20)]:
+        assert lib.zs_build_csr_workspace_bytes(e, n) == radix(e)
     assert lib.zs_build_csr_workspace_bytes(E, 4096) == want
     # forward: per window of at least 128 CSR positions (plus one), a pair of 15 x C
     # partials and one crossing-node entry, each array 256-byte aligned

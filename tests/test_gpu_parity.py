@@ -155,6 +155,21 @@ def test_csr_radix_pass_boundaries(N):
     assert int(bad.cpu()[0]) == b2 == 0
 
 
+@pytest.mark.parametrize("E,N", [(2_000_000, 3000), (70_000, 5118), (70_000, 5119), (70_000, 5120), (513, 0), (1, 1)])
+def test_csr_counting_path_limits(E, N):
+    # the one-pass counting construction covers N + 1 <= 5120 (radix beyond);
+    # 2M edges give tiles of 8192 edges in more than one wave
+    rng = np.random.default_rng(E + N)
+    dst = rng.integers(-2, N + 2, size=E).astype(np.int32)
+    if N > 0:
+        dst[: E // 4] = N - 1
+    row_ptr, perm, bad = zs.zs_build_csr(dev(dst), N)
+    r2, p2, b2 = oracle.build_csr(dst, N)
+    assert np.array_equal(row_ptr.cpu().numpy(), r2)
+    assert np.array_equal(perm.cpu().numpy(), p2)
+    assert int(bad.cpu()[0]) == b2
+
+
 def test_self_loops_and_nan():
     w = workloads.make_random(40, 6000, 32, seed=9, self_loops=True)
     e_nan = 1234
