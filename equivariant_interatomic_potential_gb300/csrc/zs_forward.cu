@@ -15,8 +15,11 @@
 //     registers and written directly;
 //   * a node cut by window edges is summed piecewise: the pieces inside one
 //     CTA are added in shared memory in window order, and a node that crosses
-//     CTA windows leaves one partial per CTA in the workspace, which a second
-//     small kernel adds in CTA order.
+//     CTA windows leaves one partial per CTA in the workspace.  On the C == 32
+//     path the CTA where such a node ends adds the earlier CTAs' partials in
+//     CTA order once their flags say they are written (every CTA of that
+//     single-wave grid is resident, and a CTA only waits for lower ones);
+//     the per-channel path leaves that to a second small kernel.
 // Every sum is therefore formed in one fixed order: run to run bitwise
 // deterministic, no floating-point atomics.
 #include <mutex>
@@ -123,6 +126,43 @@ __device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, i
     return n_lb;
 }
 
+// Tag that marks a partial as written by this launch: %gridid numbers the
+// launches of a context (a new value for every launch, graph replays
+// included), mixed with a per-call value from the host.
+__device__ __forceinline__ uint64_t launch_tag(uint64_t salt) {
+    uint64_t id;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
+    return (id * 0x9E3779B97F4A7C15ull) ^ salt;
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until flags[k] == tag; false (and one count in g_zs_timeouts)
+// if it never comes.
+__device__ __forceinline__ bool wait_flag(const uint64_t* flags, int k, uint64_t tag) {
+    for (uint32_t i = 0; i < kMaxSpins; ++i)
+        if (ld_acquire_u64(flags + k) == tag) return true;
+    atomicAdd(&g_zs_timeouts, 1u);
+    return false;
+}
+
+__device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, float4 acc[4], const Lane32& L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 4 * L.g + i;
+        acc[i] = r < kRows ? __ldcg(reinterpret_cast<const float4*>(part + r * kC32 + 4 * L.q))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 // C == 32 forward with TMA-fed warps.  W warps per CTA, one CTA per SM; warp
 // gw owns the window [gw*KW, gw*KW + KW) of CSR positions and walks it in
 // position order, closing a node when its last position is reached.
@@ -131,15 +171,13 @@ __global__ void __launch_bounds__(W * 32, 1)
 fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
             int E, int32_t N, int KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part,
-            int32_t* __restrict__ cross) {
+            uint64_t* __restrict__ flags, uint64_t salt) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
-    __shared__ int cross_node;
     const int warp = threadIdx.x >> 5;
     const Lane32 L(threadIdx.x & 31);
     const int gw = blockIdx.x * W + warp;
     const bool active = gw < Wtot;
-    if (threadIdx.x == 0) cross_node = -1;
     pdl_wait();
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
@@ -237,8 +275,11 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
 
     // Combine the warp pieces of nodes cut by window edges inside this CTA:
     // the lowest warp holding a piece of node m adds them in window order.
-    const int64_t P0 = imin<int64_t>((int64_t)blockIdx.x * W * KW, E);
-    const int64_t P1 = imin<int64_t>(P0 + (int64_t)W * KW, E);
+    const int64_t span = (int64_t)W * KW;   // CSR positions per CTA
+    const int64_t P0 = imin<int64_t>((int64_t)blockIdx.x * span, E);
+    const int64_t P1 = imin<int64_t>(P0 + span, E);
+    int pend_node = -1;                      // a node that started in an earlier CTA and ends here
+    float4 pend[4];
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot) {
         const int m = sp_node[warp][slot];
@@ -255,13 +296,38 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
         const int ma = __ldg(row_ptr + m), mb = __ldg(row_ptr + m + 1);
         if (ma >= P0 && mb <= P1) {
             store_node32(out + (int64_t)m * kNodeFloats32, sum, L);
+        } else if (ma < P0 && mb <= P1) {
+            pend_node = m;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pend[i] = sum[i];
         } else {
+            // slot 1: starts here and runs past this CTA; slot 0: covers all of it
             store_part32(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * kPartFloats32, sum, L);
-            if (ma >= P0 && L.lane == 0) cross_node = m;   // starts here, continues past this CTA
         }
     }
+    // publish this CTA's partials: every writer fences, then one release store
+    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) cross[blockIdx.x] = cross_node;
+    const uint64_t tag = launch_tag(salt);
+    if (threadIdx.x == 0) st_release_u64(flags + blockIdx.x, tag);
+    if (pend_node < 0) return;
+    // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
+    // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
+    const int b0 = (int)(__ldg(row_ptr + pend_node) / span);
+    if (L.lane == 0)
+        for (int k = b0; k < (int)blockIdx.x; ++k) wait_flag(flags, k, tag);
+    __syncwarp();
+    float4 total[4];
+    load_part32_cg(cta_part + ((int64_t)b0 * 2 + 1) * kPartFloats32, total, L);
+    for (int k = b0 + 1; k < (int)blockIdx.x; ++k) {
+        float4 t4[4];
+        load_part32_cg(cta_part + (int64_t)k * 2 * kPartFloats32, t4, L);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) total[i] = f4_add(total[i], t4[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) total[i] = f4_add(total[i], pend[i]);
+    store_node32(out + (int64_t)pend_node * kNodeFloats32, total, L);
 }
 
 // --------------------------------------------------------------------------
@@ -419,11 +485,35 @@ unsigned int take_timeouts_forward() { return take_timeouts_local(); }
 
 using namespace zs;
 
-// Bytes of scratch for `windows` windows: a pair of (15 x C) partials and
-// one crossing-node entry per window.
+// Scratch for `windows` windows: a pair of (15 x C) partials, one
+// crossing-node entry and one 64-bit flag per window, each array 256-byte
+// aligned.
+struct Scratch {
+    float* part;
+    int32_t* cross;
+    uint64_t* flags;
+};
+
+static size_t part_bytes(int64_t windows, int C) { return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256); }
+
 static size_t scratch_bytes(int64_t windows, int C) {
-    return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256) +
-           align_up((size_t)windows * sizeof(int32_t), 256);
+    return part_bytes(windows, C) + align_up((size_t)windows * sizeof(int32_t), 256) +
+           align_up((size_t)windows * sizeof(uint64_t), 256);
+}
+
+static Scratch scratch_at(void* base, int64_t windows, int C) {
+    char* b = static_cast<char*>(base);
+    Scratch sc;
+    sc.part = reinterpret_cast<float*>(b);
+    sc.cross = reinterpret_cast<int32_t*>(b + part_bytes(windows, C));
+    sc.flags = reinterpret_cast<uint64_t*>(b + part_bytes(windows, C) + align_up((size_t)windows * sizeof(int32_t), 256));
+    return sc;
+}
+
+// Per-call value mixed into the C == 32 forward's launch tags.
+static uint64_t next_salt() {
+    static std::atomic<uint64_t> counter{0x2545F4914F6CDD1Dull ^ (uint64_t)(uintptr_t)&counter};
+    return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
 }
 
 extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
@@ -453,7 +543,6 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace NULL or not 256-byte aligned");
     if (N == 0) return ZS_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    float* part = static_cast<float*>(workspace);
     const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
     if (fast) {
         // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
@@ -462,24 +551,20 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
         const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
         const int64_t Wtot = imax<int64_t>(ceil_div(E, KW), 1);
         const int64_t ctas = ceil_div(Wtot, kTmaWarps);
-        int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
-                                                    align_up((size_t)ctas * 2 * kRows * C * sizeof(float), 256));
+        const Scratch sc = scratch_at(workspace, ctas, C);
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static std::atomic<bool> attr_done[kMaxDevices];
         set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
-        launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
-               (int)(KW * kTmaWarps), (const float*)part, out);
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, sc.part, sc.flags, next_salt());
     } else {
         const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
         const int64_t ctas = ceil_div(Wtot, kFwdWarps);
-        int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
-                                                    align_up((size_t)Wtot * 2 * kRows * C * sizeof(float), 256));
+        const Scratch sc = scratch_at(workspace, Wtot, C);
         launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
-               part, cross);
-        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C, kGenWin,
-               (const float*)part, out);
+               sc.part, sc.cross);
+        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, kGenWin,
+               (const float*)sc.part, out);
     }
     return check_launch("zs_forward");
 }
@@ -489,8 +574,9 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
 // memory (for example code that runs where cudaMalloc is not allowed, such
 // as inside a region that must not touch the allocator, or a host framework
 // that owns all device memory and hands out only the tensors themselves).
-// The partial sums the forward keeps between its two kernels live in a
-// fixed, file-scope device array instead of a caller workspace.
+// The partial sums and flags the forward keeps between its CTAs (and, on
+// the per-channel path, between its two kernels) live in a fixed, file-scope
+// device array instead of a caller workspace.
 // --------------------------------------------------------------------------
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB, held by every GPU that loads the library
@@ -551,25 +637,22 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
         return fail(ZS_ERR_INVALID_ARG,
                     "zs_forward_noalloc: this call needs %zu bytes of scratch but the library's static scratch holds "
                     "%zu; use zs_forward with a caller workspace", need, kNoAllocScratchBytes);
-    float* part = nullptr;
-    const zs_status st = forward_scratch_address(&part);
+    float* base = nullptr;
+    const zs_status st = forward_scratch_address(&base);
     if (st != ZS_OK) return st;
-    int32_t* cross = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(part) +
-                                                align_up((size_t)windows * 2 * kRows * C * sizeof(float), 256));
+    const Scratch sc = scratch_at(base, windows, C);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fast) {
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static std::atomic<bool> attr_done[kMaxDevices];
         set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, part, cross);
-        launch(fwd_fixup, (unsigned)ctas, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C,
-               (int)(KW * kTmaWarps), (const float*)part, out);
+               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, sc.part, sc.flags, next_salt());
     } else {
         launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
-               part, cross);
-        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)cross, C, kGenWin,
-               (const float*)part, out);
+               sc.part, sc.cross);
+        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, kGenWin,
+               (const float*)sc.part, out);
     }
     return check_launch("zs_forward_noalloc");
 }

@@ -105,7 +105,8 @@ ZS_API zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
 
 /*
  * Bytes of device workspace zs_forward needs (partial sums of nodes whose
- * edges are split across work units).  256-byte alignment required.
+ * edges are split across work units, and flags that mark them written).
+ * 256-byte alignment required; its contents need not start at zero.
  */
 ZS_API size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C);
 
@@ -174,7 +175,7 @@ ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float*
  *   live instead in one static device array of 4 MiB that every GPU
  *   loading the library holds until the process exits.  C == 32 with
  *   16-byte aligned rad, out and coup needs about 3.8 KB per SM whatever E
- *   is; other channel counts need 120*C + 4 bytes per 256 edges.  A call
+ *   is; other channel counts need 120*C + 12 bytes per 256 edges.  A call
  *   that would need more returns ZS_ERR_INVALID_ARG and enqueues nothing.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.

@@ -131,10 +131,10 @@ def test_workspace_sizes(lib):
         assert lib.zs_build_csr_workspace_bytes(e, n) == radix(e)
     assert lib.zs_build_csr_workspace_bytes(E, 4096) == want
     # forward: per window of at least 128 CSR positions (plus one), a pair of 15 x C
-    # partials and one crossing-node entry, each array 256-byte aligned
+    # partials, one crossing-node entry and one 64-bit flag, each array 256-byte aligned
     def ws(E, C):
         w = -(-max(E, 1) // 128) + 1
-        return -(-(w * 2 * 15 * C * 4) // 256) * 256 + -(-(w * 4) // 256) * 256
+        return -(-(w * 2 * 15 * C * 4) // 256) * 256 + -(-(w * 4) // 256) * 256 + -(-(w * 8) // 256) * 256
     assert lib.zs_forward_workspace_bytes(E, 4096, 32) == ws(E, 32)
     assert lib.zs_forward_workspace_bytes(0, 4096, 32) == ws(0, 32)
     assert lib.zs_forward_workspace_bytes(1000, 10, 40) == ws(1000, 40)

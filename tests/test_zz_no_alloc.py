@@ -42,7 +42,7 @@ def test_noalloc_forward_matches_workspace_forward(case):
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
-    # C = 40 needs 120*C + 4 bytes per 256 edges: 300000 edges exceed the 4 MiB scratch
+    # C = 40 needs 120*C + 12 bytes per 256 edges: 300000 edges exceed the 4 MiB scratch
     E, N, C = 300000, 1000, 40
     lib = zs.load()
     coup = torch.zeros((E, 15), device="cuda")
