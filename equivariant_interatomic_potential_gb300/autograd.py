@@ -1,0 +1,90 @@
+"""PyTorch operators over libzs, with first-order autograd.
+
+The pull request "fused Triton zonal scatter for the GIE head" (deepmd-kit)
+puts the zonal scatter behind a differentiable operator whose backward is
+the edge-parallel pass and which has no double backward (sections "What"
+and "Tests").  Here that operator is a ``torch.library`` custom op:
+
+  ``zs_gie::build_csr(dst, num_nodes) -> (row_ptr, perm)``
+  ``zs_gie::zonal_scatter(coup, rad, dst, row_ptr, perm, num_nodes) -> out``
+
+``zonal_scatter``'s backward is ``zs_gie::zonal_scatter_backward`` (the
+edge-order ``zs_backward``), itself an operator without a derivative, so a
+second backward raises.  Every operator has a fake (meta) implementation,
+so ``torch.compile`` traces through them with shapes only; the launch grid
+is chosen inside libzs from the runtime sizes.  The operators run libzs's
+CUDA kernels and nothing else: CPU tensors are rejected.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import zs
+
+_NS = "zs_gie"
+
+
+def _cuda_only(name: str, *tensors: torch.Tensor) -> None:
+    for t in tensors:
+        if t.device.type != "cuda":
+            raise ValueError(f"{_NS}::{name} runs on CUDA tensors only (got a {t.device.type} tensor)")
+
+
+@torch.library.custom_op(f"{_NS}::build_csr", mutates_args=())
+def build_csr(dst: torch.Tensor, num_nodes: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """Stable destination CSR of int32 ``dst``: (row_ptr (N+1,), perm (E,)), int32."""
+    _cuda_only("build_csr", dst)
+    row_ptr, perm, _ = zs.zs_build_csr(dst.contiguous(), num_nodes)
+    return row_ptr, perm
+
+
+@build_csr.register_fake
+def _(dst, num_nodes):
+    return (dst.new_empty((num_nodes + 1,), dtype=torch.int32), dst.new_empty(dst.shape, dtype=torch.int32))
+
+
+@torch.library.custom_op(f"{_NS}::zonal_scatter", mutates_args=())
+def zonal_scatter(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, row_ptr: torch.Tensor,
+                  perm: torch.Tensor, num_nodes: int) -> torch.Tensor:
+    """out (N, 16, C): row 0 zero, rows 1..15 the zonal scatter of coup (E, 15) x rad (E, 3, C)."""
+    _cuda_only("zonal_scatter", coup, rad, dst, row_ptr, perm)
+    return zs.zs_forward(coup.contiguous(), rad.contiguous(), row_ptr.contiguous(), perm.contiguous(), num_nodes)
+
+
+@zonal_scatter.register_fake
+def _(coup, rad, dst, row_ptr, perm, num_nodes):
+    return coup.new_empty((num_nodes, 16, rad.shape[2]))
+
+
+@torch.library.custom_op(f"{_NS}::zonal_scatter_backward", mutates_args=())
+def zonal_scatter_backward(grad_out: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor,
+                           num_nodes: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """(d_coup (E, 15), d_rad (E, 3, C)) for the cotangent grad_out (N, 16, C); edge order."""
+    _cuda_only("zonal_scatter_backward", grad_out, coup, rad, dst)
+    return zs.zs_backward(grad_out.contiguous(), coup.contiguous(), rad.contiguous(), dst.contiguous(), num_nodes)
+
+
+@zonal_scatter_backward.register_fake
+def _(grad_out, coup, rad, dst, num_nodes):
+    return coup.new_empty(coup.shape), rad.new_empty(rad.shape)
+
+
+def _setup_context(ctx, inputs, output):
+    coup, rad, dst, row_ptr, perm, num_nodes = inputs
+    ctx.save_for_backward(coup, rad, dst)
+    ctx.num_nodes = num_nodes
+
+
+def _backward(ctx, grad_out):
+    coup, rad, dst = ctx.saved_tensors
+    d_coup, d_rad = zonal_scatter_backward(grad_out, coup, rad, dst, ctx.num_nodes)
+    return d_coup, d_rad, None, None, None, None
+
+
+zonal_scatter.register_autograd(_backward, setup_context=_setup_context)
+
+
+def zonal_scatter_from_dst(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, num_nodes: int) -> torch.Tensor:
+    """Build the CSR of dst, then the differentiable zonal scatter."""
+    row_ptr, perm = build_csr(dst, num_nodes)
+    return zonal_scatter(coup, rad, dst, row_ptr, perm, num_nodes)
