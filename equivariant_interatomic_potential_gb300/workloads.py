@@ -41,9 +41,9 @@ class Workload:
     seed: int
     src: np.ndarray        # (E,) int32, ascending
     dst: np.ndarray        # (E,) int32
-    coup: np.ndarray       # (E, 15) float32
-    rad: np.ndarray        # (E, 3, C) float32
-    grad_out: np.ndarray   # (N, 16, C) float32
+    coup: np.ndarray       # (E, 15) float32 ((E, D-1) for another ladder degree)
+    rad: np.ndarray        # (E, 3, C) float32 ((E, lmax, C))
+    grad_out: np.ndarray   # (N, 16, C) float32 ((N, D, C))
 
     def nbytes(self) -> int:
         return sum(a.nbytes for a in (self.dst, self.coup, self.rad, self.grad_out))
@@ -118,10 +118,13 @@ def zipf_dst(rng: np.random.Generator, src: np.ndarray, N: int,
     return perm[k].astype(np.int32)
 
 
-def draw_operands(rng: np.random.Generator, N: int, E: int, C: int):
-    coup = (rng.random((E, ROWS), dtype=np.float32) * np.float32(2.0) - np.float32(1.0)).astype(np.float32)
-    rad = rng.standard_normal((E, SLOTS, C), dtype=np.float32)
-    grad_out = rng.standard_normal((N, D, C), dtype=np.float32)
+def draw_operands(rng: np.random.Generator, N: int, E: int, C: int, lmax: int = 3):
+    """coup (E, R) uniform(-1, 1), rad (E, lmax, C) and grad_out (N, D, C) standard
+    normal, D = (lmax+1)^2, R = D - 1 (15 / 3 / 16 at lmax = 3)."""
+    d = (lmax + 1) ** 2
+    coup = (rng.random((E, d - 1), dtype=np.float32) * np.float32(2.0) - np.float32(1.0)).astype(np.float32)
+    rad = rng.standard_normal((E, lmax, C), dtype=np.float32)
+    grad_out = rng.standard_normal((N, d, C), dtype=np.float32)
     return coup, rad, grad_out
 
 
@@ -141,10 +144,11 @@ def make_workload(name: str, C: int = 32, seed: int | None = None) -> Workload:
 
 
 def make_random(N: int, E: int, C: int, seed: int, *, self_loops: bool = False,
-                hot_node: int | None = None, hot_fraction: float = 0.0) -> Workload:
+                hot_node: int | None = None, hot_fraction: float = 0.0, lmax: int = 3) -> Workload:
     """Small ad-hoc graph: uniform destinations, optional self loops and a hot node.
 
-    Used for edge cases (ragged sizes, odd channel counts, one heavy node).
+    Used for edge cases (ragged sizes, odd channel counts, one heavy node,
+    other ladder degrees lmax).
     """
     rng = np.random.default_rng(seed)
     src = np.sort(rng.integers(0, max(N, 1), size=E)).astype(np.int32) if N > 0 else np.zeros(E, np.int32)
@@ -157,5 +161,6 @@ def make_random(N: int, E: int, C: int, seed: int, *, self_loops: bool = False,
     if hot_node is not None and E > 0:
         hot = rng.random(E) < hot_fraction
         dst = np.where(hot, np.int32(hot_node), dst).astype(np.int32)
-    coup, rad, grad_out = draw_operands(rng, max(N, 0), E, C)
-    return Workload(f"random_N{N}_E{E}_C{C}", N, E, C, seed, src, dst, coup, rad, grad_out)
+    coup, rad, grad_out = draw_operands(rng, max(N, 0), E, C, lmax)
+    tag = "" if lmax == 3 else f"_L{lmax}"
+    return Workload(f"random_N{N}_E{E}_C{C}{tag}", N, E, C, seed, src, dst, coup, rad, grad_out)

@@ -54,11 +54,11 @@ def _load():
             lib.oracle_build_csr.restype = ctypes.c_int64
             lib.oracle_build_csr.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P]
             lib.oracle_forward.restype = None
-            lib.oracle_forward.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+            lib.oracle_forward.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            P, ctypes.c_int64, P, P]
             lib.oracle_backward.restype = None
             lib.oracle_backward.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int32,
-                                            ctypes.c_int32, P, ctypes.c_int64, P, P, P, P]
+                                            ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64, P, P, P, P]
             lib.oracle_slot_of_row.restype = ctypes.c_int
             lib.oracle_slot_of_row.argtypes = [ctypes.c_int]
             _lib = lib
@@ -83,40 +83,55 @@ def build_csr(dst: np.ndarray, N: int):
     return row_ptr, perm, int(bad)
 
 
+def ladder(lmax: int):
+    """(D, R) of the degree-lmax ladder: D = (lmax+1)^2 node rows, R = D - 1 zonal rows."""
+    D = (lmax + 1) ** 2
+    return D, D - 1
+
+
+def _lmax_of(rad) -> int:
+    """lmax from the radial operand's slot axis (E, lmax, C)."""
+    return int(np.shape(rad)[1]) if np.ndim(rad) == 3 else 3
+
+
 def forward(coup, rad, row_ptr, perm, N: int, nodes=None):
-    """Forward in fp64: (out, absum), each (n_out, 16, C)."""
+    """Forward in fp64: (out, absum), each (n_out, D, C); lmax = rad.shape[1]."""
     coup = _c(coup, np.float32)
     rad = _c(rad, np.float32)
+    lmax = _lmax_of(rad)
+    D, R = ladder(lmax)
     C = rad.shape[2] if rad.ndim == 3 else 0
     row_ptr = _c(row_ptr, np.int32)
     perm = _c(perm, np.int32)
     nodes_a = None if nodes is None else _c(nodes, np.int32)
     n_out = N if nodes_a is None else nodes_a.shape[0]
-    out = np.zeros((n_out, 16, C), np.float64)
-    absum = np.zeros((n_out, 16, C), np.float64)
+    out = np.zeros((n_out, D, C), np.float64)
+    absum = np.zeros((n_out, D, C), np.float64)
     if n_out and C:
-        _load().oracle_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), N, C,
+        _load().oracle_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), N, C, lmax,
                                _ptr(nodes_a), 0 if nodes_a is None else n_out,
                                _ptr(out), _ptr(absum))
     return out, absum
 
 
 def backward(g, coup, rad, dst, N: int, edges=None):
-    """Backward in fp64: (d_coup (n,15), d_rad (n,3,C), abs_dcoup, abs_drad)."""
+    """Backward in fp64: (d_coup (n, D-1), d_rad (n, lmax, C), abs_dcoup, abs_drad)."""
     g = _c(g, np.float32)
     coup = _c(coup, np.float32)
     rad = _c(rad, np.float32)
     dst = _c(dst, np.int32)
+    lmax = _lmax_of(rad)
+    D, R = ladder(lmax)
     E = dst.shape[0]
     C = rad.shape[2]
     edges_a = None if edges is None else _c(edges, np.int64)
     n_out = E if edges_a is None else edges_a.shape[0]
-    d_coup = np.zeros((n_out, 15), np.float64)
-    d_rad = np.zeros((n_out, 3, C), np.float64)
-    a_dc = np.zeros((n_out, 15), np.float64)
-    a_dr = np.zeros((n_out, 3, C), np.float64)
+    d_coup = np.zeros((n_out, R), np.float64)
+    d_rad = np.zeros((n_out, lmax, C), np.float64)
+    a_dc = np.zeros((n_out, R), np.float64)
+    a_dr = np.zeros((n_out, lmax, C), np.float64)
     if n_out and C:
-        _load().oracle_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C,
+        _load().oracle_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C, lmax,
                                 _ptr(edges_a), 0 if edges_a is None else n_out,
                                 _ptr(d_coup), _ptr(d_rad), _ptr(a_dc), _ptr(a_dr))
     return d_coup, d_rad, a_dc, a_dr

@@ -13,13 +13,18 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-# zonal row -> radial slot for the lmax = 3 ladder, degree groups of 3/5/7 rows
-# (section "Boundary and layout contract": "row groups 3/5/7")
+# zonal row -> radial slot: degree groups of 2l+1 rows for l = 1..lmax
+# (section "Boundary and layout contract": "row groups 3/5/7" at lmax = 3)
 ROW_GROUPS = (3, 5, 7)
 
 
-def slot_index() -> torch.Tensor:
-    return torch.repeat_interleave(torch.arange(len(ROW_GROUPS)), torch.tensor(ROW_GROUPS))
+def row_groups(lmax: int = 3) -> tuple:
+    return tuple(2 * l + 1 for l in range(1, lmax + 1))
+
+
+def slot_index(lmax: int = 3) -> torch.Tensor:
+    groups = row_groups(lmax)
+    return torch.repeat_interleave(torch.arange(len(groups)), torch.tensor(groups))
 
 
 def _valid(dst: torch.Tensor, N: int) -> torch.Tensor:
@@ -27,20 +32,21 @@ def _valid(dst: torch.Tensor, N: int) -> torch.Tensor:
 
 
 def message(coup, rad) -> torch.Tensor:
-    """(E, 15, C) fp64 message: coupling broadcast over its degree's radial row."""
+    """(E, D-1, C) fp64 message: coupling broadcast over its degree's radial row."""
     coup = torch.as_tensor(np.asarray(coup)).to(torch.float64)
     rad = torch.as_tensor(np.asarray(rad)).to(torch.float64)
-    return coup[:, :, None] * rad[:, slot_index(), :]
+    return coup[:, :, None] * rad[:, slot_index(rad.shape[1]), :]
 
 
 def forward(coup, rad, dst, N: int, chunk: int = 1 << 16) -> np.ndarray:
-    """(N, 16, C) fp64: scalar row zero, rows 1..15 = index_add of the message."""
+    """(N, D, C) fp64: scalar row zero, rows 1..D-1 = index_add of the message."""
     coup_t = torch.as_tensor(np.asarray(coup))
     rad_t = torch.as_tensor(np.asarray(rad))
     dst_t = torch.as_tensor(np.asarray(dst)).to(torch.int64)
     E = dst_t.shape[0]
     C = rad_t.shape[2]
-    out = torch.zeros((N, 16, C), dtype=torch.float64)
+    lmax = rad_t.shape[1]
+    out = torch.zeros((N, (lmax + 1) ** 2, C), dtype=torch.float64)
     body = out[:, 1:, :]
     for a in range(0, E, chunk):
         b = min(E, a + chunk)
@@ -52,7 +58,7 @@ def forward(coup, rad, dst, N: int, chunk: int = 1 << 16) -> np.ndarray:
 
 
 def backward(g, coup, rad, dst, N: int):
-    """Adjoint of the composition: (d_coup (E,15), d_rad (E,3,C)) in fp64.
+    """Adjoint of the composition: (d_coup (E,D-1), d_rad (E,lmax,C)) in fp64.
 
     d_msg = g[dst, 1:, :]; d_coup = sum_c d_msg * rad[:, slot(r)];
     d_rad[:, s] = sum over rows r of slot s of d_msg[:, r] * coup[:, r].
@@ -63,11 +69,12 @@ def backward(g, coup, rad, dst, N: int):
     dst_t = torch.as_tensor(np.asarray(dst)).to(torch.int64)
     E = dst_t.shape[0]
     C = rad_t.shape[2]
+    lmax = rad_t.shape[1]
     keep = _valid(dst_t, N)
-    d_msg = torch.zeros((E, 15, C), dtype=torch.float64)
+    d_msg = torch.zeros((E, (lmax + 1) ** 2 - 1, C), dtype=torch.float64)
     d_msg[keep] = g_t[dst_t[keep], 1:, :]
-    idx = slot_index()
+    idx = slot_index(lmax)
     d_coup = (d_msg * rad_t[:, idx, :]).sum(dim=2)
-    d_rad = torch.zeros((E, 3, C), dtype=torch.float64)
+    d_rad = torch.zeros((E, lmax, C), dtype=torch.float64)
     d_rad.index_add_(1, idx, d_msg * coup_t[:, :, None])
     return d_coup.numpy(), d_rad.numpy()

@@ -1,5 +1,5 @@
 /*
- * CPU fp64 oracle for the GIE zonal scatter (lmax = 3).  TEST INFRASTRUCTURE.
+ * CPU fp64 oracle for the GIE zonal scatter.  TEST INFRASTRUCTURE.
  *
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
  * load this file's library.  It shares no source with the CUDA path.
@@ -8,14 +8,18 @@
  * scatter for the GIE head (DP_GIE_SCATTER_INFER)":
  *   - section "What", forward bullet: a destination CSR in stable edge order
  *     is walked per node and the per-edge message is summed into the padded
- *     (N, 16, C) node layout whose scalar row 0 is zero;
+ *     (N, D, C) node layout whose scalar row 0 is zero;
  *   - section "What", backward bullet: per edge, the coupling gradient
- *     (E, 15) and the radial gradient (E, 3, C);
+ *     (E, D-1) and the radial gradient (E, lmax, C);
  *   - section "Boundary and layout contract": the lmax = 3 ladder packs the
  *     15 zonal rows as contiguous degree groups of 3, 5 and 7 rows.
  *
- * Row r belongs to degree 1 for r in [0,3), degree 2 for r in [3,8) and
- * degree 3 for r in [8,15); the radial slot of degree l is l - 1.
+ * The ladder of degree lmax has D = (lmax+1)^2 node rows: the scalar row and
+ * D - 1 zonal rows packed as contiguous degree groups of 2l+1 rows for
+ * l = 1..lmax, so row r belongs to degree l for r in [l^2 - 1, (l+1)^2 - 1)
+ * (degree 1: rows 0..2, degree 2: rows 3..7, degree 3: rows 8..14, ...); the
+ * radial slot of degree l is l - 1.  lmax = 3 is the pages' operator; other
+ * lmax (1..5) extend it the same way.
  *
  * Message, forward and backward (plain definition, accumulated in fp64):
  *   msg[e,r,c]    = coup[e,r] * rad[e, slot(r), c]
@@ -37,15 +41,12 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define ORACLE_ROWS 15
-#define ORACLE_SLOTS 3
-#define ORACLE_D 16
-
-/* degree group of zonal row r, as a radial slot index (0, 1 or 2) */
+/* degree group of zonal row r, as a radial slot index (degree - 1): the
+ * degree l of row r is the one whose group [l^2 - 1, (l+1)^2 - 1) holds r */
 static int slot_of_row(int r) {
-    if (r < 3) return 0;
-    if (r < 8) return 1;
-    return 2;
+    int l = 1;
+    while ((l + 1) * (l + 1) - 1 <= r) ++l;
+    return l - 1;
 }
 
 /*
@@ -82,16 +83,18 @@ int64_t oracle_build_csr(const int32_t* dst, int64_t E, int32_t N,
 
 /*
  * Forward for the nodes listed in `nodes` (or all N nodes when nodes == NULL,
- * in which case n_nodes is ignored).  out and absum are (n_out, 16, C) fp64,
- * one block per listed node, in list order.
+ * in which case n_nodes is ignored).  coup is (E, D-1), rad (E, lmax, C);
+ * out and absum are (n_out, D, C) fp64, one block per listed node, in list
+ * order.
  */
 void oracle_forward(const float* coup, const float* rad,
                     const int32_t* row_ptr, const int32_t* perm,
-                    int32_t N, int32_t C,
+                    int32_t N, int32_t C, int32_t lmax,
                     const int32_t* nodes, int64_t n_nodes,
                     double* out, double* absum) {
+    const int D = (lmax + 1) * (lmax + 1), R = D - 1, S = lmax;
     int64_t n_out = nodes ? n_nodes : (int64_t)N;
-    size_t block = (size_t)ORACLE_D * (size_t)C;
+    size_t block = (size_t)D * (size_t)C;
     memset(out, 0, sizeof(double) * block * (size_t)n_out);
     if (absum) memset(absum, 0, sizeof(double) * block * (size_t)n_out);
     for (int64_t k = 0; k < n_out; ++k) {
@@ -100,9 +103,9 @@ void oracle_forward(const float* coup, const float* rad,
         double* a = absum ? absum + block * (size_t)k : NULL;
         for (int32_t j = row_ptr[n]; j < row_ptr[n + 1]; ++j) {
             int64_t e = perm[j];
-            const float* cp = coup + (size_t)e * ORACLE_ROWS;
-            const float* rp = rad + (size_t)e * ORACLE_SLOTS * (size_t)C;
-            for (int r = 0; r < ORACLE_ROWS; ++r) {
+            const float* cp = coup + (size_t)e * R;
+            const float* rp = rad + (size_t)e * S * (size_t)C;
+            for (int r = 0; r < R; ++r) {
                 double cv = (double)cp[r];
                 const float* rs = rp + (size_t)slot_of_row(r) * (size_t)C;
                 double* orow = o + (size_t)(1 + r) * (size_t)C;
@@ -119,30 +122,31 @@ void oracle_forward(const float* coup, const float* rad,
 
 /*
  * Backward for the edges listed in `edges` (or all E edges when
- * edges == NULL).  d_coup / abs_dcoup are (n_out, 15), d_rad / abs_drad are
- * (n_out, 3, C), fp64, one block per listed edge in list order.  g is the
- * (N, 16, C) output cotangent; its row 0 is never read.
+ * edges == NULL).  d_coup / abs_dcoup are (n_out, D-1), d_rad / abs_drad are
+ * (n_out, lmax, C), fp64, one block per listed edge in list order.  g is the
+ * (N, D, C) output cotangent; its row 0 is never read.
  */
 void oracle_backward(const float* g, const float* coup, const float* rad,
-                     const int32_t* dst, int64_t E, int32_t N, int32_t C,
+                     const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
                      const int64_t* edges, int64_t n_edges,
                      double* d_coup, double* d_rad,
                      double* abs_dcoup, double* abs_drad) {
+    const int D = (lmax + 1) * (lmax + 1), R = D - 1, S = lmax;
     int64_t n_out = edges ? n_edges : E;
     for (int64_t k = 0; k < n_out; ++k) {
         int64_t e = edges ? edges[k] : k;
-        double* dc = d_coup + (size_t)k * ORACLE_ROWS;
-        double* dr = d_rad + (size_t)k * ORACLE_SLOTS * (size_t)C;
-        double* adc = abs_dcoup ? abs_dcoup + (size_t)k * ORACLE_ROWS : NULL;
-        double* adr = abs_drad ? abs_drad + (size_t)k * ORACLE_SLOTS * (size_t)C : NULL;
-        for (int r = 0; r < ORACLE_ROWS; ++r) { dc[r] = 0.0; if (adc) adc[r] = 0.0; }
-        for (size_t i = 0; i < (size_t)ORACLE_SLOTS * (size_t)C; ++i) { dr[i] = 0.0; if (adr) adr[i] = 0.0; }
+        double* dc = d_coup + (size_t)k * R;
+        double* dr = d_rad + (size_t)k * S * (size_t)C;
+        double* adc = abs_dcoup ? abs_dcoup + (size_t)k * R : NULL;
+        double* adr = abs_drad ? abs_drad + (size_t)k * S * (size_t)C : NULL;
+        for (int r = 0; r < R; ++r) { dc[r] = 0.0; if (adc) adc[r] = 0.0; }
+        for (size_t i = 0; i < (size_t)S * (size_t)C; ++i) { dr[i] = 0.0; if (adr) adr[i] = 0.0; }
         int32_t d = dst[e];
         if (d < 0 || d >= N) continue;
-        const float* cp = coup + (size_t)e * ORACLE_ROWS;
-        const float* rp = rad + (size_t)e * ORACLE_SLOTS * (size_t)C;
-        const float* gn = g + (size_t)d * ORACLE_D * (size_t)C;
-        for (int r = 0; r < ORACLE_ROWS; ++r) {
+        const float* cp = coup + (size_t)e * R;
+        const float* rp = rad + (size_t)e * S * (size_t)C;
+        const float* gn = g + (size_t)d * D * (size_t)C;
+        for (int r = 0; r < R; ++r) {
             int s = slot_of_row(r);
             const float* grow = gn + (size_t)(1 + r) * (size_t)C;
             const float* rs = rp + (size_t)s * (size_t)C;

@@ -295,3 +295,133 @@ def run_all(fwd, bwd, csr):
         except PinFailure:
             failed.append(name)
     return failed
+
+
+# ---------------------------------------------------------------- general lmax
+#
+# The ladder of degree lmax: D = (lmax+1)^2 node rows, the scalar row then
+# degree groups of 2l+1 zonal rows (l = 1..lmax), radial slot l - 1 (the lmax
+# = 3 case is the pages' 3/5/7).  The slot list is built here by counting
+# rows degree by degree, independently of any implementation's formula.
+
+
+def ladder_slots(lmax):
+    slots = []
+    for l in range(1, lmax + 1):
+        slots += [l - 1] * (2 * l + 1)
+    return np.array(slots, np.int64)
+
+
+def tiny_graph_l(seed, N, E, C, lmax, *, quantised=False):
+    rng = np.random.default_rng(1000 * lmax + seed)
+    R = (lmax + 1) ** 2 - 1
+    dst = rng.integers(0, N, size=E).astype(np.int32)
+    if quantised:
+        coup = (rng.integers(-2 ** 19, 2 ** 19, size=(E, R)) / 2.0 ** 19).astype(np.float32)
+        rad = (rng.integers(-2 ** 18, 2 ** 18, size=(E, lmax, C)) / 2.0 ** 16).astype(np.float32)
+    else:
+        coup = rng.uniform(-1, 1, size=(E, R)).astype(np.float32)
+        rad = rng.standard_normal((E, lmax, C)).astype(np.float32)
+    g = rng.standard_normal((N, R + 1, C)).astype(np.float32)
+    return dst, coup, rad, g
+
+
+def brute_forward_l(coup, rad, dst, N, lmax):
+    E, C = rad.shape[0], rad.shape[2]
+    slots = ladder_slots(lmax)
+    out = np.zeros((N, len(slots) + 1, C))
+    for n in range(N):
+        for e in range(E):
+            if dst[e] != n:
+                continue
+            for r, s in enumerate(slots):
+                for c in range(C):
+                    out[n, 1 + r, c] += float(coup[e, r]) * float(rad[e, s, c])
+    return out
+
+
+def brute_backward_l(g, coup, rad, dst, N, lmax):
+    E, C = rad.shape[0], rad.shape[2]
+    slots = ladder_slots(lmax)
+    d_coup = np.zeros((E, len(slots)))
+    d_rad = np.zeros((E, lmax, C))
+    for e in range(E):
+        n = int(dst[e])
+        if n < 0 or n >= N:
+            continue
+        for r, s in enumerate(slots):
+            for c in range(C):
+                d_coup[e, r] += float(g[n, 1 + r, c]) * float(rad[e, s, c])
+                d_rad[e, s, c] += float(g[n, 1 + r, c]) * float(coup[e, r])
+    return d_coup, d_rad
+
+
+def pin_general_lmax(fwd, bwd, lmax):
+    """Brute force, closed forms, adjoint identity and finite differences at lmax."""
+    R = (lmax + 1) ** 2 - 1
+    slots = ladder_slots(lmax)
+    _require(len(slots) == R, "ladder size")
+    # brute force over every (node, edge) pair
+    for N, E, C, seed in ((5, 14, 3, 0), (3, 9, 2, 1)):
+        dst, coup, rad, g = tiny_graph_l(seed, N, E, C, lmax)
+        out = np.asarray(fwd(coup, rad, dst, N))
+        _require(out.shape == (N, R + 1, C), f"lmax {lmax} output shape {out.shape}")
+        _require(np.allclose(out, brute_forward_l(coup, rad, dst, N, lmax), rtol=1e-12, atol=1e-12),
+                 f"lmax {lmax} forward vs brute force")
+        dc, dr = bwd(g, coup, rad, dst, N)
+        rdc, rdr = brute_backward_l(g, coup, rad, dst, N, lmax)
+        _require(np.shape(dc) == rdc.shape and np.shape(dr) == rdr.shape, f"lmax {lmax} gradient shapes")
+        _require(np.allclose(dc, rdc, rtol=1e-12, atol=1e-12), f"lmax {lmax} d_coup vs brute force")
+        _require(np.allclose(dr, rdr, rtol=1e-12, atol=1e-12), f"lmax {lmax} d_rad vs brute force")
+    # all-ones operands: out = in-degree; d_coup = sum_c g; d_rad = the slot's rows of g summed
+    rng = np.random.default_rng(70 + lmax)
+    N, E, C = 7, 150, 4
+    dst = rng.integers(0, N, E).astype(np.int32)
+    out = np.asarray(fwd(np.ones((E, R), np.float32), np.ones((E, lmax, C), np.float32), dst, N))
+    indeg = np.bincount(dst, minlength=N).astype(np.float64)
+    _require(np.array_equal(out[:, 1:, :], np.broadcast_to(indeg[:, None, None], (N, R, C))), f"lmax {lmax} ones")
+    _require(np.all(out[:, 0, :] == 0), f"lmax {lmax} scalar row")
+    g = rng.standard_normal((N, R + 1, C)).astype(np.float32)
+    dc, dr = bwd(g, np.ones((E, R), np.float32), np.ones((E, lmax, C), np.float32), dst, N)
+    gd = g[dst].astype(np.float64)
+    _require(np.allclose(dc, gd[:, 1:, :].sum(2), rtol=1e-13, atol=1e-13), f"lmax {lmax} ones d_coup")
+    first = 0
+    for l in range(1, lmax + 1):
+        rows = slice(1 + first, 1 + first + 2 * l + 1)
+        _require(np.allclose(np.asarray(dr)[:, l - 1], gd[:, rows].sum(1), rtol=1e-13, atol=1e-13),
+                 f"lmax {lmax} ones d_rad degree {l}")
+        first += 2 * l + 1
+    # adjoint identity (the op is bilinear)
+    dst, coup, rad, g = tiny_graph_l(5, 11, 200, 3, lmax)
+    out = np.asarray(fwd(coup, rad, dst, 11))
+    dc, dr = bwd(g, coup, rad, dst, 11)
+    a = float(np.sum(g.astype(np.float64)[:, 1:] * out[:, 1:]))
+    b = float(np.sum(np.asarray(dc) * coup.astype(np.float64)))
+    c = float(np.sum(np.asarray(dr) * rad.astype(np.float64)))
+    scale = float(np.sum(np.abs(g.astype(np.float64)[dst][:, 1:] * coup.astype(np.float64)[:, :, None]
+                                * rad.astype(np.float64)[:, slots, :])))
+    _require(abs(a - b) <= 1e-12 * scale and abs(a - c) <= 1e-12 * scale, f"lmax {lmax} adjoint {a} {b} {c}")
+    # central differences with perturbations exact in fp32
+    h = 2.0 ** -10
+    N, E, C = 3, 6, 2
+    dst, coup, rad, g = tiny_graph_l(9, N, E, C, lmax, quantised=True)
+    g64 = g.astype(np.float64)
+
+    def L(cp, rd):
+        return float(np.sum(g64 * np.asarray(fwd(cp, rd, dst, N))))
+
+    dc, dr = bwd(g, coup, rad, dst, N)
+    dc = np.asarray(dc)
+    dr = np.asarray(dr)
+    scale = 1.0 + max(np.abs(dc).max(), np.abs(dr).max())
+    for e in range(E):
+        for r in sorted({0, R // 2, R - 1}):
+            p = coup.copy(); p[e, r] += np.float32(h)
+            m = coup.copy(); m[e, r] -= np.float32(h)
+            fd = (L(p, rad) - L(m, rad)) / (2 * h)
+            _require(abs(fd - dc[e, r]) <= 1e-9 * scale, f"lmax {lmax} FD d_coup[{e},{r}]")
+        for s in range(lmax):
+            p = rad.copy(); p[e, s, 0] += np.float32(h)
+            m = rad.copy(); m[e, s, 0] -= np.float32(h)
+            fd = (L(coup, p) - L(coup, m)) / (2 * h)
+            _require(abs(fd - dr[e, s, 0]) <= 1e-9 * scale, f"lmax {lmax} FD d_rad[{e},{s},0]")

@@ -61,6 +61,55 @@ def test_slot_map_matches_row_groups():
     # rows 0-2 -> degree 1, 3-7 -> degree 2, 8-14 -> degree 3 (row groups 3/5/7)
     assert [oracle.slot_of_row(r) for r in range(15)] == [0] * 3 + [1] * 5 + [2] * 7
     assert composition.slot_index().tolist() == [0] * 3 + [1] * 5 + [2] * 7
+    assert composition.row_groups(3) == composition.ROW_GROUPS
+    # further degrees continue the ladder: 9 rows of degree 4, 11 of degree 5
+    assert [oracle.slot_of_row(r) for r in range(35)] == pins.ladder_slots(5).tolist()
+
+
+@pytest.mark.parametrize("lmax", [1, 2, 3, 4, 5])
+def test_general_lmax_pins(lmax):
+    pins.pin_general_lmax(a_fwd, a_bwd, lmax)
+    pins.pin_general_lmax(b_fwd, b_bwd, lmax)
+
+
+def test_general_lmax_a_matches_composition():
+    for lmax in (1, 2, 4, 5):
+        w = workloads.make_random(40, 3000, 6, seed=lmax, lmax=lmax)
+        out_a = a_fwd(w.coup, w.rad, w.dst, w.N)
+        out_b = b_fwd(w.coup, w.rad, w.dst, w.N)
+        _, absum = oracle.forward(w.coup, w.rad, *oracle.build_csr(w.dst, w.N)[:2], w.N)
+        err, bad = oracle.normalised_error(out_a, out_b, absum)
+        assert err <= 1e-12 and bad == 0
+        dca, dra = a_bwd(w.grad_out, w.coup, w.rad, w.dst, w.N)
+        dcb, drb = b_bwd(w.grad_out, w.coup, w.rad, w.dst, w.N)
+        assert np.allclose(dca, dcb, rtol=1e-12, atol=1e-12) and np.allclose(dra, drb, rtol=1e-12, atol=1e-12)
+
+
+def _general_groups_mutant(groups):
+    # the composition with the degree-4/5 groups resized (rows move to the wrong slot)
+    def fwd(cp, rd, d, N):
+        old = composition.row_groups
+        composition.row_groups = lambda lmax=3: groups[:lmax]
+        try:
+            return composition.forward(cp, rd, d, N)
+        finally:
+            composition.row_groups = old
+
+    def bwd(g, cp, rd, d, N):
+        old = composition.row_groups
+        composition.row_groups = lambda lmax=3: groups[:lmax]
+        try:
+            return composition.backward(g, cp, rd, d, N)
+        finally:
+            composition.row_groups = old
+    return fwd, bwd
+
+
+@pytest.mark.parametrize("groups", [(3, 5, 7, 10, 10), (3, 5, 8, 8, 11), (3, 5, 7, 11, 9)])
+def test_general_lmax_planted_groups_caught(groups):
+    fwd, bwd = _general_groups_mutant(groups)
+    with pytest.raises(pins.PinFailure):
+        pins.pin_general_lmax(fwd, bwd, 5)
 
 
 # ----------------------------------------------------------- A against B
@@ -132,21 +181,20 @@ def _mut_slot_reversed():
 
 
 def _mut_groups(groups):
-    def fwd(cp, rd, d, N):
-        old = composition.ROW_GROUPS
-        composition.ROW_GROUPS = groups
+    # the composition with its row grouping replaced
+    def patched(call):
+        old = composition.row_groups
+        composition.row_groups = lambda lmax=3: groups
         try:
-            return composition.forward(cp, rd, d, N)
+            return call()
         finally:
-            composition.ROW_GROUPS = old
+            composition.row_groups = old
+
+    def fwd(cp, rd, d, N):
+        return patched(lambda: composition.forward(cp, rd, d, N))
 
     def bwd(g, cp, rd, d, N):
-        old = composition.ROW_GROUPS
-        composition.ROW_GROUPS = groups
-        try:
-            return composition.backward(g, cp, rd, d, N)
-        finally:
-            composition.ROW_GROUPS = old
+        return patched(lambda: composition.backward(g, cp, rd, d, N))
     return fwd, bwd, a_csr
 
 
