@@ -43,12 +43,20 @@ KERNEL_SOURCES = {
 
 # ---------------------------------------------------------------- byte models
 
-def algorithmic_bytes(N: int, E: int, C: int) -> dict:
-    """Bytes each step must move at least (fp32 data, int32 indices)."""
-    fwd = E * (4 + 60 + 12 * C) + 4 * (N + 1) + 64 * N * C
-    bwd = E * (4 + 60 + 12 * C + 60 + 12 * C) + 64 * N * C
+def algorithmic_bytes(N: int, E: int, C: int, lmax: int = 3) -> dict:
+    """Bytes each step must move at least (fp32 data, int32 indices); ladder of
+    degree lmax: R = (lmax+1)^2 - 1 coupling rows, lmax radial slots, D = R + 1
+    node rows (R = 15, D = 16 at lmax = 3)."""
+    D = (lmax + 1) ** 2
+    R = D - 1
+    fwd = E * (4 + 4 * R + 4 * lmax * C) + 4 * (N + 1) + 4 * D * N * C
+    bwd = E * (4 + 4 * R + 4 * lmax * C + 4 * R + 4 * lmax * C) + 4 * D * N * C
     csr = E * (4 + 4) + 4 * (N + 1)
     return {"fwd": fwd, "bwd": bwd, "csr": csr}
+
+
+def metric_for(lmax: int) -> str:
+    return METRIC if lmax == 3 else METRIC.replace("C=32;", f"C=32,lmax={lmax};")
 
 
 def measured_peaks() -> tuple[float, str]:
@@ -107,7 +115,9 @@ def job_throughput(units_per_rank: int, steps: int, max_ms: float, world: int) -
 
 def workload_config(w, backward: str) -> dict:
     entry = "zs_backward_csr" if backward == "csr" else "zs_backward"
-    return {"workload": f"{w.name}: N={w.N}, E={w.E}, C={w.C}, lmax=3 (rows 3/5/7), fp32, seed {w.seed}",
+    lmax = w.rad.shape[1]
+    rows = "/".join(str(2 * l + 1) for l in range(1, lmax + 1))
+    return {"workload": f"{w.name}: N={w.N}, E={w.E}, C={w.C}, lmax={lmax} (rows {rows}), fp32, seed {w.seed}",
             "step": "zs_build_csr + zs_forward + " + entry,
             "l2": ("inputs larger than L2" if w.coup.nbytes + w.rad.nbytes > L2_BYTES else
                    "inputs smaller than L2, no flush") + " (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6)}
@@ -185,8 +195,9 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    w = workloads.make_workload(args.config)
-    N, E, C = w.N, w.E, w.C
+    w = workloads.make_workload(args.config, lmax=args.lmax)
+    N, E, C, L = w.N, w.E, w.C, args.lmax
+    D, R = (L + 1) ** 2, (L + 1) ** 2 - 1
     dev = torch.device("cuda", local)
     lib = zs.load()
 
@@ -198,10 +209,10 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     perm = torch.empty(E, dtype=torch.int32, device=dev)
     bad = torch.empty(1, dtype=torch.int32, device=dev)
     ws_csr = torch.empty(max(1, zs.zs_build_csr_workspace_bytes(E, N)), dtype=torch.uint8, device=dev)
-    ws_fwd = torch.empty(max(1, zs.zs_forward_workspace_bytes(E, N, C)), dtype=torch.uint8, device=dev)
-    out = torch.empty((N, 16, C), dtype=torch.float32, device=dev)
-    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev)
-    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev)
+    ws_fwd = torch.empty(max(1, zs.zs_forward_workspace_bytes(E, N, C, L)), dtype=torch.uint8, device=dev)
+    out = torch.empty((N, D, C), dtype=torch.float32, device=dev)
+    d_coup = torch.empty((E, R), dtype=torch.float32, device=dev)
+    d_rad = torch.empty((E, L, C), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
@@ -213,15 +224,15 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         assert st == 0, lib.zs_last_error()
 
     def fwd():
-        st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, 3, P(out), P(ws_fwd), fwd_ws_bytes, sp)
+        st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(out), P(ws_fwd), fwd_ws_bytes, sp)
         assert st == 0, lib.zs_last_error()
 
     def bwd_edge():
-        st = lib.zs_backward(P(g), P(coup), P(rad), P(dst), E, N, C, 3, P(d_coup), P(d_rad), sp)
+        st = lib.zs_backward(P(g), P(coup), P(rad), P(dst), E, N, C, L, P(d_coup), P(d_rad), sp)
         assert st == 0, lib.zs_last_error()
 
     def bwd_csr():
-        st = lib.zs_backward_csr(P(g), P(coup), P(rad), P(row_ptr), P(perm), E, N, C, 3, P(d_coup), P(d_rad), sp)
+        st = lib.zs_backward_csr(P(g), P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(d_coup), P(d_rad), sp)
         assert st == 0, lib.zs_last_error()
 
     bwd, bwd_other, other_name = (bwd_csr, bwd_edge, "bwd_edge") if args.backward == "csr" else \
@@ -229,15 +240,15 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
     # zs_build_csr: three launches on its one-pass counting path (N + 1 <= 5120),
     # else three per 8-bit radix pass plus the row_ptr pass (one launch for E = 0);
-    # zs_forward: one kernel at C = 32 (aligned tensors), else main kernel and
-    # fix-up; the backward: one kernel (none for E = 0)
+    # zs_forward: one kernel at lmax = 3, C = 32 (aligned tensors), else main
+    # kernel and fix-up; the backward: one kernel (none for E = 0)
     if E == 0:
         csr_launches = 1
     elif N + 1 <= 5120:
         csr_launches = 3
     else:
         csr_launches = 3 * max(1, (max(N, 1).bit_length() + 7) // 8) + 1
-    launches_per_step = csr_launches + (1 if C == 32 else 2) + (1 if E > 0 else 0)
+    launches_per_step = csr_launches + (1 if (C == 32 and L == 3) else 2) + (1 if E > 0 else 0)
 
     for _ in range(args.warmup):
         csr(); fwd(); bwd()
@@ -333,7 +344,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     if rank != 0:
         return None
 
-    ab = algorithmic_bytes(N, E, C)
+    ab = algorithmic_bytes(N, E, C, L)
     peak, peak_kind = measured_peaks()
     kernels = {}
     ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
@@ -348,12 +359,12 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     roof = {"kernel": {"fwd": "zs_forward", "bwd": bwd_entry}[dom], "bound": "hbm",
             "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
             "frac": kernels[dom]["GBs"] / peak, "peak_kind": peak_kind,
-            "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config),
+            "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config) if L == 3 else None,
             "algorithmic_bytes_per_launch": ab[dom]}
     ms_per_step = total_ms / args.steps
     fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
     res = {
-        "metric": METRIC,
+        "metric": metric_for(L),
         "value": job_throughput(E, args.steps, total_ms, world),
         "unit": "edges/s",
         "n_gpus": world,
@@ -379,13 +390,13 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def run_oracle(config: str, min_seconds: float, w=None) -> dict:
+def run_oracle(config: str, min_seconds: float, w=None, lmax: int = 3) -> dict:
     """The fp64 oracle (single-threaded C) on the full graph, repeated until
     min_seconds of CPU work has been timed."""
     import oracle
     from equivariant_interatomic_potential_gb300 import workloads
 
-    w = workloads.make_workload(config) if w is None else w
+    w = workloads.make_workload(config, lmax=lmax) if w is None else w
     oracle.build()
     reps, t_csr, t_fwd, t_bwd = 0, 0.0, 0.0, 0.0
     while reps == 0 or (t_csr + t_fwd + t_bwd) < min_seconds:
@@ -422,6 +433,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--lmax", type=int, default=3, choices=[1, 2, 3, 4, 5],
+                    help="ladder degree of the operands (3: the 3/5/7 rows of the headline workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -434,7 +447,7 @@ def main():
         if rank != 0:
             return
         from equivariant_interatomic_potential_gb300 import workloads
-        w = workloads.make_workload(args.config)
+        w = workloads.make_workload(args.config, lmax=args.lmax)
         t0 = time.perf_counter()
         steps = []
         for i in range(args.warmup + args.steps):
@@ -445,7 +458,7 @@ def main():
         val = w.E / (ms / 1e3)
         sample = (f"full {w.name} graph (N={w.N}, E={w.E}, C={w.C}) per step: csr build, forward, backward, "
                   f"fp64 sequential C, {args.steps} timed steps after {args.warmup} warm-up")
-        res = {"impl": "reference", "metric": METRIC, "value": val, "unit": "edges/s", "n_gpus": world,
+        res = {"impl": "reference", "metric": metric_for(args.lmax), "value": val, "unit": "edges/s", "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                "config": dict(workload_config(w, args.backward), parallelism="replicas" if world > 1 else "single GPU"),
@@ -463,7 +476,7 @@ def main():
         res = run_gpu_arm(args, rank, world)
         if rank == 0 and res is not None:
             if not args.no_cpu_baseline:
-                res["cpu_baseline"] = run_oracle(args.config, args.cpu_seconds)
+                res["cpu_baseline"] = run_oracle(args.config, args.cpu_seconds, lmax=args.lmax)
             print(json.dumps(res))
     finally:
         if world > 1:

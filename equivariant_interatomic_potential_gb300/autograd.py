@@ -46,20 +46,23 @@ def _(dst, num_nodes):
 @torch.library.custom_op(f"{_NS}::zonal_scatter", mutates_args=())
 def zonal_scatter(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, row_ptr: torch.Tensor,
                   perm: torch.Tensor, num_nodes: int) -> torch.Tensor:
-    """out (N, 16, C): row 0 zero, rows 1..15 the zonal scatter of coup (E, 15) x rad (E, 3, C)."""
+    """out (N, D, C): row 0 zero, rows 1..D-1 the zonal scatter of coup (E, D-1) x rad (E, lmax, C).
+
+    lmax = rad.shape[1] (3 for the pages' 3/5/7 ladder), D = (lmax + 1)^2."""
     _cuda_only("zonal_scatter", coup, rad, dst, row_ptr, perm)
     return zs.zs_forward(coup.contiguous(), rad.contiguous(), row_ptr.contiguous(), perm.contiguous(), num_nodes)
 
 
 @zonal_scatter.register_fake
 def _(coup, rad, dst, row_ptr, perm, num_nodes):
-    return coup.new_empty((num_nodes, 16, rad.shape[2]))
+    # ladder of degree lmax = rad.shape[1]: (lmax + 1)^2 node rows
+    return coup.new_empty((num_nodes, (rad.shape[1] + 1) ** 2, rad.shape[2]))
 
 
 @torch.library.custom_op(f"{_NS}::zonal_scatter_backward", mutates_args=())
 def zonal_scatter_backward(grad_out: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor,
                            num_nodes: int) -> tuple[torch.Tensor, torch.Tensor]:
-    """(d_coup (E, 15), d_rad (E, 3, C)) for the cotangent grad_out (N, 16, C); edge order."""
+    """(d_coup (E, D-1), d_rad (E, lmax, C)) for the cotangent grad_out (N, D, C); edge order."""
     _cuda_only("zonal_scatter_backward", grad_out, coup, rad, dst)
     return zs.zs_backward(grad_out.contiguous(), coup.contiguous(), rad.contiguous(), dst.contiguous(), num_nodes)
 

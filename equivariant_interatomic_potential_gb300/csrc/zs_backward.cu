@@ -1,4 +1,5 @@
-// Backward of the zonal scatter, lmax = 3, one edge-parallel pass:
+// Backward of the zonal scatter, one edge-parallel pass (lmax = 3 ladder shown;
+// the per-channel kernels take any ladder degree 1..5 the same way):
 //   d_coup[e,r]  = sum_c g[dst[e],1+r,c] * rad[e,slot(r),c]
 //   d_rad[e,s,c] = sum over rows r of slot s of g[dst[e],1+r,c] * coup[e,r]
 // (deepmd-kit pull request "fused Triton zonal scatter for the GIE head",
@@ -34,54 +35,69 @@ constexpr unsigned kFull = 0xffffffffu;
 // Per-channel path (any C, any alignment): lane = channel within a chunk of
 // 32; d_coup is reduced over the warp after the channel loop.
 // --------------------------------------------------------------------------
+// Sum over the warp of 32 values at once, each lane ending with the total
+// of value `lane` (a transposed butterfly: 16 + 8 + 4 + 2 + 1 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float v[32], int lane) {
+#pragma unroll
+    for (int half = 16; half >= 1; half >>= 1) {
+        const bool up = (lane & half) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float keep = up ? v[k + half] : v[k];
+            const float send = up ? v[k] : v[k + half];
+            v[k] = keep + __shfl_xor_sync(kFull, send, half);
+        }
+    }
+    return v[0];
+}
+
 // Gradients of one edge e whose destination is d (d < 0: no node, zero
-// gradients), lane = channel within chunks of 32.
+// gradients), lane = channel within chunks of 32; ladder of degree L.
+template <int L>
 __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const float* __restrict__ coup,
                                              const float* __restrict__ rad, int64_t e, int d, int C, int lane,
                                              float* __restrict__ d_coup, float* __restrict__ d_rad) {
+    constexpr int R = Ladder<L>::R, S = Ladder<L>::S, D = Ladder<L>::D;
+    constexpr int RP = (R + 31) / 32 * 32;   // rows padded to whole warps for the reduction
     const bool ok = d >= 0;
-    float cv[15];
+    float cv[R];
 #pragma unroll
-    for (int r = 0; r < 15; ++r) cv[r] = __ldg(coup + e * 15 + r);
-    float pc[15];
+    for (int r = 0; r < R; ++r) cv[r] = __ldg(coup + e * R + r);
+    float pc[RP];
 #pragma unroll
-    for (int r = 0; r < 15; ++r) pc[r] = 0.f;
-    const float* rp = rad + e * 3 * C;
-    float* drp = d_rad + e * 3 * C;
-    const float* gn = g + (int64_t)(ok ? d : 0) * 16 * C;
+    for (int r = 0; r < RP; ++r) pc[r] = 0.f;
+    const float* rp = rad + e * S * C;
+    float* drp = d_rad + e * S * C;
+    const float* gn = g + (int64_t)(ok ? d : 0) * D * C;
     for (int c = lane; c < C; c += 32) {
         if (!ok) {
-            drp[c] = 0.f; drp[C + c] = 0.f; drp[2 * C + c] = 0.f;
+#pragma unroll
+            for (int k = 0; k < S; ++k) drp[k * C + c] = 0.f;
             continue;
         }
-        const float r0 = __ldg(rp + c), r1 = __ldg(rp + C + c), r2 = __ldg(rp + 2 * C + c);
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+        float rv[S], sv[S];
 #pragma unroll
-        for (int r = 0; r < 15; ++r) {
-            const float gv = __ldg(gn + (1 + r) * C + c);
-            const float rv = r < 3 ? r0 : (r < 8 ? r1 : r2);
-            pc[r] = fmaf(gv, rv, pc[r]);
-            if (r < 3) s0 = fmaf(gv, cv[r], s0);
-            else if (r < 8) s1 = fmaf(gv, cv[r], s1);
-            else s2 = fmaf(gv, cv[r], s2);
+        for (int k = 0; k < S; ++k) {
+            rv[k] = __ldg(rp + k * C + c);
+            sv[k] = 0.f;
         }
-        drp[c] = s0; drp[C + c] = s1; drp[2 * C + c] = s2;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float gv = __ldg(gn + (1 + r) * C + c);
+            pc[r] = fmaf(gv, rv[ladder_slot(r)], pc[r]);
+            sv[ladder_slot(r)] = fmaf(gv, cv[r], sv[ladder_slot(r)]);
+        }
+#pragma unroll
+        for (int k = 0; k < S; ++k) drp[k * C + c] = sv[k];
     }
 #pragma unroll
-    for (int r = 0; r < 15; ++r) {
-        float v = pc[r];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-        pc[r] = v;
-    }
-    if (lane < 15) {
-        float v = 0.f;
-#pragma unroll
-        for (int r = 0; r < 15; ++r) if (r == lane) v = pc[r];
-        d_coup[e * 15 + lane] = ok ? v : 0.f;
+    for (int r0 = 0; r0 < RP; r0 += 32) {
+        const float v = warp_reduce_scatter32(pc + r0, lane);
+        if (r0 + lane < R) d_coup[e * R + r0 + lane] = ok ? v : 0.f;
     }
 }
 
+template <int L>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
         const int32_t* __restrict__ dst, int64_t E, int32_t N, int C,
@@ -91,7 +107,7 @@ bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float
     pdl_trigger();
     for (int64_t e = (int64_t)blockIdx.x * kBwdWarps + warp; e < E; e += (int64_t)gridDim.x * kBwdWarps) {
         const int d = __ldg(dst + e);
-        bwd_gen_edge(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad);
+        bwd_gen_edge<L>(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad);
     }
 }
 
@@ -458,6 +474,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
 }
 
 // Per-channel CSR-order backward (any C, any alignment): same walk, no TMA.
+template <int L>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
@@ -480,7 +497,7 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
         }
         const int e = __ldg(perm + pos);
         if ((uint32_t)e >= (uint64_t)E) continue;
-        bwd_gen_edge(g, coup, rad, e, d, C, lane, d_coup, d_rad);
+        bwd_gen_edge<L>(g, coup, rad, e, d, C, lane, d_coup, d_rad);
     }
 }
 
@@ -523,6 +540,24 @@ zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s) {
     return check_launch("zs_selftest_bounded_wait");
 }
 
+template <int L>
+void launch_gen_edges(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
+                      int C, float* d_coup, float* d_rad, cudaStream_t s) {
+    const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
+    const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
+    launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad);
+}
+
+template <int L>
+void launch_gen_csr(const float* g, const float* coup, const float* rad, const int32_t* row_ptr,
+                    const int32_t* perm, int64_t E, int32_t N, int C, float* d_coup, float* d_rad, cudaStream_t s) {
+    const int64_t KW = 64;
+    const int64_t Wtot = (E + KW - 1) / KW;
+    const int64_t ctas = (Wtot + kBwdWarps - 1) / kBwdWarps;
+    launch(bwd_csr_gen<L>, (unsigned)ctas, kBwdThreads, 0, s, g, coup, rad, row_ptr, perm, E, N, C, KW, (int)Wtot,
+           d_coup, d_rad);
+}
+
 }  // namespace zs
 
 using namespace zs;
@@ -530,14 +565,15 @@ using namespace zs;
 extern "C" zs_status zs_backward(const float* g, const float* coup, const float* rad,
                                  const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
                                  float* d_coup, float* d_rad, zs_stream_t stream) {
-    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_backward: lmax=%d, only lmax=3 (row groups 3/5/7) is supported", lmax);
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "zs_backward: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward: E=%lld exceeds the int32 index range", (long long)E);
     if (E == 0) return ZS_OK;
     if (!coup || !rad || !dst || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward: NULL array with E > 0");
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward: g is NULL with N > 0");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
+    const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
         // While the cotangent block is small enough to stay in L2 next to the
         // streams, more warps with one tile in flight each hide the gather
@@ -547,9 +583,13 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
         if (small_g) launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
         else launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
     } else {
-        const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
-        const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
-        launch(bwd_gen, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad);
+        switch (lmax) {
+            case 1: launch_gen_edges<1>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+            case 2: launch_gen_edges<2>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+            case 3: launch_gen_edges<3>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+            case 4: launch_gen_edges<4>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+            default: launch_gen_edges<5>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+        }
     }
     return check_launch("zs_backward");
 }
@@ -558,7 +598,8 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
                                      const int32_t* row_ptr, const int32_t* perm,
                                      int64_t E, int32_t N, int32_t C, int32_t lmax,
                                      float* d_coup, float* d_rad, zs_stream_t stream) {
-    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_backward_csr: lmax=%d, only lmax=3 (row groups 3/5/7) is supported", lmax);
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "zs_backward_csr: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: E=%lld exceeds the int32 index range", (long long)E);
     if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: row_ptr is NULL");
@@ -566,7 +607,7 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
     if (!coup || !rad || !perm || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: NULL array with E > 0");
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: g is NULL with N > 0");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
+    const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
         constexpr int W = ZS_BWD_WARPS, S = ZS_BWD_STAGES, T = ZS_BWD_TILE;
         const int64_t warps_max = (int64_t)num_sms() * W;
@@ -579,11 +620,13 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
         launch(bwd_csr_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
                (int)KW, (int)Wtot, d_coup, d_rad);
     } else {
-        const int64_t KW = 64;
-        const int64_t Wtot = (E + KW - 1) / KW;
-        const int64_t ctas = (Wtot + kBwdWarps - 1) / kBwdWarps;
-        launch(bwd_csr_gen, (unsigned)ctas, kBwdThreads, 0, s, g, coup, rad, row_ptr, perm, E, N, C, KW, (int)Wtot,
-                                                            d_coup, d_rad);
+        switch (lmax) {
+            case 1: launch_gen_csr<1>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
+            case 2: launch_gen_csr<2>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
+            case 3: launch_gen_csr<3>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
+            case 4: launch_gen_csr<4>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
+            default: launch_gen_csr<5>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
+        }
     }
     return check_launch("zs_backward_csr");
 }

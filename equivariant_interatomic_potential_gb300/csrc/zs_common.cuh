@@ -18,6 +18,27 @@ constexpr int kD = 16;      // node rows: scalar row + 15
 // Degree group of zonal row r as a radial slot (row groups 3/5/7).
 __host__ __device__ __forceinline__ int slot_of_row(int r) { return r < 3 ? 0 : (r < 8 ? 1 : 2); }
 
+// The ladder of degree L (1..kMaxLmax): D = (L+1)^2 node rows, the scalar row
+// then degree groups of 2l+1 zonal rows for l = 1..L (3/5/7 at L = 3), radial
+// slot l - 1 for the rows of degree l.
+constexpr int kMaxLmax = 5;
+template <int L>
+struct Ladder {
+    static_assert(L >= 1 && L <= kMaxLmax, "ladder degree 1..5");
+    static constexpr int D = (L + 1) * (L + 1);
+    static constexpr int R = D - 1;
+    static constexpr int S = L;
+};
+
+// Radial slot of zonal row r: degree l holds rows [l^2 - 1, (l+1)^2 - 1).
+__host__ __device__ constexpr int ladder_slot(int r) {
+    int l = 1;
+    while ((l + 1) * (l + 1) - 1 <= r) ++l;
+    return l - 1;
+}
+
+inline int ladder_rows(int lmax) { return (lmax + 1) * (lmax + 1) - 1; }
+
 // Record a message for zs_last_error() and return the status.
 zs_status fail(zs_status st, const char* fmt, ...);
 // Check the last launch on this thread; ZS_ERR_CUDA with a message on failure.

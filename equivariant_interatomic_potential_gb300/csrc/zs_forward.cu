@@ -336,9 +336,12 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
 // leaves a partial per window in the workspace.
 // --------------------------------------------------------------------------
 
+template <int L>
 __device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, const float* __restrict__ rad,
                                                const int32_t* __restrict__ perm, int64_t E, int C, int c,
-                                               int s, int t, float (*cs)[16], int lane, float acc[kRows]) {
+                                               int s, int t, float (*cs)[Ladder<L>::R + 1], int lane,
+                                               float acc[Ladder<L>::R]) {
+    constexpr int R = Ladder<L>::R, S = Ladder<L>::S;
     const bool cok = c < C;
     for (int base = s; base < t; base += 32) {
         const int cnt = min(32, t - base);
@@ -347,44 +350,46 @@ __device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, c
             e_l = __ldg(perm + base + lane);
             if ((uint32_t)e_l >= (uint64_t)E) e_l = -1;
         }
+        // the coupling rows of the (up to) 32 edges, staged through shared memory
 #pragma unroll
-        for (int it = 0; it < kRows; ++it) {
+        for (int it = 0; it < R; ++it) {
             const int v = it * 32 + lane;
-            const int j = v / kRows;
-            const int r = v - j * kRows;
+            const int j = v / R;
+            const int r = v - j * R;
             const int e = __shfl_sync(kFull, e_l, j);
             float cv = 0.f;
-            if (j < cnt && e >= 0) cv = __ldg(coup + (int64_t)e * kRows + r);
+            if (j < cnt && e >= 0) cv = __ldg(coup + (int64_t)e * R + r);
             cs[j][r] = cv;
         }
         __syncwarp();
         for (int j = 0; j < cnt; ++j) {
             const int e = __shfl_sync(kFull, e_l, j);
             if (e < 0 || !cok) continue;
-            const float* rp = rad + (int64_t)e * kSlots * C + c;
-            const float r0 = __ldg(rp), r1 = __ldg(rp + C), r2 = __ldg(rp + 2 * C);
+            const float* rp = rad + (int64_t)e * S * C + c;
+            float rv[S];
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                const float rv = r < 3 ? r0 : (r < 8 ? r1 : r2);
-                acc[r] = fmaf(cs[j][r], rv, acc[r]);
-            }
+            for (int k = 0; k < S; ++k) rv[k] = __ldg(rp + k * C);
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[r] = fmaf(cs[j][r], rv[ladder_slot(r)], acc[r]);
         }
         __syncwarp();
     }
 }
 
+template <int L>
 __global__ void __launch_bounds__(kFwdThreads)
 fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
              const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
              int64_t E, int32_t N, int C, int Wtot, float* __restrict__ out, float* __restrict__ part,
              int32_t* __restrict__ cross) {
-    __shared__ float cs[kFwdWarps][32][16];
+    constexpr int R = Ladder<L>::R, D = Ladder<L>::D;
+    __shared__ float cs[kFwdWarps][32][R + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kFwdWarps + warp;
     pdl_wait();
     pdl_trigger();
     if (gw >= Wtot) return;
-    const int64_t V = (int64_t)kRows * C;
+    const int64_t V = (int64_t)R * C;
     const int64_t p0 = (int64_t)gw * kGenWin;
     const int64_t p1 = min(p0 + kGenWin, E);
     const bool is_last = gw == Wtot - 1;
@@ -392,9 +397,9 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
     for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
         const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
         if (a >= p1 && !(is_last && a == b)) break;
-        float* node = out + (int64_t)n * kD * C;
+        float* node = out + (int64_t)n * D * C;
         if (a == b) {
-            for (int64_t i = lane; i < (int64_t)kD * C; i += 32) node[i] = 0.f;
+            for (int64_t i = lane; i < (int64_t)D * C; i += 32) node[i] = 0.f;
             continue;
         }
         const bool full = a >= p0 && b <= p1;
@@ -403,14 +408,14 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
             for (int c = lane; c < C; c += 32) node[c] = 0.f;
         for (int c0 = 0; c0 < C; c0 += 32) {
             const int c = c0 + lane;
-            float acc[kRows];
+            float acc[R];
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
-            accumulate_gen(coup, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
-                           cs[warp], lane, acc);
+            for (int r = 0; r < R; ++r) acc[r] = 0.f;
+            accumulate_gen<L>(coup, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
+                              cs[warp], lane, acc);
             if (c < C) {
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) dstp[(int64_t)r * C + c] = acc[r];
+                for (int r = 0; r < R; ++r) dstp[(int64_t)r * C + c] = acc[r];
             }
         }
         if (!full && a >= p0) crossing = n;
@@ -432,11 +437,11 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
 constexpr int kFixVals = 256;   // values per chunk: 8 per lane
 
 __global__ void __launch_bounds__(kFwdThreads)
-fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross, int C, int win,
+fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross, int C, int R, int win,
           const float* __restrict__ part, float* __restrict__ out) {
     __shared__ float red[kFwdWarps][kFixVals];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t V = (int64_t)kRows * C;
+    const int64_t V = (int64_t)R * C;
     const int wa = blockIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -444,7 +449,7 @@ fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross
     if (n < 0) return;
     const int b = __ldg(row_ptr + n + 1);
     const int np = (b - 1) / win - wa + 1;
-    float* node = out + (int64_t)n * kD * C;
+    float* node = out + (int64_t)n * (R + 1) * C;
     for (int c = threadIdx.x; c < C; c += kFwdThreads) node[c] = 0.f;
     for (int64_t v0 = 0; v0 < V; v0 += kFixVals) {
         float sacc[kFixVals / 32];
@@ -494,19 +499,21 @@ struct Scratch {
     uint64_t* flags;
 };
 
-static size_t part_bytes(int64_t windows, int C) { return align_up((size_t)windows * 2 * kRows * (size_t)C * sizeof(float), 256); }
+static size_t part_bytes(int64_t windows, int C, int R) {
+    return align_up((size_t)windows * 2 * (size_t)R * (size_t)C * sizeof(float), 256);
+}
 
-static size_t scratch_bytes(int64_t windows, int C) {
-    return part_bytes(windows, C) + align_up((size_t)windows * sizeof(int32_t), 256) +
+static size_t scratch_bytes(int64_t windows, int C, int R) {
+    return part_bytes(windows, C, R) + align_up((size_t)windows * sizeof(int32_t), 256) +
            align_up((size_t)windows * sizeof(uint64_t), 256);
 }
 
-static Scratch scratch_at(void* base, int64_t windows, int C) {
+static Scratch scratch_at(void* base, int64_t windows, int C, int R) {
     char* b = static_cast<char*>(base);
     Scratch sc;
     sc.part = reinterpret_cast<float*>(b);
-    sc.cross = reinterpret_cast<int32_t*>(b + part_bytes(windows, C));
-    sc.flags = reinterpret_cast<uint64_t*>(b + part_bytes(windows, C) + align_up((size_t)windows * sizeof(int32_t), 256));
+    sc.cross = reinterpret_cast<int32_t*>(b + part_bytes(windows, C, R));
+    sc.flags = reinterpret_cast<uint64_t*>(b + part_bytes(windows, C, R) + align_up((size_t)windows * sizeof(int32_t), 256));
     return sc;
 }
 
@@ -516,14 +523,77 @@ static uint64_t next_salt() {
     return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
 }
 
-extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
-    if (E < 0 || N < 0 || C < 1) return 0;
+// How zs_forward splits a call: the C == 32 single-wave kernel (lmax 3,
+// 16-byte aligned operands) or the per-channel kernel and its fix-up.
+struct FwdPlan {
+    bool fast;
+    int R;
+    int64_t KW, Wtot, ctas, windows;
+};
+
+static FwdPlan fwd_plan(const float* coup, const float* rad, const float* out, int64_t E, int C, int lmax) {
+    FwdPlan p{};
+    p.R = ladder_rows(lmax);
+    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
+    if (p.fast) {
+        // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
+        // the same number of CSR positions (at least one tile).
+        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
+        p.KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
+        p.Wtot = imax<int64_t>(ceil_div(E, p.KW), 1);
+        p.ctas = ceil_div(p.Wtot, kTmaWarps);
+        p.windows = p.ctas;
+    } else {
+        p.Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
+        p.ctas = ceil_div(p.Wtot, kFwdWarps);
+        p.windows = p.Wtot;
+    }
+    return p;
+}
+
+template <int L>
+static void launch_gen(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t E, int32_t N, int C, float* out, const Scratch& sc,
+                       cudaStream_t s) {
+    launch(fwd_gen_main<L>, (unsigned)p.ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)p.Wtot,
+           out, sc.part, sc.cross);
+    launch(fwd_fixup, (unsigned)p.Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, Ladder<L>::R,
+           kGenWin, (const float*)sc.part, out);
+}
+
+static void launch_forward(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
+                           const int32_t* perm, int64_t E, int32_t N, int C, int lmax, float* out,
+                           const Scratch& sc, cudaStream_t s) {
+    if (p.fast) {
+        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
+        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)p.ctas, kTmaWarps * 32, smem, s,
+               coup, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, out, sc.part, sc.flags, next_salt());
+        return;
+    }
+    switch (lmax) {
+        case 1: launch_gen<1>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+        case 2: launch_gen<2>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+        case 3: launch_gen<3>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+        case 4: launch_gen<4>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+        default: launch_gen<5>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+    }
+}
+
+extern "C" size_t zs_forward_workspace_bytes_lmax(int64_t E, int32_t N, int32_t C, int32_t lmax) {
+    if (E < 0 || N < 0 || C < 1 || lmax < 1 || lmax > kMaxLmax) return 0;
     (void)N;
     // Sized for the smaller of the two window lengths: kGenWin positions per
     // warp on the per-channel path, at least kTmaWarps * kTile per CTA on the
-    // C == 32 path.
-    const int64_t windows = ceil_div(E > 0 ? E : 1, imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile)) + 1;
-    return scratch_bytes(windows, C);
+    // C == 32 path (lmax 3 only).
+    const int64_t win = lmax == 3 ? imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile) : kGenWin;
+    const int64_t windows = ceil_div(E > 0 ? E : 1, win) + 1;
+    return scratch_bytes(windows, C, ladder_rows(lmax));
+}
+
+extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
+    return zs_forward_workspace_bytes_lmax(E, N, C, 3);
 }
 
 extern "C" zs_status zs_forward(const float* coup, const float* rad,
@@ -531,41 +601,21 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
                                 int64_t E, int32_t N, int32_t C, int32_t lmax,
                                 float* out, void* workspace, size_t workspace_bytes,
                                 zs_stream_t stream) {
-    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_forward: lmax=%d, only lmax=3 (row groups 3/5/7) is supported", lmax);
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "zs_forward: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: E=%lld exceeds the int32 index range", (long long)E);
     if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_forward: row_ptr is NULL");
     if (N > 0 && !out) return fail(ZS_ERR_INVALID_ARG, "zs_forward: out is NULL");
     if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward: coup, rad or perm is NULL with E > 0");
-    const size_t need = zs_forward_workspace_bytes(E, N, C);
+    const size_t need = zs_forward_workspace_bytes_lmax(E, N, C, lmax);
     if (workspace_bytes < need) return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace of %zu bytes, %zu needed", workspace_bytes, need);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace NULL or not 256-byte aligned");
     if (N == 0) return ZS_OK;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
-    if (fast) {
-        // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
-        // the same number of CSR positions (at least one tile).
-        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
-        const int64_t KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
-        const int64_t Wtot = imax<int64_t>(ceil_div(E, KW), 1);
-        const int64_t ctas = ceil_div(Wtot, kTmaWarps);
-        const Scratch sc = scratch_at(workspace, ctas, C);
-        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
-        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, sc.part, sc.flags, next_salt());
-    } else {
-        const int64_t Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
-        const int64_t ctas = ceil_div(Wtot, kFwdWarps);
-        const Scratch sc = scratch_at(workspace, Wtot, C);
-        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
-               sc.part, sc.cross);
-        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, kGenWin,
-               (const float*)sc.part, out);
-    }
+    const FwdPlan p = fwd_plan(coup, rad, out, E, C, lmax);
+    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, out, scratch_at(workspace, p.windows, C, p.R),
+                   reinterpret_cast<cudaStream_t>(stream));
     return check_launch("zs_forward");
 }
 
@@ -611,28 +661,17 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
                                         const int32_t* row_ptr, const int32_t* perm,
                                         int64_t E, int32_t N, int32_t C, int32_t lmax,
                                         float* out, zs_stream_t stream) {
-    if (lmax != 3) return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: lmax=%d, only lmax=3 is supported", lmax);
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: E=%lld exceeds the int32 index range", (long long)E);
     if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: row_ptr is NULL");
     if (N > 0 && !out) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: out is NULL");
     if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: coup, rad or perm is NULL with E > 0");
     if (N == 0) return ZS_OK;
-    const bool fast = C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
     // the same split as zs_forward; the scratch holds one pair of partials per window
-    int64_t KW = 0, Wtot = 0, ctas = 0, windows = 0;
-    if (fast) {
-        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
-        KW = imax<int64_t>(ceil_div(E, warps_max), kTile);
-        Wtot = imax<int64_t>(ceil_div(E, KW), 1);
-        ctas = ceil_div(Wtot, kTmaWarps);
-        windows = ctas;
-    } else {
-        Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
-        ctas = ceil_div(Wtot, kFwdWarps);
-        windows = Wtot;
-    }
-    const size_t need = scratch_bytes(windows, C);
+    const FwdPlan p = fwd_plan(coup, rad, out, E, C, lmax);
+    const size_t need = scratch_bytes(p.windows, C, p.R);
     if (need > kNoAllocScratchBytes)
         return fail(ZS_ERR_INVALID_ARG,
                     "zs_forward_noalloc: this call needs %zu bytes of scratch but the library's static scratch holds "
@@ -640,19 +679,7 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     float* base = nullptr;
     const zs_status st = forward_scratch_address(&base);
     if (st != ZS_OK) return st;
-    const Scratch sc = scratch_at(base, windows, C);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (fast) {
-        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
-        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)KW, (int)Wtot, out, sc.part, sc.flags, next_salt());
-    } else {
-        launch(fwd_gen_main, (unsigned)ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)Wtot, out,
-               sc.part, sc.cross);
-        launch(fwd_fixup, (unsigned)Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, kGenWin,
-               (const float*)sc.part, out);
-    }
+    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, out, scratch_at(base, p.windows, C, p.R),
+                   reinterpret_cast<cudaStream_t>(stream));
     return check_launch("zs_forward_noalloc");
 }

@@ -128,8 +128,9 @@ def draw_operands(rng: np.random.Generator, N: int, E: int, C: int, lmax: int = 
     return coup, rad, grad_out
 
 
-def make_workload(name: str, C: int = 32, seed: int | None = None) -> Workload:
-    """Build one of the named configurations (tiny, n1000, n4096, zipf, large)."""
+def make_workload(name: str, C: int = 32, seed: int | None = None, lmax: int = 3) -> Workload:
+    """Build one of the named configurations (tiny, n1000, n4096, zipf, large);
+    lmax picks the ladder of the operands (3: the pages' 3/5/7 rows)."""
     cfg = CONFIGS[name]
     N, E = cfg["N"], cfg["E"]
     rng = np.random.default_rng(cfg["seed"] if seed is None else seed)
@@ -139,7 +140,7 @@ def make_workload(name: str, C: int = 32, seed: int | None = None) -> Workload:
         dst = zipf_dst(rng, src, N)
     else:
         dst = uniform_dst(rng, src, N)
-    coup, rad, grad_out = draw_operands(rng, N, E, C)
+    coup, rad, grad_out = draw_operands(rng, N, E, C, lmax)
     return Workload(name, N, E, C, cfg["seed"] if seed is None else seed, src, dst, coup, rad, grad_out)
 
 

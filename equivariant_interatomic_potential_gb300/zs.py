@@ -57,6 +57,8 @@ def load(build_if_missing: bool = True):
         lib.zs_build_csr.argtypes = [P, I64, I32, P, P, P, P, SZ, P]
         lib.zs_forward_workspace_bytes.restype = SZ
         lib.zs_forward_workspace_bytes.argtypes = [I64, I32, I32]
+        lib.zs_forward_workspace_bytes_lmax.restype = SZ
+        lib.zs_forward_workspace_bytes_lmax.argtypes = [I64, I32, I32, I32]
         lib.zs_forward.restype = ctypes.c_int
         lib.zs_forward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
         lib.zs_backward.restype = ctypes.c_int
@@ -124,8 +126,19 @@ def zs_build_csr_workspace_bytes(E: int, N: int) -> int:
     return int(load().zs_build_csr_workspace_bytes(E, N))
 
 
-def zs_forward_workspace_bytes(E: int, N: int, C: int) -> int:
-    return int(load().zs_forward_workspace_bytes(E, N, C))
+def zs_forward_workspace_bytes(E: int, N: int, C: int, lmax: int = 3) -> int:
+    return int(load().zs_forward_workspace_bytes_lmax(E, N, C, lmax))
+
+
+def ladder(lmax: int) -> tuple[int, int]:
+    """(D, R): node rows (lmax+1)^2 and zonal rows D - 1 of the degree-lmax ladder."""
+    D = (lmax + 1) ** 2
+    return D, D - 1
+
+
+def _lmax(rad: torch.Tensor, lmax: int | None) -> int:
+    """The ladder degree: given, else the radial operand's slot count (E, lmax, C)."""
+    return int(rad.shape[1]) if lmax is None else int(lmax)
 
 
 def zs_build_csr(dst: torch.Tensor, N: int, row_ptr=None, perm=None, bad_dst_count=None,
@@ -149,19 +162,21 @@ def zs_build_csr(dst: torch.Tensor, N: int, row_ptr=None, perm=None, bad_dst_cou
 
 
 def zs_forward(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,
-               out=None, workspace=None, stream=None, lmax: int = 3):
-    """Forward zonal scatter.  Returns out (N, 16, C) fp32."""
+               out=None, workspace=None, stream=None, lmax: int | None = None):
+    """Forward zonal scatter.  Returns out (N, D, C) fp32; lmax defaults to rad.shape[1]."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
     E = coup.shape[0]
     C = rad.shape[2]
     dev = coup.device
-    _need(coup, "coup", torch.float32, (E, 15))
-    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
     _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
     _need(perm, "perm", torch.int32, (E,))
-    out = torch.empty((N, 16, C), dtype=torch.float32, device=dev) if out is None else out
-    _need(out, "out", torch.float32, (N, 16, C))
+    out = torch.empty((N, D, C), dtype=torch.float32, device=dev) if out is None else out
+    _need(out, "out", torch.float32, (N, D, C))
     if workspace is None:
-        workspace = _workspace(zs_forward_workspace_bytes(E, N, C), dev)
+        workspace = _workspace(zs_forward_workspace_bytes(E, N, C, lmax), dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("zs_forward", load().zs_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), E, N, C, lmax,
                                            _ptr(out), _ptr(workspace), wbytes, _stream(stream)))
@@ -169,39 +184,43 @@ def zs_forward(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, per
 
 
 def zs_backward(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, N: int,
-                d_coup=None, d_rad=None, stream=None, lmax: int = 3):
-    """Backward.  Returns (d_coup (E, 15), d_rad (E, 3, C)) fp32."""
+                d_coup=None, d_rad=None, stream=None, lmax: int | None = None):
+    """Backward.  Returns (d_coup (E, R), d_rad (E, lmax, C)) fp32; lmax defaults to rad.shape[1]."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
     E = coup.shape[0]
     C = rad.shape[2]
     dev = coup.device
-    _need(g, "g", torch.float32, (N, 16, C))
-    _need(coup, "coup", torch.float32, (E, 15))
-    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(g, "g", torch.float32, (N, D, C))
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
     _need(dst, "dst", torch.int32, (E,))
-    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev) if d_coup is None else d_coup
-    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
-    _need(d_coup, "d_coup", torch.float32, (E, 15))
-    _need(d_rad, "d_rad", torch.float32, (E, 3, C))
+    d_coup = torch.empty((E, R), dtype=torch.float32, device=dev) if d_coup is None else d_coup
+    d_rad = torch.empty((E, lmax, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_coup, "d_coup", torch.float32, (E, R))
+    _need(d_rad, "d_rad", torch.float32, (E, lmax, C))
     _check("zs_backward", load().zs_backward(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst), E, N, C, lmax,
                                              _ptr(d_coup), _ptr(d_rad), _stream(stream)))
     return d_coup, d_rad
 
 
 def zs_backward_csr(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor,
-                    perm: torch.Tensor, N: int, d_coup=None, d_rad=None, stream=None, lmax: int = 3):
-    """Backward with edges visited in CSR order.  Returns (d_coup (E, 15), d_rad (E, 3, C)) fp32."""
+                    perm: torch.Tensor, N: int, d_coup=None, d_rad=None, stream=None, lmax: int | None = None):
+    """Backward with edges visited in CSR order.  Returns (d_coup (E, R), d_rad (E, lmax, C)) fp32."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
     E = coup.shape[0]
     C = rad.shape[2]
     dev = coup.device
-    _need(g, "g", torch.float32, (N, 16, C))
-    _need(coup, "coup", torch.float32, (E, 15))
-    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(g, "g", torch.float32, (N, D, C))
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
     _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
     _need(perm, "perm", torch.int32, (E,))
-    d_coup = torch.empty((E, 15), dtype=torch.float32, device=dev) if d_coup is None else d_coup
-    d_rad = torch.empty((E, 3, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
-    _need(d_coup, "d_coup", torch.float32, (E, 15))
-    _need(d_rad, "d_rad", torch.float32, (E, 3, C))
+    d_coup = torch.empty((E, R), dtype=torch.float32, device=dev) if d_coup is None else d_coup
+    d_rad = torch.empty((E, lmax, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_coup, "d_coup", torch.float32, (E, R))
+    _need(d_rad, "d_rad", torch.float32, (E, lmax, C))
     _check("zs_backward_csr", load().zs_backward_csr(_ptr(g), _ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm),
                                                      E, N, C, lmax, _ptr(d_coup), _ptr(d_rad), _stream(stream)))
     return d_coup, d_rad
@@ -213,20 +232,22 @@ def zs_check_timeouts() -> None:
 
 
 def zs_forward_noalloc(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,
-                       out: torch.Tensor, stream=None, lmax: int = 3):
+                       out: torch.Tensor, stream=None, lmax: int | None = None):
     """zs_forward with the library's static device scratch instead of a workspace.
 
     For callers that cannot allocate device memory: ``out`` must be given,
     nothing is allocated.  See include/zs.h for the size limit and the rule
     that overlapping calls race.
     """
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
     E = coup.shape[0]
     C = rad.shape[2]
-    _need(coup, "coup", torch.float32, (E, 15))
-    _need(rad, "rad", torch.float32, (E, 3, C))
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
     _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
     _need(perm, "perm", torch.int32, (E,))
-    _need(out, "out", torch.float32, (N, 16, C))
+    _need(out, "out", torch.float32, (N, D, C))
     _check("zs_forward_noalloc", load().zs_forward_noalloc(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm),
                                                            E, N, C, lmax, _ptr(out), _stream(stream)))
     return out

@@ -19,6 +19,12 @@
  *   rad   (E, 3, C)   fp32, row-major, contiguous
  *   out   (N, 16, C)  fp32, row-major, contiguous
  *   g     (N, 16, C)  fp32 cotangent of out (row 0 is never read)
+ * Every entry point with an lmax argument also takes the other ladders
+ * lmax = 1..5 (an extension of the pages' operator, same definitions):
+ * D = (lmax+1)^2, R = D - 1, degree l holding rows [l^2 - 1, (l+1)^2 - 1),
+ * coup (E, R), rad (E, lmax, C), out and g (N, D, C).  lmax = 3 with C = 32
+ * and 16-byte aligned operands takes the tuned kernels; every other shape
+ * takes per-channel kernels.
  *   forward:  out[n,0,c] = 0,
  *             out[n,1+r,c] = sum over CSR positions j of node n, in order,
  *                            of coup[e,r] * rad[e,s(r),c], e = perm[j]
@@ -67,7 +73,7 @@ typedef struct CUstream_st* zs_stream_t;
 typedef enum zs_status {
     ZS_OK = 0,
     ZS_ERR_INVALID_ARG = 1,  /* null pointer with nonzero size, negative size, E >= 2^31, C < 1, workspace too small */
-    ZS_ERR_UNSUPPORTED = 2,  /* lmax != 3 */
+    ZS_ERR_UNSUPPORTED = 2,  /* lmax outside 1..5 */
     ZS_ERR_CUDA = 3,         /* a CUDA call or launch failed; zs_last_error() has the message */
     ZS_ERR_TIMEOUT = 4       /* a bounded device wait ran out (see zs_check_timeouts) */
 } zs_status;
@@ -104,11 +110,18 @@ ZS_API zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
                        void* workspace, size_t workspace_bytes, zs_stream_t stream);
 
 /*
- * Bytes of device workspace zs_forward needs (partial sums of nodes whose
- * edges are split across work units, and flags that mark them written).
- * 256-byte alignment required; its contents need not start at zero.
+ * Bytes of device workspace zs_forward needs at lmax = 3 (partial sums of
+ * nodes whose edges are split across work units, and flags that mark them
+ * written).  256-byte alignment required; its contents need not start at
+ * zero.
  */
 ZS_API size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C);
+
+/*
+ * The same for any ladder lmax = 1..5 (0 for an lmax outside that range);
+ * equal to zs_forward_workspace_bytes at lmax = 3.
+ */
+ZS_API size_t zs_forward_workspace_bytes_lmax(int64_t E, int32_t N, int32_t C, int32_t lmax);
 
 /*
  * Forward zonal scatter (pull request "fused Triton zonal scatter for the
@@ -117,7 +130,8 @@ ZS_API size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C);
  *   row_ptr (N+1,), perm (E,) a CSR as produced by zs_build_csr; positions
  *                             row_ptr[N]..E-1 are ignored
  *   E                         length of perm and number of rows of coup/rad
- *   lmax                      must be 3 (else ZS_ERR_UNSUPPORTED)
+ *   lmax                      1..5 (else ZS_ERR_UNSUPPORTED); the workspace is
+ *                             zs_forward_workspace_bytes_lmax(E, N, C, lmax)
  *   out (N,16,C)              output, fully written: row 0 and the rows of
  *                             nodes without edges are exact zeros
  * Each node's sum is formed in fp32 in a fixed order: CSR order within

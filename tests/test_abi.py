@@ -20,7 +20,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = zs.declared_functions()
     for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_backward_csr", "zs_build_csr_workspace_bytes",
-               "zs_forward_workspace_bytes", "zs_status_string", "zs_last_error", "zs_version",
+               "zs_forward_workspace_bytes", "zs_forward_workspace_bytes_lmax", "zs_status_string", "zs_last_error", "zs_version",
                "zs_check_timeouts", "zs_selftest_bounded_wait", "zs_forward_noalloc"):
         assert fn in names
 
@@ -56,8 +56,12 @@ FAKE = 1 << 20   # a non-null, 256-byte aligned address never dereferenced by th
 
 def test_forward_argument_checks(lib):
     ws = lib.zs_forward_workspace_bytes(100, 10, 32)
-    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 2, FAKE, FAKE, ws, None) == UNSUPPORTED
-    assert b"lmax" in lib.zs_last_error()
+    for lmax in (0, 6, -3):   # ladders lmax 1..5 only
+        assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, lmax, FAKE, FAKE, 1 << 40, None) == UNSUPPORTED
+        assert b"lmax" in lib.zs_last_error()
+    # another ladder needs its own, larger workspace
+    assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 5, FAKE, FAKE, ws, None) == INVALID
+    assert b"workspace" in lib.zs_last_error()
     assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, -1, 10, 32, 3, FAKE, FAKE, ws, None) == INVALID
     assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, -1, 32, 3, FAKE, FAKE, ws, None) == INVALID
     assert lib.zs_forward(FAKE, FAKE, FAKE, FAKE, 100, 10, 0, 3, FAKE, FAKE, ws, None) == INVALID
@@ -73,7 +77,8 @@ def test_forward_argument_checks(lib):
 
 
 def test_backward_argument_checks(lib):
-    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 4, FAKE, FAKE, None) == UNSUPPORTED
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 6, FAKE, FAKE, None) == UNSUPPORTED
+    assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 0, FAKE, FAKE, None) == UNSUPPORTED
     assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, -5, 10, 32, 3, FAKE, FAKE, None) == INVALID
     assert lib.zs_backward(FAKE, FAKE, FAKE, FAKE, 100, 10, -3, 3, FAKE, FAKE, None) == INVALID
     assert lib.zs_backward(FAKE, FAKE, FAKE, None, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
@@ -84,7 +89,7 @@ def test_backward_argument_checks(lib):
 
 
 def test_backward_csr_argument_checks(lib):
-    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 1, FAKE, FAKE, None) == UNSUPPORTED
+    assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 10, 32, 6, FAKE, FAKE, None) == UNSUPPORTED
     assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 10, 32, 3, FAKE, FAKE, None) == INVALID
     assert lib.zs_backward_csr(FAKE, FAKE, FAKE, None, FAKE, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
     assert lib.zs_backward_csr(FAKE, FAKE, FAKE, FAKE, None, 100, 10, 32, 3, FAKE, FAKE, None) == INVALID
@@ -138,6 +143,18 @@ def test_workspace_sizes(lib):
     assert lib.zs_forward_workspace_bytes(E, 4096, 32) == ws(E, 32)
     assert lib.zs_forward_workspace_bytes(0, 4096, 32) == ws(0, 32)
     assert lib.zs_forward_workspace_bytes(1000, 10, 40) == ws(1000, 40)
+    # other ladders: per window of 256 positions (plus one), a pair of R x C
+    # partials (R = (lmax+1)^2 - 1), one crossing-node entry and one flag
+    def ws_l(E, C, lmax):
+        w = -(-max(E, 1) // 256) + 1
+        R = (lmax + 1) ** 2 - 1
+        return -(-(w * 2 * R * C * 4) // 256) * 256 + -(-(w * 4) // 256) * 256 + -(-(w * 8) // 256) * 256
+    for lmax in (1, 2, 4, 5):
+        for e, c in ((E, 32), (0, 7), (1000, 40)):
+            assert lib.zs_forward_workspace_bytes_lmax(e, 4096, c, lmax) == ws_l(e, c, lmax)
+    assert lib.zs_forward_workspace_bytes_lmax(E, 4096, 32, 3) == ws(E, 32)
+    assert lib.zs_forward_workspace_bytes_lmax(E, 4096, 32, 0) == 0
+    assert lib.zs_forward_workspace_bytes_lmax(E, 4096, 32, 6) == 0
     assert lib.zs_forward_workspace_bytes(10, 4096, 0) == 0
 
 
