@@ -56,7 +56,8 @@ __device__ __forceinline__ float warp_reduce_scatter32(float v[32], int lane) {
 template <int L>
 __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const float* __restrict__ coup,
                                              const float* __restrict__ rad, int64_t e, int d, int C, int lane,
-                                             float* __restrict__ d_coup, float* __restrict__ d_rad) {
+                                             float* __restrict__ d_coup, float* __restrict__ d_rad,
+                                             const float* __restrict__ scale = nullptr) {
     constexpr int R = Ladder<L>::R, S = Ladder<L>::S, D = Ladder<L>::D;
     constexpr int RP = (R + 31) / 32 * 32;   // rows padded to whole warps for the reduction
     const bool ok = d >= 0;
@@ -69,6 +70,7 @@ __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const 
     const float* rp = rad + e * S * C;
     float* drp = d_rad + e * S * C;
     const float* gn = g + (int64_t)(ok ? d : 0) * D * C;
+    const float sc = (ok && scale) ? __ldg(scale + d) : 1.f;   // the destination's scale (1: plain operator)
     for (int c = lane; c < C; c += 32) {
         if (!ok) {
 #pragma unroll
@@ -88,12 +90,12 @@ __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const 
             sv[ladder_slot(r)] = fmaf(gv, cv[r], sv[ladder_slot(r)]);
         }
 #pragma unroll
-        for (int k = 0; k < S; ++k) drp[k * C + c] = sv[k];
+        for (int k = 0; k < S; ++k) drp[k * C + c] = scale ? sv[k] * sc : sv[k];
     }
 #pragma unroll
     for (int r0 = 0; r0 < RP; r0 += 32) {
         const float v = warp_reduce_scatter32(pc + r0, lane);
-        if (r0 + lane < R) d_coup[e * R + r0 + lane] = ok ? v : 0.f;
+        if (r0 + lane < R) d_coup[e * R + r0 + lane] = ok ? (scale ? v * sc : v) : 0.f;
     }
 }
 
@@ -101,13 +103,13 @@ template <int L>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
         const int32_t* __restrict__ dst, int64_t E, int32_t N, int C,
-        float* __restrict__ d_coup, float* __restrict__ d_rad) {
+        float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
     for (int64_t e = (int64_t)blockIdx.x * kBwdWarps + warp; e < E; e += (int64_t)gridDim.x * kBwdWarps) {
         const int d = __ldg(dst + e);
-        bwd_gen_edge<L>(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad);
+        bwd_gen_edge<L>(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad, scale);
     }
 }
 
@@ -402,7 +404,7 @@ template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
                  const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
-                 float* __restrict__ d_coup, float* __restrict__ d_rad) {
+                 float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const QuadLane Q(threadIdx.x & 31);
@@ -460,6 +462,14 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 float* dc = d_coup + e * 15 + row;
                 float* dr = d_rad + e * (3 * kC32) + 4 * Q.q;
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (scale && ok) {   // gradients of the scaled output: the destination's scale times these
+                    const float sc = __ldg(scale + m);
+                    s0 = make_float4(s0.x * sc, s0.y * sc, s0.z * sc, s0.w * sc);
+                    s1 = make_float4(s1.x * sc, s1.y * sc, s1.z * sc, s1.w * sc);
+                    s2 = make_float4(s2.x * sc, s2.y * sc, s2.z * sc, s2.w * sc);
+                    t0 *= sc;
+                    t1 *= sc;
+                }
                 st_hint4(dr, ok ? s0 : z, pol_out);
                 st_hint4(dr + kC32, ok ? s1 : z, pol_out);
                 st_hint4(dr + 2 * kC32, ok ? s2 : z, pol_out);
@@ -507,7 +517,7 @@ constexpr int kEdgeWarpsLarge = 8;    // 3-stage rings of 4 edges: 8 warps
 
 template <int W, int S, int T>
 void launch_edge_tma(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
-                     float* d_coup, float* d_rad, cudaStream_t s) {
+                     float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
     const int64_t warps_max = (int64_t)num_sms() * W;
     const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
     const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
@@ -516,7 +526,7 @@ void launch_edge_tma(const float* g, const float* coup, const float* rad, const 
     static std::atomic<bool> attr_done[kMaxDevices];
     set_smem_limit_once(bwd_edge_c32_tma<W, S, T>, smem, attr_done);
     launch(bwd_edge_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
-           (int)Wtot, d_coup, d_rad);
+           (int)Wtot, d_coup, d_rad, scale);
 }
 
 // One warp waits on an mbarrier that nothing arrives on, with a limit of
@@ -540,12 +550,32 @@ zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s) {
     return check_launch("zs_selftest_bounded_wait");
 }
 
+// Gradient of the node scale of the scaled forward: d_scale[n] = sum over
+// rows 1..D-1 and channels of g[n,r,c] * out_raw[n,r,c], one warp per node,
+// lane-strided products added in a fixed order.
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32_t N, int64_t node_floats, int C,
+               float* __restrict__ d_scale) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * kBwdWarps + warp;
+    pdl_wait();
+    pdl_trigger();
+    if (n >= N) return;
+    const float* gp = g + n * node_floats;
+    const float* rp = raw + n * node_floats;
+    float acc = 0.f;
+    for (int64_t i = C + lane; i < node_floats; i += 32) acc = fmaf(__ldg(gp + i), __ldg(rp + i), acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    if (lane == 0) d_scale[n] = acc;
+}
+
 template <int L>
 void launch_gen_edges(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
-                      int C, float* d_coup, float* d_rad, cudaStream_t s) {
+                      int C, float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
     const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
     const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
-    launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad);
+    launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad, scale);
 }
 
 template <int L>
@@ -562,17 +592,16 @@ void launch_gen_csr(const float* g, const float* coup, const float* rad, const i
 
 using namespace zs;
 
-extern "C" zs_status zs_backward(const float* g, const float* coup, const float* rad,
-                                 const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
-                                 float* d_coup, float* d_rad, zs_stream_t stream) {
+static zs_status backward_impl(const char* name, const float* g, const float* coup, const float* rad,
+                               const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
+                               float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
     if (lmax < 1 || lmax > kMaxLmax)
-        return fail(ZS_ERR_UNSUPPORTED, "zs_backward: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
-    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
-    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_backward: E=%lld exceeds the int32 index range", (long long)E);
+        return fail(ZS_ERR_UNSUPPORTED, "%s: lmax=%d, supported ladders are lmax 1..%d", name, lmax, kMaxLmax);
+    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "%s: bad sizes E=%lld N=%d C=%d", name, (long long)E, N, C);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "%s: E=%lld exceeds the int32 index range", name, (long long)E);
     if (E == 0) return ZS_OK;
-    if (!coup || !rad || !dst || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward: NULL array with E > 0");
-    if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward: g is NULL with N > 0");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!coup || !rad || !dst || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "%s: NULL array with E > 0", name);
+    if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "%s: g is NULL with N > 0", name);
     const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
         // While the cotangent block is small enough to stay in L2 next to the
@@ -580,18 +609,47 @@ extern "C" zs_status zs_backward(const float* g, const float* coup, const float*
         // latency best; a larger block misses L2 more often and wants more
         // tiles in flight per warp.
         const bool small_g = (int64_t)N * 16 * kC32 * 4 <= kSmallCotangentBytes;
-        if (small_g) launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
-        else launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, s);
+        if (small_g) launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, scale, s);
+        else launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, scale, s);
     } else {
         switch (lmax) {
-            case 1: launch_gen_edges<1>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
-            case 2: launch_gen_edges<2>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
-            case 3: launch_gen_edges<3>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
-            case 4: launch_gen_edges<4>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
-            default: launch_gen_edges<5>(g, coup, rad, dst, E, N, C, d_coup, d_rad, s); break;
+            case 1: launch_gen_edges<1>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
+            case 2: launch_gen_edges<2>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
+            case 3: launch_gen_edges<3>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
+            case 4: launch_gen_edges<4>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
+            default: launch_gen_edges<5>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
         }
     }
-    return check_launch("zs_backward");
+    return check_launch(name);
+}
+
+extern "C" zs_status zs_backward(const float* g, const float* coup, const float* rad,
+                                 const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                 float* d_coup, float* d_rad, zs_stream_t stream) {
+    return backward_impl("zs_backward", g, coup, rad, dst, E, N, C, lmax, d_coup, d_rad, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" zs_status zs_backward_scaled(const float* g, const float* coup, const float* rad, const int32_t* dst,
+                                        const float* node_scale, const float* out_raw,
+                                        int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                        float* d_coup, float* d_rad, float* d_scale, zs_stream_t stream) {
+    if (N > 0 && !node_scale) return fail(ZS_ERR_INVALID_ARG, "zs_backward_scaled: node_scale is NULL");
+    if (N > 0 && d_scale && (!out_raw || !g))
+        return fail(ZS_ERR_INVALID_ARG, "zs_backward_scaled: d_scale needs out_raw and g");
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "zs_backward_scaled: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
+    if (E < 0 || N < 0 || C < 1)
+        return fail(ZS_ERR_INVALID_ARG, "zs_backward_scaled: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N > 0 && d_scale) {
+        const int64_t node_floats = (int64_t)(lmax + 1) * (lmax + 1) * C;
+        launch(bwd_scale_grad, (unsigned)((N + kBwdWarps - 1) / kBwdWarps), kBwdThreads, 0, s, g, out_raw, N,
+               node_floats, (int)C, d_scale);
+        const zs_status st = check_launch("zs_backward_scaled");
+        if (st != ZS_OK) return st;
+    }
+    return backward_impl("zs_backward_scaled", g, coup, rad, dst, E, N, C, lmax, d_coup, d_rad, node_scale, s);
 }
 
 extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const float* rad,

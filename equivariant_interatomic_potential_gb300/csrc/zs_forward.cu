@@ -99,6 +99,35 @@ __device__ __forceinline__ void zero_node32(float* __restrict__ node, int lane) 
         *reinterpret_cast<float4*>(node + 4 * (lane + 32 * k)) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Where a finished node goes.  out gets scale[n] times the node's sum (the
+// sum itself when scale is null: the plain operator), raw the unscaled sum
+// when it is not null.  Nodes without edges are zero in both, whatever
+// their scale, and the scalar row is always zero.
+struct NodeOut {
+    float* out;
+    float* raw;
+    const float* scale;
+};
+
+__device__ __forceinline__ void put_node32(const NodeOut& o, int n, const float4 acc[4], const Lane32& L) {
+    const int64_t at = (int64_t)n * kNodeFloats32;
+    if (o.raw) store_node32(o.raw + at, acc, L);
+    if (o.scale) {
+        const float sc = __ldg(o.scale + n);
+        float4 t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc);
+        store_node32(o.out + at, t, L);
+    } else {
+        store_node32(o.out + at, acc, L);
+    }
+}
+
+__device__ __forceinline__ void zero_put32(const NodeOut& o, int n, int lane) {
+    zero_node32(o.out + (int64_t)n * kNodeFloats32, lane);
+    if (o.raw) zero_node32(o.raw + (int64_t)n * kNodeFloats32, lane);
+}
+
 // Add the message of the edge at tile slot j of stage st.  Rows of
 // positions without an edge are zero in the ring, so there is no branch.
 struct TileView {
@@ -170,7 +199,7 @@ template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-            int E, int32_t N, int KW, int Wtot, float* __restrict__ out, float* __restrict__ cta_part,
+            int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
             uint64_t* __restrict__ flags, uint64_t salt) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
@@ -211,7 +240,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
         };
         auto advance = [&]() {
             while (n < N && a == b && (a < p1 || is_last)) {
-                zero_node32(out + (int64_t)n * kNodeFloats32, L.lane);
+                zero_put32(o, n, L.lane);
                 step();
             }
         };
@@ -238,7 +267,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
                 j = stop;
                 if (tb + j == b) {                   // node n ends inside this window
                     if (a >= p0) {
-                        store_node32(out + (int64_t)n * kNodeFloats32, acc, L);
+                        put_node32(o, n, acc, L);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
@@ -295,7 +324,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
         }
         const int ma = __ldg(row_ptr + m), mb = __ldg(row_ptr + m + 1);
         if (ma >= P0 && mb <= P1) {
-            store_node32(out + (int64_t)m * kNodeFloats32, sum, L);
+            put_node32(o, m, sum, L);
         } else if (ma < P0 && mb <= P1) {
             pend_node = m;
 #pragma unroll
@@ -327,7 +356,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) total[i] = f4_add(total[i], pend[i]);
-    store_node32(out + (int64_t)pend_node * kNodeFloats32, total, L);
+    put_node32(o, pend_node, total, L);
 }
 
 // --------------------------------------------------------------------------
@@ -380,7 +409,7 @@ template <int L>
 __global__ void __launch_bounds__(kFwdThreads)
 fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
              const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-             int64_t E, int32_t N, int C, int Wtot, float* __restrict__ out, float* __restrict__ part,
+             int64_t E, int32_t N, int C, int Wtot, NodeOut o, float* __restrict__ part,
              int32_t* __restrict__ cross) {
     constexpr int R = Ladder<L>::R, D = Ladder<L>::D;
     __shared__ float cs[kFwdWarps][32][R + 1];
@@ -397,15 +426,22 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
     for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
         const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
         if (a >= p1 && !(is_last && a == b)) break;
-        float* node = out + (int64_t)n * D * C;
+        float* node = o.out + (int64_t)n * D * C;
+        float* rnode = o.raw ? o.raw + (int64_t)n * D * C : nullptr;
         if (a == b) {
             for (int64_t i = lane; i < (int64_t)D * C; i += 32) node[i] = 0.f;
+            if (rnode)
+                for (int64_t i = lane; i < (int64_t)D * C; i += 32) rnode[i] = 0.f;
             continue;
         }
         const bool full = a >= p0 && b <= p1;
         float* dstp = full ? node + C : part + ((int64_t)gw * 2 + (a < p0 ? 0 : 1)) * V;
-        if (full)
+        const float sc = (full && o.scale) ? __ldg(o.scale + n) : 1.f;
+        if (full) {
             for (int c = lane; c < C; c += 32) node[c] = 0.f;
+            if (rnode)
+                for (int c = lane; c < C; c += 32) rnode[c] = 0.f;
+        }
         for (int c0 = 0; c0 < C; c0 += 32) {
             const int c = c0 + lane;
             float acc[R];
@@ -414,8 +450,17 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
             accumulate_gen<L>(coup, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
                               cs[warp], lane, acc);
             if (c < C) {
+                if (full && rnode) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) dstp[(int64_t)r * C + c] = acc[r];
+                    for (int r = 0; r < R; ++r) rnode[C + (int64_t)r * C + c] = acc[r];
+                }
+                if (full && o.scale) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) dstp[(int64_t)r * C + c] = acc[r] * sc;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) dstp[(int64_t)r * C + c] = acc[r];
+                }
             }
         }
         if (!full && a >= p0) crossing = n;
@@ -438,7 +483,7 @@ constexpr int kFixVals = 256;   // values per chunk: 8 per lane
 
 __global__ void __launch_bounds__(kFwdThreads)
 fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross, int C, int R, int win,
-          const float* __restrict__ part, float* __restrict__ out) {
+          const float* __restrict__ part, NodeOut o) {
     __shared__ float red[kFwdWarps][kFixVals];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t V = (int64_t)R * C;
@@ -449,8 +494,13 @@ fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross
     if (n < 0) return;
     const int b = __ldg(row_ptr + n + 1);
     const int np = (b - 1) / win - wa + 1;
-    float* node = out + (int64_t)n * (R + 1) * C;
-    for (int c = threadIdx.x; c < C; c += kFwdThreads) node[c] = 0.f;
+    float* node = o.out + (int64_t)n * (R + 1) * C;
+    float* rnode = o.raw ? o.raw + (int64_t)n * (R + 1) * C : nullptr;
+    const float sc = o.scale ? __ldg(o.scale + n) : 1.f;
+    for (int c = threadIdx.x; c < C; c += kFwdThreads) {
+        node[c] = 0.f;
+        if (rnode) rnode[c] = 0.f;
+    }
     for (int64_t v0 = 0; v0 < V; v0 += kFixVals) {
         float sacc[kFixVals / 32];
 #pragma unroll
@@ -473,7 +523,8 @@ fwd_fixup(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cross
                 float t = red[0][vl];
 #pragma unroll
                 for (int w = 1; w < kFwdWarps; ++w) t += red[w][vl];
-                node[C + v] = t;
+                if (rnode) rnode[C + v] = t;
+                node[C + v] = o.scale ? t * sc : t;
             }
         }
         __syncthreads();
@@ -531,10 +582,11 @@ struct FwdPlan {
     int64_t KW, Wtot, ctas, windows;
 };
 
-static FwdPlan fwd_plan(const float* coup, const float* rad, const float* out, int64_t E, int C, int lmax) {
+static FwdPlan fwd_plan(const float* coup, const float* rad, const NodeOut& o, int64_t E, int C, int lmax) {
     FwdPlan p{};
     p.R = ladder_rows(lmax);
-    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(out) && aligned16(coup);
+    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(o.out) && aligned16(coup) &&
+             (o.raw == nullptr || aligned16(o.raw));
     if (p.fast) {
         // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
         // the same number of CSR positions (at least one tile).
@@ -553,31 +605,31 @@ static FwdPlan fwd_plan(const float* coup, const float* rad, const float* out, i
 
 template <int L>
 static void launch_gen(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
-                       const int32_t* perm, int64_t E, int32_t N, int C, float* out, const Scratch& sc,
+                       const int32_t* perm, int64_t E, int32_t N, int C, const NodeOut& o, const Scratch& sc,
                        cudaStream_t s) {
     launch(fwd_gen_main<L>, (unsigned)p.ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)p.Wtot,
-           out, sc.part, sc.cross);
+           o, sc.part, sc.cross);
     launch(fwd_fixup, (unsigned)p.Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, Ladder<L>::R,
-           kGenWin, (const float*)sc.part, out);
+           kGenWin, (const float*)sc.part, o);
 }
 
 static void launch_forward(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
-                           const int32_t* perm, int64_t E, int32_t N, int C, int lmax, float* out,
+                           const int32_t* perm, int64_t E, int32_t N, int C, int lmax, const NodeOut& o,
                            const Scratch& sc, cudaStream_t s) {
     if (p.fast) {
         const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
         static std::atomic<bool> attr_done[kMaxDevices];
         set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)p.ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, out, sc.part, sc.flags, next_salt());
+               coup, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, o, sc.part, sc.flags, next_salt());
         return;
     }
     switch (lmax) {
-        case 1: launch_gen<1>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
-        case 2: launch_gen<2>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
-        case 3: launch_gen<3>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
-        case 4: launch_gen<4>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
-        default: launch_gen<5>(p, coup, rad, row_ptr, perm, E, N, C, out, sc, s); break;
+        case 1: launch_gen<1>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 2: launch_gen<2>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 3: launch_gen<3>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 4: launch_gen<4>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        default: launch_gen<5>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
     }
 }
 
@@ -596,27 +648,44 @@ extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
     return zs_forward_workspace_bytes_lmax(E, N, C, 3);
 }
 
+static zs_status forward_impl(const char* name, const float* coup, const float* rad, const int32_t* row_ptr,
+                              const int32_t* perm, int64_t E, int32_t N, int32_t C, int32_t lmax, const NodeOut& o,
+                              void* workspace, size_t workspace_bytes, zs_stream_t stream) {
+    if (lmax < 1 || lmax > kMaxLmax)
+        return fail(ZS_ERR_UNSUPPORTED, "%s: lmax=%d, supported ladders are lmax 1..%d", name, lmax, kMaxLmax);
+    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "%s: bad sizes E=%lld N=%d C=%d", name, (long long)E, N, C);
+    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "%s: E=%lld exceeds the int32 index range", name, (long long)E);
+    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "%s: row_ptr is NULL", name);
+    if (N > 0 && !o.out) return fail(ZS_ERR_INVALID_ARG, "%s: out is NULL", name);
+    if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "%s: coup, rad or perm is NULL with E > 0", name);
+    const size_t need = zs_forward_workspace_bytes_lmax(E, N, C, lmax);
+    if (workspace_bytes < need) return fail(ZS_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(ZS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
+    if (N == 0) return ZS_OK;
+    const FwdPlan p = fwd_plan(coup, rad, o, E, C, lmax);
+    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(workspace, p.windows, C, p.R),
+                   reinterpret_cast<cudaStream_t>(stream));
+    return check_launch(name);
+}
+
 extern "C" zs_status zs_forward(const float* coup, const float* rad,
                                 const int32_t* row_ptr, const int32_t* perm,
                                 int64_t E, int32_t N, int32_t C, int32_t lmax,
                                 float* out, void* workspace, size_t workspace_bytes,
                                 zs_stream_t stream) {
-    if (lmax < 1 || lmax > kMaxLmax)
-        return fail(ZS_ERR_UNSUPPORTED, "zs_forward: lmax=%d, supported ladders are lmax 1..%d", lmax, kMaxLmax);
-    if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: bad sizes E=%lld N=%d C=%d", (long long)E, N, C);
-    if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "zs_forward: E=%lld exceeds the int32 index range", (long long)E);
-    if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "zs_forward: row_ptr is NULL");
-    if (N > 0 && !out) return fail(ZS_ERR_INVALID_ARG, "zs_forward: out is NULL");
-    if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward: coup, rad or perm is NULL with E > 0");
-    const size_t need = zs_forward_workspace_bytes_lmax(E, N, C, lmax);
-    if (workspace_bytes < need) return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace of %zu bytes, %zu needed", workspace_bytes, need);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return fail(ZS_ERR_INVALID_ARG, "zs_forward: workspace NULL or not 256-byte aligned");
-    if (N == 0) return ZS_OK;
-    const FwdPlan p = fwd_plan(coup, rad, out, E, C, lmax);
-    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, out, scratch_at(workspace, p.windows, C, p.R),
-                   reinterpret_cast<cudaStream_t>(stream));
-    return check_launch("zs_forward");
+    return forward_impl("zs_forward", coup, rad, row_ptr, perm, E, N, C, lmax, NodeOut{out, nullptr, nullptr},
+                        workspace, workspace_bytes, stream);
+}
+
+extern "C" zs_status zs_forward_scaled(const float* coup, const float* rad,
+                                       const int32_t* row_ptr, const int32_t* perm, const float* node_scale,
+                                       int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                       float* out, float* out_raw, void* workspace, size_t workspace_bytes,
+                                       zs_stream_t stream) {
+    if (N > 0 && !node_scale) return fail(ZS_ERR_INVALID_ARG, "zs_forward_scaled: node_scale is NULL");
+    return forward_impl("zs_forward_scaled", coup, rad, row_ptr, perm, E, N, C, lmax,
+                        NodeOut{out, out_raw, node_scale}, workspace, workspace_bytes, stream);
 }
 
 // --------------------------------------------------------------------------
@@ -670,7 +739,8 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     if (E > 0 && (!coup || !rad || !perm)) return fail(ZS_ERR_INVALID_ARG, "zs_forward_noalloc: coup, rad or perm is NULL with E > 0");
     if (N == 0) return ZS_OK;
     // the same split as zs_forward; the scratch holds one pair of partials per window
-    const FwdPlan p = fwd_plan(coup, rad, out, E, C, lmax);
+    const NodeOut o{out, nullptr, nullptr};
+    const FwdPlan p = fwd_plan(coup, rad, o, E, C, lmax);
     const size_t need = scratch_bytes(p.windows, C, p.R);
     if (need > kNoAllocScratchBytes)
         return fail(ZS_ERR_INVALID_ARG,
@@ -679,7 +749,7 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     float* base = nullptr;
     const zs_status st = forward_scratch_address(&base);
     if (st != ZS_OK) return st;
-    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, out, scratch_at(base, p.windows, C, p.R),
+    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(base, p.windows, C, p.R),
                    reinterpret_cast<cudaStream_t>(stream));
     return check_launch("zs_forward_noalloc");
 }

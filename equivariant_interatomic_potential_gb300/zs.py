@@ -63,6 +63,10 @@ def load(build_if_missing: bool = True):
         lib.zs_forward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
         lib.zs_backward.restype = ctypes.c_int
         lib.zs_backward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P]
+        lib.zs_forward_scaled.restype = ctypes.c_int
+        lib.zs_forward_scaled.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P, SZ, P]
+        lib.zs_backward_scaled.restype = ctypes.c_int
+        lib.zs_backward_scaled.argtypes = [P, P, P, P, P, P, I64, I32, I32, I32, P, P, P, P]
         lib.zs_backward_csr.restype = ctypes.c_int
         lib.zs_backward_csr.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P]
         lib.zs_forward_noalloc.restype = ctypes.c_int
@@ -181,6 +185,68 @@ def zs_forward(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, per
     _check("zs_forward", load().zs_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), E, N, C, lmax,
                                            _ptr(out), _ptr(workspace), wbytes, _stream(stream)))
     return out
+
+
+def zs_forward_scaled(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor,
+                      node_scale: torch.Tensor, N: int, out=None, out_raw=None, want_raw: bool = True,
+                      workspace=None, stream=None, lmax: int | None = None):
+    """Forward with the per-node factor fused in.  Returns (out, out_raw); out_raw is
+    None when want_raw is False and none is given."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    _need(node_scale, "node_scale", torch.float32, (N,))
+    out = torch.empty((N, D, C), dtype=torch.float32, device=dev) if out is None else out
+    _need(out, "out", torch.float32, (N, D, C))
+    if out_raw is None and want_raw:
+        out_raw = torch.empty((N, D, C), dtype=torch.float32, device=dev)
+    if out_raw is not None:
+        _need(out_raw, "out_raw", torch.float32, (N, D, C))
+    if workspace is None:
+        workspace = _workspace(zs_forward_workspace_bytes(E, N, C, lmax), dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("zs_forward_scaled", load().zs_forward_scaled(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm),
+                                                         _ptr(node_scale), E, N, C, lmax, _ptr(out), _ptr(out_raw),
+                                                         _ptr(workspace), wbytes, _stream(stream)))
+    return out, out_raw
+
+
+def zs_backward_scaled(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor,
+                       node_scale: torch.Tensor, N: int, out_raw=None, d_coup=None, d_rad=None, d_scale=None,
+                       want_scale_grad: bool = True, stream=None, lmax: int | None = None):
+    """Backward of zs_forward_scaled.  Returns (d_coup, d_rad, d_scale); d_scale is
+    None unless out_raw is given (and want_scale_grad)."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(g, "g", torch.float32, (N, D, C))
+    _need(coup, "coup", torch.float32, (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
+    _need(dst, "dst", torch.int32, (E,))
+    _need(node_scale, "node_scale", torch.float32, (N,))
+    d_coup = torch.empty((E, R), dtype=torch.float32, device=dev) if d_coup is None else d_coup
+    d_rad = torch.empty((E, lmax, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_coup, "d_coup", torch.float32, (E, R))
+    _need(d_rad, "d_rad", torch.float32, (E, lmax, C))
+    if out_raw is not None:
+        _need(out_raw, "out_raw", torch.float32, (N, D, C))
+        if d_scale is None and want_scale_grad:
+            d_scale = torch.empty(N, dtype=torch.float32, device=dev)
+    if d_scale is not None:
+        _need(d_scale, "d_scale", torch.float32, (N,))
+    _check("zs_backward_scaled", load().zs_backward_scaled(_ptr(g), _ptr(coup), _ptr(rad), _ptr(dst),
+                                                           _ptr(node_scale), _ptr(out_raw), E, N, C, lmax,
+                                                           _ptr(d_coup), _ptr(d_rad), _ptr(d_scale),
+                                                           _stream(stream)))
+    return d_coup, d_rad, d_scale
 
 
 def zs_backward(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, N: int,

@@ -144,6 +144,46 @@ ZS_API zs_status zs_forward(const float* coup, const float* rad,
                      zs_stream_t stream);
 
 /*
+ * Forward with the degree normalisation fused in.  The pages apply an
+ * inverse-square-root degree normalisation to the operator's output in the
+ * traced graph, so that its own cotangent keeps flowing (pull request
+ * "fused Triton zonal scatter for the GIE head", section "What", third
+ * bullet, and its sequence diagram); here the per-node factor is applied
+ * as the node is written, saving a pass over the (N, D, C) output.
+ *   node_scale (N,)   per-node factor s[n] (for instance 1/sqrt of a
+ *                     degree); any finite or non-finite value
+ *   out (N, D, C)     out[n,1+r,c] = s[n] * (the zs_forward value), row 0
+ *                     zero; nodes without edges are zero whatever s[n]
+ *   out_raw (N, D, C) may be NULL; else also receives the unscaled
+ *                     zs_forward result (what zs_backward_scaled needs for
+ *                     the scale's gradient)
+ * Other arguments, workspace, errors and summation order as zs_forward;
+ * out equals zs_forward's result times s[n] rounded once (bitwise).
+ */
+ZS_API zs_status zs_forward_scaled(const float* coup, const float* rad,
+                                   const int32_t* row_ptr, const int32_t* perm, const float* node_scale,
+                                   int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                   float* out, float* out_raw, void* workspace, size_t workspace_bytes,
+                                   zs_stream_t stream);
+
+/*
+ * Backward of zs_forward_scaled, edge order: for the cotangent g of the
+ * scaled out,
+ *   d_coup[e,r]  = s[dst[e]] * (zs_backward's d_coup with the same g)
+ *   d_rad[e,l,c] = s[dst[e]] * (zs_backward's d_rad)
+ *   d_scale[n]   = sum over rows 1..D-1 and channels of g[n,r,c] * out_raw[n,r,c]
+ * node_scale (N,) as given to the forward; out_raw (N, D, C) the forward's
+ * unscaled result, needed only when d_scale is not NULL; d_scale (N,) may
+ * be NULL.  Each product of a gradient and s is rounded once.  Errors as
+ * zs_backward, plus ZS_ERR_INVALID_ARG for a NULL node_scale, or a d_scale
+ * without out_raw.  Needs no workspace.
+ */
+ZS_API zs_status zs_backward_scaled(const float* g, const float* coup, const float* rad, const int32_t* dst,
+                                    const float* node_scale, const float* out_raw,
+                                    int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                    float* d_coup, float* d_rad, float* d_scale, zs_stream_t stream);
+
+/*
  * Backward of the zonal scatter (pull request "fused Triton zonal scatter
  * for the GIE head", section "What", backward bullet): one edge-parallel
  * pass writing both operand gradients.

@@ -137,6 +137,44 @@ def backward(g, coup, rad, dst, N: int, edges=None):
     return d_coup, d_rad, a_dc, a_dr
 
 
+def forward_scaled(coup, rad, row_ptr, perm, N: int, scale):
+    """The forward with a per-node factor applied to each node's sum (the degree
+    normalisation the pages apply after the operator): (out, absum, out_raw,
+    absum_raw), fp64.  Nodes without edges are zero whatever their factor."""
+    out_raw, absum_raw = forward(coup, rad, row_ptr, perm, N)
+    s = np.asarray(scale, np.float64).reshape(-1)
+    rp = np.asarray(row_ptr, np.int64)
+    has = (rp[1:] > rp[:-1])[:, None, None]
+    with np.errstate(invalid="ignore", over="ignore"):
+        out = np.where(has, s[:, None, None] * out_raw, 0.0)
+        absum = np.where(has, np.abs(s)[:, None, None] * absum_raw, 0.0)
+    return out, absum, out_raw, absum_raw
+
+
+def backward_scaled(g, coup, rad, dst, N: int, scale, out_raw):
+    """Gradients of forward_scaled for the cotangent g of its scaled output:
+    (d_coup, d_rad, d_scale, abs_dcoup, abs_drad, abs_dscale), fp64.
+
+    d_coup and d_rad are those of the plain operator times the destination's
+    factor (the operator is linear in each node's sum); d_scale[n] is the
+    product of g[n] with the node's unscaled sum out_raw[n] over rows 1..D-1."""
+    dc, dr, adc, adr = backward(g, coup, rad, dst, N)
+    s = np.asarray(scale, np.float64).reshape(-1)
+    d = np.asarray(dst, np.int64)
+    ok = (d >= 0) & (d < N)
+    se = np.where(ok, s[np.where(ok, d, 0)], 0.0)
+    with np.errstate(invalid="ignore", over="ignore"):
+        dc = dc * se[:, None]
+        dr = dr * se[:, None, None]
+        adc = adc * np.abs(se)[:, None]
+        adr = adr * np.abs(se)[:, None, None]
+    g64 = np.asarray(g, np.float64)
+    raw = np.asarray(out_raw, np.float64)
+    d_scale = np.einsum("nrc,nrc->n", g64[:, 1:], raw[:, 1:])
+    abs_ds = np.einsum("nrc,nrc->n", np.abs(g64[:, 1:]), np.abs(raw[:, 1:]))
+    return dc, dr, d_scale, adc, adr, abs_ds
+
+
 def slot_of_row(r: int) -> int:
     return int(_load().oracle_slot_of_row(r))
 

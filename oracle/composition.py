@@ -78,3 +78,24 @@ def backward(g, coup, rad, dst, N: int):
     d_rad = torch.zeros((E, lmax, C), dtype=torch.float64)
     d_rad.index_add_(1, idx, d_msg * coup_t[:, :, None])
     return d_coup.numpy(), d_rad.numpy()
+
+
+def scaled_with_autograd(coup, rad, dst, N: int, scale, g):
+    """The degree-normalised composition with its gradients taken by torch
+    autograd in fp64 (no hand-written adjoint): returns (out, d_coup, d_rad,
+    d_scale) for the cotangent g of out = scale[n] * composition(n), nodes
+    without edges zero."""
+    coup_t = torch.as_tensor(np.asarray(coup)).to(torch.float64).requires_grad_(True)
+    rad_t = torch.as_tensor(np.asarray(rad)).to(torch.float64).requires_grad_(True)
+    s_t = torch.as_tensor(np.asarray(scale)).to(torch.float64).requires_grad_(True)
+    dst_t = torch.as_tensor(np.asarray(dst)).to(torch.int64)
+    lmax = rad_t.shape[1]
+    keep = _valid(dst_t, N)
+    msg = coup_t[keep][:, :, None] * rad_t[keep][:, slot_index(lmax), :]
+    body = torch.zeros((N, msg.shape[1], rad_t.shape[2]), dtype=torch.float64).index_add(0, dst_t[keep], msg)
+    indeg = torch.bincount(dst_t[keep], minlength=N)
+    factor = torch.where(indeg > 0, s_t, torch.zeros_like(s_t))
+    out = torch.cat([torch.zeros((N, 1, rad_t.shape[2]), dtype=torch.float64), factor[:, None, None] * body], dim=1)
+    g_t = torch.as_tensor(np.asarray(g)).to(torch.float64)
+    d_coup, d_rad, d_s = torch.autograd.grad(out, (coup_t, rad_t, s_t), g_t)
+    return out.detach().numpy(), d_coup.numpy(), d_rad.numpy(), d_s.numpy()

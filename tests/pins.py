@@ -425,3 +425,61 @@ def pin_general_lmax(fwd, bwd, lmax):
             m = rad.copy(); m[e, s, 0] -= np.float32(h)
             fd = (L(coup, p) - L(coup, m)) / (2 * h)
             _require(abs(fd - dr[e, s, 0]) <= 1e-9 * scale, f"lmax {lmax} FD d_rad[{e},{s},0]")
+
+
+# ---------------------------------------------------------------- node factor
+#
+# The degree normalisation the pages apply to the operator's output (section
+# "What", third bullet): out[n] = s[n] * (operator output)[n], s one factor
+# per node; reading: a node without edges stays zero whatever s[n].
+#   fwd_s(coup, rad, dst, N, s)            -> (out, out_raw)
+#   bwd_s(g, coup, rad, dst, N, s, raw)    -> (d_coup, d_rad, d_scale)
+
+
+def pin_node_factor(fwd_s, bwd_s):
+    rng = np.random.default_rng(404)
+    # s = 1 is the plain operator, by brute force
+    N, E, C = 6, 20, 3
+    dst, coup, rad, g = tiny_graph(41, N, E, C)
+    out, raw = fwd_s(coup, rad, dst, N, np.ones(N, np.float32))
+    ref = brute_forward(coup, rad, dst, N)
+    _require(np.allclose(out, ref, rtol=1e-12, atol=1e-12) and np.allclose(raw, ref, rtol=1e-12, atol=1e-12),
+             "node factor 1 vs brute force")
+    # each node's rows scale by its factor; a node without edges is zero even for s = inf
+    dst = (dst % (N - 1)).astype(np.int32)          # node N-1 gets no edge
+    ref = brute_forward(coup, rad, dst, N)
+    s = rng.uniform(-2, 2, N).astype(np.float32)
+    empty = np.setdiff1d(np.arange(N), dst)
+    s[empty[0]] = np.inf
+    out, raw = fwd_s(coup, rad, dst, N, s)
+    has = np.isin(np.arange(N), dst)
+    want = np.zeros_like(ref)
+    want[has] = s.astype(np.float64)[has, None, None] * ref[has]
+    _require(np.allclose(out, want, rtol=1e-12, atol=1e-12), "node factor scaling")
+    _require(np.all(np.asarray(out)[empty] == 0), "node without edges under its factor")
+    # trilinear adjoint: <g, out> = <d_coup, coup> = <d_rad, rad> = <d_scale, s>
+    N, E, C = 17, 400, 4
+    dst, coup, rad, g = tiny_graph(42, N, E, C)
+    s = rng.uniform(0.1, 2, N).astype(np.float32)
+    out, raw = fwd_s(coup, rad, dst, N, s)
+    dc, dr, ds = bwd_s(g, coup, rad, dst, N, s, raw)
+    a = float(np.sum(g.astype(np.float64)[:, 1:] * np.asarray(out)[:, 1:]))
+    b = float(np.sum(np.asarray(dc) * coup.astype(np.float64)))
+    c = float(np.sum(np.asarray(dr) * rad.astype(np.float64)))
+    d = float(np.sum(np.asarray(ds) * s.astype(np.float64)))
+    scale = float(np.sum(np.abs(g.astype(np.float64)[:, 1:] * np.asarray(out)[:, 1:]))) + 1.0
+    _require(max(abs(a - b), abs(a - c), abs(a - d)) <= 1e-11 * scale, f"node factor adjoint {a} {b} {c} {d}")
+    # central differences in s (the output is linear in s)
+    h = 2.0 ** -8
+    N, E, C = 5, 30, 2
+    dst, coup, rad, g = tiny_graph(43, N, E, C, quantised=True)
+    s = (rng.integers(1, 64, N) / 16.0).astype(np.float32)
+    out, raw = fwd_s(coup, rad, dst, N, s)
+    _, _, ds = bwd_s(g, coup, rad, dst, N, s, raw)
+    g64 = g.astype(np.float64)
+    for n in range(N):
+        p = s.copy(); p[n] += np.float32(h)
+        m = s.copy(); m[n] -= np.float32(h)
+        fd = (float(np.sum(g64 * np.asarray(fwd_s(coup, rad, dst, N, p)[0]))) -
+              float(np.sum(g64 * np.asarray(fwd_s(coup, rad, dst, N, m)[0])))) / (2 * h)
+        _require(abs(fd - float(np.asarray(ds)[n])) <= 1e-9 * (1.0 + abs(fd)), f"FD d_scale[{n}]")

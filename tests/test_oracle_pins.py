@@ -314,3 +314,53 @@ def test_planted_mistake_is_caught(name):
     fwd, bwd, csr = MUTANTS[name]()
     failed = pins.run_all(fwd, bwd, csr)
     assert failed, f"planted mistake {name} passed every pin"
+
+
+# ----------------------------------------------------------- node factor
+
+
+def a_fwd_s(coup, rad, dst, N, s):
+    row_ptr, perm, _ = oracle.build_csr(dst, N)
+    out, _, raw, _ = oracle.forward_scaled(coup, rad, row_ptr, perm, N, s)
+    return out, raw
+
+
+def a_bwd_s(g, coup, rad, dst, N, s, raw):
+    dc, dr, ds, _, _, _ = oracle.backward_scaled(g, coup, rad, dst, N, s, raw)
+    return dc, dr, ds
+
+
+def test_node_factor_pins():
+    pins.pin_node_factor(a_fwd_s, a_bwd_s)
+
+
+def test_node_factor_oracle_matches_autograd_composition():
+    for lmax, C in ((3, 5), (2, 3)):
+        w = workloads.make_random(30, 900, C, seed=55 + lmax, lmax=lmax)
+        s = np.random.default_rng(lmax).uniform(-1.5, 1.5, w.N).astype(np.float32)
+        row_ptr, perm, _ = oracle.build_csr(w.dst, w.N)
+        out, _, raw, _ = oracle.forward_scaled(w.coup, w.rad, row_ptr, perm, w.N, s)
+        dc, dr, ds, _, _, _ = oracle.backward_scaled(w.grad_out, w.coup, w.rad, w.dst, w.N, s, raw)
+        out_b, dc_b, dr_b, ds_b = composition.scaled_with_autograd(w.coup, w.rad, w.dst, w.N, s, w.grad_out)
+        for x, y in ((out, out_b), (dc, dc_b), (dr, dr_b), (ds, ds_b)):
+            assert np.allclose(x, y, rtol=1e-11, atol=1e-11)
+
+
+@pytest.mark.parametrize("mistake", ["d_scale_from_scaled_out", "gradients_unscaled", "factor_on_empty_nodes"])
+def test_node_factor_planted_mistakes_caught(mistake):
+    def fwd(coup, rad, dst, N, s):
+        out, raw = a_fwd_s(coup, rad, dst, N, s)
+        if mistake == "factor_on_empty_nodes":
+            out = np.asarray(s, np.float64)[:, None, None] * np.asarray(raw)
+        return out, raw
+
+    def bwd(g, coup, rad, dst, N, s, raw):
+        dc, dr, ds = a_bwd_s(g, coup, rad, dst, N, s, raw)
+        if mistake == "d_scale_from_scaled_out":
+            ds = ds * np.asarray(s, np.float64)
+        if mistake == "gradients_unscaled":
+            dc, dr = a_bwd(g, coup, rad, dst, N)
+        return dc, dr, ds
+    with pytest.raises((pins.PinFailure, FloatingPointError)):
+        with np.errstate(invalid="raise"):
+            pins.pin_node_factor(fwd, bwd)
