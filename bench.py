@@ -55,8 +55,17 @@ def algorithmic_bytes(N: int, E: int, C: int, lmax: int = 3) -> dict:
     return {"fwd": fwd, "bwd": bwd, "csr": csr}
 
 
-def metric_for(lmax: int) -> str:
-    return METRIC if lmax == 3 else METRIC.replace("C=32;", f"C=32,lmax={lmax};")
+def metric_for(lmax: int, scaled: bool = False) -> str:
+    m = METRIC if lmax == 3 else METRIC.replace("C=32;", f"C=32,lmax={lmax};")
+    return m.replace("zonal-scatter", "degree-normalised zonal-scatter") if scaled else m
+
+
+def scaled_extra_bytes(N: int, C: int, lmax: int) -> dict:
+    """What fusing the per-node factor adds: the factor (4 B per node) and the
+    unscaled output the scale's gradient needs (written by the forward, read
+    with g again by the backward)."""
+    node = 4 * (lmax + 1) ** 2 * C
+    return {"fwd": 4 * N + node * N, "bwd": 4 * N + 2 * node * N + 4 * N}
 
 
 def measured_peaks() -> tuple[float, str]:
@@ -113,12 +122,14 @@ def job_throughput(units_per_rank: int, steps: int, max_ms: float, world: int) -
     return world * units_per_rank * steps / (max_ms / 1e3)
 
 
-def workload_config(w, backward: str) -> dict:
+def workload_config(w, backward: str, scaled: bool = False) -> dict:
     entry = "zs_backward_csr" if backward == "csr" else "zs_backward"
+    if scaled:
+        entry = "zs_backward_scaled"
     lmax = w.rad.shape[1]
     rows = "/".join(str(2 * l + 1) for l in range(1, lmax + 1))
     return {"workload": f"{w.name}: N={w.N}, E={w.E}, C={w.C}, lmax={lmax} (rows {rows}), fp32, seed {w.seed}",
-            "step": "zs_build_csr + zs_forward + " + entry,
+            "step": "zs_build_csr + " + ("zs_forward_scaled" if scaled else "zs_forward") + " + " + entry,
             "l2": ("inputs larger than L2" if w.coup.nbytes + w.rad.nbytes > L2_BYTES else
                    "inputs smaller than L2, no flush") + " (coup+rad = %.0f MB)" % ((w.coup.nbytes + w.rad.nbytes) / 1e6)}
 
@@ -238,6 +249,39 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     bwd, bwd_other, other_name = (bwd_csr, bwd_edge, "bwd_edge") if args.backward == "csr" else \
         (bwd_edge, bwd_csr, "bwd_csr")
 
+    if args.scaled:
+        # the degree normalisation fused in: s[n] = 1/sqrt(in-degree), 0 without edges
+        indeg = np.bincount(w.dst[(w.dst >= 0) & (w.dst < N)], minlength=N)
+        s_host = np.where(indeg > 0, 1.0 / np.sqrt(np.maximum(indeg, 1)), 0.0).astype(np.float32)
+        node_scale = torch.from_numpy(s_host).to(dev)
+        out_raw = torch.empty_like(out)
+        d_scale = torch.empty(N, dtype=torch.float32, device=dev)
+
+        def fwd():
+            st = lib.zs_forward_scaled(P(coup), P(rad), P(row_ptr), P(perm), P(node_scale), E, N, C, L, P(out),
+                                       P(out_raw), P(ws_fwd), fwd_ws_bytes, sp)
+            assert st == 0, lib.zs_last_error()
+
+        def bwd():
+            st = lib.zs_backward_scaled(P(g), P(coup), P(rad), P(dst), P(node_scale), P(out_raw), E, N, C, L,
+                                        P(d_coup), P(d_rad), P(d_scale), sp)
+            assert st == 0, lib.zs_last_error()
+
+        def fwd_unfused():
+            plain_fwd()
+            torch.mul(out_raw, node_scale[:, None, None], out=out)
+
+        def bwd_unfused():
+            gs = g * node_scale[:, None, None]
+            st = lib.zs_backward(P(gs), P(coup), P(rad), P(dst), E, N, C, L, P(d_coup), P(d_rad), sp)
+            assert st == 0, lib.zs_last_error()
+            torch.sum(g[:, 1:] * out_raw[:, 1:], dim=(1, 2), out=d_scale)
+
+        def plain_fwd():
+            st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(out_raw), P(ws_fwd),
+                                fwd_ws_bytes, sp)
+            assert st == 0, lib.zs_last_error()
+
     # zs_build_csr: three launches on its one-pass counting path (N + 1 <= 5120),
     # else three per 8-bit radix pass plus the row_ptr pass (one launch for E = 0);
     # zs_forward: one kernel at lmax = 3, C = 32 (aligned tensors), else main
@@ -249,6 +293,8 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     else:
         csr_launches = 3 * max(1, (max(N, 1).bit_length() + 7) // 8) + 1
     launches_per_step = csr_launches + (1 if (C == 32 and L == 3) else 2) + (1 if E > 0 else 0)
+    if args.scaled:
+        launches_per_step += 1   # the scale's gradient
 
     for _ in range(args.warmup):
         csr(); fwd(); bwd()
@@ -293,6 +339,23 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         b.record(stream)
     torch.cuda.synchronize()
     per[other_name] = [a.elapsed_time(b) * 1e3 for a, b in oth]
+    unfused = None
+    if args.scaled:
+        # the same step with the factor applied by separate torch ops
+        ev_u = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)] for k in ("fwd", "bwd")}
+        for _ in range(args.warmup):
+            csr(); fwd_unfused(); bwd_unfused()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            csr()
+            for k, fn in (("fwd", fwd_unfused), ("bwd", bwd_unfused)):
+                ev_u[k][i][0].record(stream)
+                fn()
+                ev_u[k][i][1].record(stream)
+        torch.cuda.synchronize()
+        unfused = {k + "_us": statistics.median(a.elapsed_time(b) * 1e3 for a, b in ev_u[k]) for k in ev_u}
+        unfused["how"] = "zs_forward + torch.mul; g*s in torch, zs_backward, torch sum for d_scale"
     zs.zs_check_timeouts()
 
     # end to end through the public API: pinned host buffers in, results out
@@ -312,10 +375,16 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
             rad.copy_(h_rad, non_blocking=True)
             g.copy_(h_g, non_blocking=True)
             zs.zs_build_csr(dst, N, row_ptr=row_ptr, perm=perm, bad_dst_count=bad, workspace=ws_csr)
-            zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
-            if args.backward == "csr":
+            if args.scaled:
+                zs.zs_forward_scaled(coup, rad, row_ptr, perm, node_scale, N, out=out, out_raw=out_raw,
+                                     workspace=ws_fwd)
+                zs.zs_backward_scaled(g, coup, rad, dst, node_scale, N, out_raw=out_raw, d_coup=d_coup,
+                                      d_rad=d_rad, d_scale=d_scale)
+            elif args.backward == "csr":
+                zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
                 zs.zs_backward_csr(g, coup, rad, row_ptr, perm, N, d_coup=d_coup, d_rad=d_rad)
             else:
+                zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
                 zs.zs_backward(g, coup, rad, dst, N, d_coup=d_coup, d_rad=d_rad)
             h_out.copy_(out, non_blocking=True)
             h_dc.copy_(d_coup, non_blocking=True)
@@ -345,6 +414,10 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         return None
 
     ab = algorithmic_bytes(N, E, C, L)
+    if args.scaled:
+        extra = scaled_extra_bytes(N, C, L)
+        ab["fwd"] += extra["fwd"]
+        ab["bwd"] += extra["bwd"]
     peak, peak_kind = measured_peaks()
     kernels = {}
     ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
@@ -364,7 +437,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     ms_per_step = total_ms / args.steps
     fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
     res = {
-        "metric": metric_for(L),
+        "metric": metric_for(L, args.scaled),
         "value": job_throughput(E, args.steps, total_ms, world),
         "unit": "edges/s",
         "n_gpus": world,
@@ -376,7 +449,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": dict(workload_config(w, args.backward),
+        "config": dict(workload_config(w, args.backward, args.scaled),
                        parallelism="replicas" if world > 1 else "single GPU"),
         "fwd_bwd_edges_per_s": E / (fwd_bwd_us * 1e-6),
         "kernels": kernels,
@@ -385,6 +458,8 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if unfused is not None:
+        res["unfused"] = unfused
     return res
 
 
@@ -433,6 +508,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--scaled", action="store_true",
+                    help="step with the degree normalisation fused in (zs_forward_scaled, zs_backward_scaled)")
     ap.add_argument("--lmax", type=int, default=3, choices=[1, 2, 3, 4, 5],
                     help="ladder degree of the operands (3: the 3/5/7 rows of the headline workload)")
     args = ap.parse_args()

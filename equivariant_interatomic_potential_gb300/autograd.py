@@ -7,6 +7,10 @@ and "Tests").  Here that operator is a ``torch.library`` custom op:
 
   ``zs_gie::build_csr(dst, num_nodes) -> (row_ptr, perm)``
   ``zs_gie::zonal_scatter(coup, rad, dst, row_ptr, perm, num_nodes) -> out``
+  ``zs_gie::zonal_scatter_scaled(coup, rad, dst, row_ptr, perm, node_scale,
+  num_nodes) -> (out, out_raw)``: the degree normalisation the pages apply
+  after the operator (section "What", third bullet), fused: out[n] =
+  node_scale[n] * the operator's sum, differentiable in node_scale too
 
 ``zonal_scatter``'s backward is ``zs_gie::zonal_scatter_backward`` (the
 edge-order ``zs_backward``), itself an operator without a derivative, so a
@@ -91,3 +95,59 @@ def zonal_scatter_from_dst(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Ten
     """Build the CSR of dst, then the differentiable zonal scatter."""
     row_ptr, perm = build_csr(dst, num_nodes)
     return zonal_scatter(coup, rad, dst, row_ptr, perm, num_nodes)
+
+
+@torch.library.custom_op(f"{_NS}::zonal_scatter_scaled", mutates_args=())
+def zonal_scatter_scaled(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, row_ptr: torch.Tensor,
+                         perm: torch.Tensor, node_scale: torch.Tensor,
+                         num_nodes: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """(out, out_raw): out[n] = node_scale[n] * out_raw[n], out_raw the zonal scatter (N, D, C)."""
+    _cuda_only("zonal_scatter_scaled", coup, rad, dst, row_ptr, perm, node_scale)
+    return zs.zs_forward_scaled(coup.contiguous(), rad.contiguous(), row_ptr.contiguous(), perm.contiguous(),
+                                node_scale.contiguous(), num_nodes)
+
+
+@zonal_scatter_scaled.register_fake
+def _(coup, rad, dst, row_ptr, perm, node_scale, num_nodes):
+    shape = (num_nodes, (rad.shape[1] + 1) ** 2, rad.shape[2])
+    return coup.new_empty(shape), coup.new_empty(shape)
+
+
+@torch.library.custom_op(f"{_NS}::zonal_scatter_scaled_backward", mutates_args=())
+def zonal_scatter_scaled_backward(grad_out: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor,
+                                  node_scale: torch.Tensor, out_raw: torch.Tensor,
+                                  num_nodes: int) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(d_coup, d_rad, d_scale) for the cotangent grad_out of the scaled output."""
+    _cuda_only("zonal_scatter_scaled_backward", grad_out, coup, rad, dst, node_scale, out_raw)
+    return zs.zs_backward_scaled(grad_out.contiguous(), coup.contiguous(), rad.contiguous(), dst.contiguous(),
+                                 node_scale.contiguous(), num_nodes, out_raw=out_raw.contiguous())
+
+
+@zonal_scatter_scaled_backward.register_fake
+def _(grad_out, coup, rad, dst, node_scale, out_raw, num_nodes):
+    return coup.new_empty(coup.shape), rad.new_empty(rad.shape), node_scale.new_empty(node_scale.shape)
+
+
+def _setup_context_scaled(ctx, inputs, output):
+    coup, rad, dst, row_ptr, perm, node_scale, num_nodes = inputs
+    out, out_raw = output
+    ctx.mark_non_differentiable(out_raw)
+    ctx.save_for_backward(coup, rad, dst, node_scale, out_raw)
+    ctx.num_nodes = num_nodes
+
+
+def _backward_scaled(ctx, grad_out, grad_raw):
+    coup, rad, dst, node_scale, out_raw = ctx.saved_tensors
+    d_coup, d_rad, d_scale = zonal_scatter_scaled_backward(grad_out, coup, rad, dst, node_scale, out_raw,
+                                                           ctx.num_nodes)
+    return d_coup, d_rad, None, None, None, d_scale, None
+
+
+zonal_scatter_scaled.register_autograd(_backward_scaled, setup_context=_setup_context_scaled)
+
+
+def degree_normalised_scatter(coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, node_scale: torch.Tensor,
+                              num_nodes: int) -> torch.Tensor:
+    """CSR of dst, then node_scale[n] * zonal scatter, differentiable in coup, rad and node_scale."""
+    row_ptr, perm = build_csr(dst, num_nodes)
+    return zonal_scatter_scaled(coup, rad, dst, row_ptr, perm, node_scale, num_nodes)[0]

@@ -428,6 +428,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
             for (int i = 0; i < T / 4; ++i) {
                 const int j = 4 * i + Q.grp;
                 const int m = ring.meta[st * T + j];
+                const float sc = (scale && m >= 0) ? __ldg(scale + m) : 1.f;   // issued early, used at the stores
                 const float* gj = ring.gs + (st * T + j) * (15 * kC32) + 4 * Q.q;
                 float4 G[15];
 #pragma unroll
@@ -463,7 +464,6 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 float* dr = d_rad + e * (3 * kC32) + 4 * Q.q;
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (scale && ok) {   // gradients of the scaled output: the destination's scale times these
-                    const float sc = __ldg(scale + m);
                     s0 = make_float4(s0.x * sc, s0.y * sc, s0.z * sc, s0.w * sc);
                     s1 = make_float4(s1.x * sc, s1.y * sc, s1.z * sc, s1.w * sc);
                     s2 = make_float4(s2.x * sc, s2.y * sc, s2.z * sc, s2.w * sc);
@@ -552,7 +552,8 @@ zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s) {
 
 // Gradient of the node scale of the scaled forward: d_scale[n] = sum over
 // rows 1..D-1 and channels of g[n,r,c] * out_raw[n,r,c], one warp per node,
-// lane-strided products added in a fixed order.
+// lane-strided products added in a fixed order (float4 steps when both rows
+// are 16-byte aligned, four steps in flight per lane).
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32_t N, int64_t node_floats, int C,
                float* __restrict__ d_scale) {
@@ -561,10 +562,32 @@ bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32
     pdl_wait();
     pdl_trigger();
     if (n >= N) return;
-    const float* gp = g + n * node_floats;
-    const float* rp = raw + n * node_floats;
+    const float* gp = g + n * node_floats + C;        // rows 1..D-1
+    const float* rp = raw + n * node_floats + C;
+    const int64_t len = node_floats - C;
     float acc = 0.f;
-    for (int64_t i = C + lane; i < node_floats; i += 32) acc = fmaf(__ldg(gp + i), __ldg(rp + i), acc);
+    if (aligned16(gp) && aligned16(rp) && (len & 3) == 0) {
+        const float4* g4 = reinterpret_cast<const float4*>(gp);
+        const float4* r4 = reinterpret_cast<const float4*>(rp);
+        const int64_t len4 = len >> 2;
+        int64_t i = lane;
+        for (; i + 96 < len4; i += 128) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a[u] = __ldg(g4 + i + 32 * u);
+                b[u] = __ldg(r4 + i + 32 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc += a[u].x * b[u].x + a[u].y * b[u].y + a[u].z * b[u].z + a[u].w * b[u].w;
+        }
+        for (; i < len4; i += 32) {
+            const float4 a = __ldg(g4 + i), b = __ldg(r4 + i);
+            acc += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+        }
+    } else {
+        for (int64_t i = lane; i < len; i += 32) acc = fmaf(__ldg(gp + i), __ldg(rp + i), acc);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
     if (lane == 0) d_scale[n] = acc;
