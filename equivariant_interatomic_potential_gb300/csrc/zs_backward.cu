@@ -57,13 +57,14 @@ template <int L>
 __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const float* __restrict__ coup,
                                              const float* __restrict__ rad, int64_t e, int d, int C, int lane,
                                              float* __restrict__ d_coup, float* __restrict__ d_rad,
-                                             const float* __restrict__ scale = nullptr) {
+                                             const float* __restrict__ scale = nullptr,
+                                             int64_t cld = Ladder<L>::R, int64_t dld = Ladder<L>::R) {
     constexpr int R = Ladder<L>::R, S = Ladder<L>::S, D = Ladder<L>::D;
     constexpr int RP = (R + 31) / 32 * 32;   // rows padded to whole warps for the reduction
     const bool ok = d >= 0;
     float cv[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) cv[r] = __ldg(coup + e * R + r);
+    for (int r = 0; r < R; ++r) cv[r] = __ldg(coup + e * cld + r);
     float pc[RP];
 #pragma unroll
     for (int r = 0; r < RP; ++r) pc[r] = 0.f;
@@ -95,7 +96,7 @@ __device__ __forceinline__ void bwd_gen_edge(const float* __restrict__ g, const 
 #pragma unroll
     for (int r0 = 0; r0 < RP; r0 += 32) {
         const float v = warp_reduce_scatter32(pc + r0, lane);
-        if (r0 + lane < R) d_coup[e * R + r0 + lane] = ok ? (scale ? v * sc : v) : 0.f;
+        if (r0 + lane < R) d_coup[e * dld + r0 + lane] = ok ? (scale ? v * sc : v) : 0.f;
     }
 }
 
@@ -103,13 +104,13 @@ template <int L>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
         const int32_t* __restrict__ dst, int64_t E, int32_t N, int C,
-        float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale) {
+        float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale, int cld, int dld) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
     for (int64_t e = (int64_t)blockIdx.x * kBwdWarps + warp; e < E; e += (int64_t)gridDim.x * kBwdWarps) {
         const int d = __ldg(dst + e);
-        bwd_gen_edge<L>(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad, scale);
+        bwd_gen_edge<L>(g, coup, rad, e, (d >= 0 && d < N) ? d : -1, C, lane, d_coup, d_rad, scale, cld, dld);
     }
 }
 
@@ -188,7 +189,7 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     if (active) {
         ring.prefetch_perm(perm, Q.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, Q.lane);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, 15, rad, E, Q.lane);
         const int vend = __ldg(row_ptr + N);
         // this group's node: n covers positions [.., b); G holds its rows 1..15
         int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
@@ -272,7 +273,7 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
                     if (row + 1 < 15) st_hint(dc + 1, has_node ? t1 : 0.f, pol_last);
                 }
             }
-            ring.refill(perm, coup, rad, E, Q.lane);
+            ring.refill(perm, coup, 15, rad, E, Q.lane);
         }
     }
     ring.drain();
@@ -342,9 +343,11 @@ struct EdgeRing {
         blk_next = load_block(dst, 1, lane);
     }
 
-    __device__ __forceinline__ void issue(const int32_t* __restrict__ dst, const float* __restrict__ coup_g,
-                                          const float* __restrict__ rad_g, const float* __restrict__ g_g,
-                                          int N, int lane) {
+    // Coupling rows are cld floats apart; coup_bulk says they are packed
+    // (cld == 15) from a 16-byte boundary, so a whole tile is one bulk copy.
+    __device__ __forceinline__ void issue(const int32_t* __restrict__ dst, const float* __restrict__ coup_g, int cld,
+                                          bool coup_bulk, const float* __restrict__ rad_g,
+                                          const float* __restrict__ g_g, int N, int lane) {
         if (issued >= ntiles) return;
         const int k = issued;
         const int st = k % S;
@@ -359,14 +362,14 @@ struct EdgeRing {
         const int cnt = imin(T, p1 - e0);
         const bool in = lane < cnt;
         const bool valid = in && d >= 0 && d < N;
-        const bool full = cnt == T;
+        const bool full = cnt == T && coup_bulk;
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         const uint32_t bytes = (uint32_t)cnt * 384u + (full ? (uint32_t)T * 60u : 0u) + nvalid * 1920u;
         const uint32_t bar = bar0 + 8 * st;
         float* cst = coups + st * T * 15;
         if (lane < T) meta[st * T + lane] = valid ? d : (in ? -1 : -2);
-        if (!full && in) {   // ragged last tile: its coupling block is not a whole number of 16-byte pieces
-            const float* src = coup_g + (int64_t)(e0 + lane) * 15;
+        if (!full && in) {   // ragged last tile, or rows not packed: plain loads of each row
+            const float* src = coup_g + (int64_t)(e0 + lane) * cld;
 #pragma unroll
             for (int r = 0; r < 15; ++r) cst[lane * 15 + r] = __ldg(src + r);
         }
@@ -400,11 +403,18 @@ struct EdgeRing {
     }
 };
 
-template <int W, int S, int T>
+// kGeneral: the scaled or strided variant (a node factor, coupling and
+// coupling-gradient rows cld / dld floats apart); the plain operator's
+// instance keeps those at their compile-time defaults.
+template <int W, int S, int T, bool kGeneral>
 __global__ void __launch_bounds__(W * 32, 1)
 bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
                  const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
-                 float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale) {
+                 float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale_arg,
+                 int cld_arg, int dld_arg, int coup_bulk_arg) {
+    const float* __restrict__ scale = kGeneral ? scale_arg : nullptr;
+    const int cld = kGeneral ? cld_arg : 15, dld = kGeneral ? dld_arg : 15;
+    const int coup_bulk = kGeneral ? coup_bulk_arg : 1;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const QuadLane Q(threadIdx.x & 31);
@@ -420,7 +430,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
     if (active) {
         ring.prefetch(dst, Q.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(dst, coup, rad, g, N, Q.lane);
+        for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
             const int e0 = p0 + k * T;
@@ -460,7 +470,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 const bool ok = m >= 0;
                 const int64_t e = e0 + j;
                 const int row = 8 * Q.b2 + 4 * Q.b1 + 2 * Q.b0;
-                float* dc = d_coup + e * 15 + row;
+                float* dc = d_coup + e * dld + row;
                 float* dr = d_rad + e * (3 * kC32) + 4 * Q.q;
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (scale && ok) {   // gradients of the scaled output: the destination's scale times these
@@ -477,7 +487,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 if (row + 1 < 15) st_stream(dc + 1, ok ? t1 : 0.f);
             }
             __syncwarp();
-            ring.issue(dst, coup, rad, g, N, Q.lane);
+            ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
         }
     }
     ring.drain();
@@ -516,17 +526,25 @@ constexpr int kEdgeWarpsSmall = 12;   // 2-stage rings of 4 edges: 12 warps fit 
 constexpr int kEdgeWarpsLarge = 8;    // 3-stage rings of 4 edges: 8 warps
 
 template <int W, int S, int T>
-void launch_edge_tma(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
-                     float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
+void launch_edge_tma(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
+                     int32_t N, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
     const int64_t warps_max = (int64_t)num_sms() * W;
     const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
     const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
     const int64_t ctas = (Wtot + W - 1) / W;
     const int smem = W * EdgeRingLayout<S, T>::kBytes;
-    static std::atomic<bool> attr_done[kMaxDevices];
-    set_smem_limit_once(bwd_edge_c32_tma<W, S, T>, smem, attr_done);
-    launch(bwd_edge_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
-           (int)Wtot, d_coup, d_rad, scale);
+    const int bulk = (cld == 15 && aligned16(coup)) ? 1 : 0;
+    if (scale == nullptr && dld == 15 && bulk) {
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_edge_c32_tma<W, S, T, false>, smem, attr_done);
+        launch(bwd_edge_c32_tma<W, S, T, false>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+    } else {
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_edge_c32_tma<W, S, T, true>, smem, attr_done);
+        launch(bwd_edge_c32_tma<W, S, T, true>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+    }
 }
 
 // One warp waits on an mbarrier that nothing arrives on, with a limit of
@@ -594,11 +612,11 @@ bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32
 }
 
 template <int L>
-void launch_gen_edges(const float* g, const float* coup, const float* rad, const int32_t* dst, int64_t E, int32_t N,
-                      int C, float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
+void launch_gen_edges(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
+                      int32_t N, int C, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
     const int64_t want = (E + kBwdWarps - 1) / kBwdWarps;
     const int grid = (int)imin<int64_t>(want, (int64_t)num_sms() * 8);
-    launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad, scale);
+    launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, cld, dld);
 }
 
 template <int L>
@@ -615,32 +633,40 @@ void launch_gen_csr(const float* g, const float* coup, const float* rad, const i
 
 using namespace zs;
 
-static zs_status backward_impl(const char* name, const float* g, const float* coup, const float* rad,
+static zs_status backward_impl(const char* name, const float* g, const float* coup, int64_t cld, const float* rad,
                                const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
-                               float* d_coup, float* d_rad, const float* scale, cudaStream_t s) {
+                               float* d_coup, int64_t dld, float* d_rad, const float* scale, cudaStream_t s) {
     if (lmax < 1 || lmax > kMaxLmax)
         return fail(ZS_ERR_UNSUPPORTED, "%s: lmax=%d, supported ladders are lmax 1..%d", name, lmax, kMaxLmax);
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "%s: bad sizes E=%lld N=%d C=%d", name, (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "%s: E=%lld exceeds the int32 index range", name, (long long)E);
+    const int R = ladder_rows(lmax);
+    if (cld < R || dld < R || cld > ((int64_t)1 << 24) || dld > ((int64_t)1 << 24))
+        return fail(ZS_ERR_INVALID_ARG, "%s: row strides %lld / %lld below %d rows or too large", name, (long long)cld,
+                    (long long)dld, R);
     if (E == 0) return ZS_OK;
     if (!coup || !rad || !dst || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "%s: NULL array with E > 0", name);
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "%s: g is NULL with N > 0", name);
-    const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
+    // coupling rows and d_coup may have any stride and 4-byte alignment on every path
+    const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad);
     if (fast) {
         // While the cotangent block is small enough to stay in L2 next to the
         // streams, more warps with one tile in flight each hide the gather
         // latency best; a larger block misses L2 more often and wants more
         // tiles in flight per warp.
         const bool small_g = (int64_t)N * 16 * kC32 * 4 <= kSmallCotangentBytes;
-        if (small_g) launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, scale, s);
-        else launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, rad, dst, E, N, d_coup, d_rad, scale, s);
+        if (small_g)
+            launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
+        else
+            launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
     } else {
+        const int c = (int)cld, d = (int)dld;
         switch (lmax) {
-            case 1: launch_gen_edges<1>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
-            case 2: launch_gen_edges<2>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
-            case 3: launch_gen_edges<3>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
-            case 4: launch_gen_edges<4>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
-            default: launch_gen_edges<5>(g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, s); break;
+            case 1: launch_gen_edges<1>(g, coup, c, rad, dst, E, N, C, d_coup, d, d_rad, scale, s); break;
+            case 2: launch_gen_edges<2>(g, coup, c, rad, dst, E, N, C, d_coup, d, d_rad, scale, s); break;
+            case 3: launch_gen_edges<3>(g, coup, c, rad, dst, E, N, C, d_coup, d, d_rad, scale, s); break;
+            case 4: launch_gen_edges<4>(g, coup, c, rad, dst, E, N, C, d_coup, d, d_rad, scale, s); break;
+            default: launch_gen_edges<5>(g, coup, c, rad, dst, E, N, C, d_coup, d, d_rad, scale, s); break;
         }
     }
     return check_launch(name);
@@ -649,8 +675,16 @@ static zs_status backward_impl(const char* name, const float* g, const float* co
 extern "C" zs_status zs_backward(const float* g, const float* coup, const float* rad,
                                  const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
                                  float* d_coup, float* d_rad, zs_stream_t stream) {
-    return backward_impl("zs_backward", g, coup, rad, dst, E, N, C, lmax, d_coup, d_rad, nullptr,
+    const int R = ladder_rows(lmax < 1 ? 1 : (lmax > kMaxLmax ? kMaxLmax : lmax));
+    return backward_impl("zs_backward", g, coup, R, rad, dst, E, N, C, lmax, d_coup, R, d_rad, nullptr,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" zs_status zs_backward_ld(const float* g, const float* coup, int64_t coup_ld, const float* rad,
+                                    const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                    float* d_coup, int64_t d_coup_ld, float* d_rad, zs_stream_t stream) {
+    return backward_impl("zs_backward_ld", g, coup, coup_ld, rad, dst, E, N, C, lmax, d_coup, d_coup_ld, d_rad,
+                         nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" zs_status zs_backward_scaled(const float* g, const float* coup, const float* rad, const int32_t* dst,
@@ -672,7 +706,8 @@ extern "C" zs_status zs_backward_scaled(const float* g, const float* coup, const
         const zs_status st = check_launch("zs_backward_scaled");
         if (st != ZS_OK) return st;
     }
-    return backward_impl("zs_backward_scaled", g, coup, rad, dst, E, N, C, lmax, d_coup, d_rad, node_scale, s);
+    const int R = ladder_rows(lmax);
+    return backward_impl("zs_backward_scaled", g, coup, R, rad, dst, E, N, C, lmax, d_coup, R, d_rad, node_scale, s);
 }
 
 extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const float* rad,

@@ -197,7 +197,7 @@ __device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, f
 // position order, closing a node when its last position is reached.
 template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
-fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
+fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
             int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
             uint64_t* __restrict__ flags, uint64_t salt) {
@@ -224,7 +224,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
     if (active) {
         ring.prefetch_perm(perm, L.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, rad, E, L.lane);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, cld, rad, E, L.lane);
         // current node n covers positions [a, b); empty nodes this window owns
         // (those starting in it, or all trailing ones for the last window) are zeroed
         // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead
@@ -280,7 +280,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
                     advance();
                 }
             }
-            ring.refill(perm, coup, rad, E, L.lane);
+            ring.refill(perm, coup, cld, rad, E, L.lane);
         }
         // a node still open at the end runs past p1
         if (n < N && a < pe && b > pe) {
@@ -366,7 +366,7 @@ fwd_c32_tma(const float* __restrict__ coup, const float* __restrict__ rad,
 // --------------------------------------------------------------------------
 
 template <int L>
-__device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, const float* __restrict__ rad,
+__device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
                                                const int32_t* __restrict__ perm, int64_t E, int C, int c,
                                                int s, int t, float (*cs)[Ladder<L>::R + 1], int lane,
                                                float acc[Ladder<L>::R]) {
@@ -387,7 +387,7 @@ __device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, c
             const int r = v - j * R;
             const int e = __shfl_sync(kFull, e_l, j);
             float cv = 0.f;
-            if (j < cnt && e >= 0) cv = __ldg(coup + (int64_t)e * R + r);
+            if (j < cnt && e >= 0) cv = __ldg(coup + (int64_t)e * cld + r);
             cs[j][r] = cv;
         }
         __syncwarp();
@@ -407,7 +407,7 @@ __device__ __forceinline__ void accumulate_gen(const float* __restrict__ coup, c
 
 template <int L>
 __global__ void __launch_bounds__(kFwdThreads)
-fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
+fwd_gen_main(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
              const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
              int64_t E, int32_t N, int C, int Wtot, NodeOut o, float* __restrict__ part,
              int32_t* __restrict__ cross) {
@@ -447,7 +447,7 @@ fwd_gen_main(const float* __restrict__ coup, const float* __restrict__ rad,
             float acc[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) acc[r] = 0.f;
-            accumulate_gen<L>(coup, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
+            accumulate_gen<L>(coup, cld, rad, perm, E, C, c, (int)max((int64_t)a, p0), (int)min((int64_t)b, p1),
                               cs[warp], lane, acc);
             if (c < C) {
                 if (full && rnode) {
@@ -582,11 +582,12 @@ struct FwdPlan {
     int64_t KW, Wtot, ctas, windows;
 };
 
-static FwdPlan fwd_plan(const float* coup, const float* rad, const NodeOut& o, int64_t E, int C, int lmax) {
+static FwdPlan fwd_plan(const float* rad, const NodeOut& o, int64_t E, int C, int lmax) {
     FwdPlan p{};
     p.R = ladder_rows(lmax);
-    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(o.out) && aligned16(coup) &&
-             (o.raw == nullptr || aligned16(o.raw));
+    // the coupling rows may have any 4-byte alignment and stride: the ring
+    // copies each one's 16-byte-aligned span
+    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(o.out) && (o.raw == nullptr || aligned16(o.raw));
     if (p.fast) {
         // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
         // the same number of CSR positions (at least one tile).
@@ -604,16 +605,16 @@ static FwdPlan fwd_plan(const float* coup, const float* rad, const NodeOut& o, i
 }
 
 template <int L>
-static void launch_gen(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
+static void launch_gen(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
                        const int32_t* perm, int64_t E, int32_t N, int C, const NodeOut& o, const Scratch& sc,
                        cudaStream_t s) {
-    launch(fwd_gen_main<L>, (unsigned)p.ctas, kFwdThreads, 0, s, coup, rad, row_ptr, perm, E, N, C, (int)p.Wtot,
+    launch(fwd_gen_main<L>, (unsigned)p.ctas, kFwdThreads, 0, s, coup, cld, rad, row_ptr, perm, E, N, C, (int)p.Wtot,
            o, sc.part, sc.cross);
     launch(fwd_fixup, (unsigned)p.Wtot, kFwdThreads, 0, s, row_ptr, (const int32_t*)sc.cross, C, Ladder<L>::R,
            kGenWin, (const float*)sc.part, o);
 }
 
-static void launch_forward(const FwdPlan& p, const float* coup, const float* rad, const int32_t* row_ptr,
+static void launch_forward(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
                            const int32_t* perm, int64_t E, int32_t N, int C, int lmax, const NodeOut& o,
                            const Scratch& sc, cudaStream_t s) {
     if (p.fast) {
@@ -621,15 +622,15 @@ static void launch_forward(const FwdPlan& p, const float* coup, const float* rad
         static std::atomic<bool> attr_done[kMaxDevices];
         set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
         launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)p.ctas, kTmaWarps * 32, smem, s,
-               coup, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, o, sc.part, sc.flags, next_salt());
+               coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, o, sc.part, sc.flags, next_salt());
         return;
     }
     switch (lmax) {
-        case 1: launch_gen<1>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
-        case 2: launch_gen<2>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
-        case 3: launch_gen<3>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
-        case 4: launch_gen<4>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
-        default: launch_gen<5>(p, coup, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 1: launch_gen<1>(p, coup, cld, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 2: launch_gen<2>(p, coup, cld, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 3: launch_gen<3>(p, coup, cld, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        case 4: launch_gen<4>(p, coup, cld, rad, row_ptr, perm, E, N, C, o, sc, s); break;
+        default: launch_gen<5>(p, coup, cld, rad, row_ptr, perm, E, N, C, o, sc, s); break;
     }
 }
 
@@ -648,11 +649,15 @@ extern "C" size_t zs_forward_workspace_bytes(int64_t E, int32_t N, int32_t C) {
     return zs_forward_workspace_bytes_lmax(E, N, C, 3);
 }
 
-static zs_status forward_impl(const char* name, const float* coup, const float* rad, const int32_t* row_ptr,
-                              const int32_t* perm, int64_t E, int32_t N, int32_t C, int32_t lmax, const NodeOut& o,
-                              void* workspace, size_t workspace_bytes, zs_stream_t stream) {
+static zs_status forward_impl(const char* name, const float* coup, int64_t cld, const float* rad,
+                              const int32_t* row_ptr, const int32_t* perm, int64_t E, int32_t N, int32_t C,
+                              int32_t lmax, const NodeOut& o, void* workspace, size_t workspace_bytes,
+                              zs_stream_t stream) {
     if (lmax < 1 || lmax > kMaxLmax)
         return fail(ZS_ERR_UNSUPPORTED, "%s: lmax=%d, supported ladders are lmax 1..%d", name, lmax, kMaxLmax);
+    if (cld < ladder_rows(lmax) || cld > (int64_t)1 << 24)
+        return fail(ZS_ERR_INVALID_ARG, "%s: coupling row stride %lld below %d rows or too large", name, (long long)cld,
+                    ladder_rows(lmax));
     if (E < 0 || N < 0 || C < 1) return fail(ZS_ERR_INVALID_ARG, "%s: bad sizes E=%lld N=%d C=%d", name, (long long)E, N, C);
     if (E >= ((int64_t)1 << 31) - 1) return fail(ZS_ERR_INVALID_ARG, "%s: E=%lld exceeds the int32 index range", name, (long long)E);
     if (!row_ptr) return fail(ZS_ERR_INVALID_ARG, "%s: row_ptr is NULL", name);
@@ -663,8 +668,8 @@ static zs_status forward_impl(const char* name, const float* coup, const float* 
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(ZS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
     if (N == 0) return ZS_OK;
-    const FwdPlan p = fwd_plan(coup, rad, o, E, C, lmax);
-    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(workspace, p.windows, C, p.R),
+    const FwdPlan p = fwd_plan(rad, o, E, C, lmax);
+    launch_forward(p, coup, (int)cld, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(workspace, p.windows, C, p.R),
                    reinterpret_cast<cudaStream_t>(stream));
     return check_launch(name);
 }
@@ -674,8 +679,16 @@ extern "C" zs_status zs_forward(const float* coup, const float* rad,
                                 int64_t E, int32_t N, int32_t C, int32_t lmax,
                                 float* out, void* workspace, size_t workspace_bytes,
                                 zs_stream_t stream) {
-    return forward_impl("zs_forward", coup, rad, row_ptr, perm, E, N, C, lmax, NodeOut{out, nullptr, nullptr},
-                        workspace, workspace_bytes, stream);
+    return forward_impl("zs_forward", coup, ladder_rows(lmax), rad, row_ptr, perm, E, N, C, lmax,
+                        NodeOut{out, nullptr, nullptr}, workspace, workspace_bytes, stream);
+}
+
+extern "C" zs_status zs_forward_ld(const float* coup, int64_t coup_ld, const float* rad,
+                                   const int32_t* row_ptr, const int32_t* perm,
+                                   int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                   float* out, void* workspace, size_t workspace_bytes, zs_stream_t stream) {
+    return forward_impl("zs_forward_ld", coup, coup_ld, rad, row_ptr, perm, E, N, C, lmax,
+                        NodeOut{out, nullptr, nullptr}, workspace, workspace_bytes, stream);
 }
 
 extern "C" zs_status zs_forward_scaled(const float* coup, const float* rad,
@@ -684,7 +697,7 @@ extern "C" zs_status zs_forward_scaled(const float* coup, const float* rad,
                                        float* out, float* out_raw, void* workspace, size_t workspace_bytes,
                                        zs_stream_t stream) {
     if (N > 0 && !node_scale) return fail(ZS_ERR_INVALID_ARG, "zs_forward_scaled: node_scale is NULL");
-    return forward_impl("zs_forward_scaled", coup, rad, row_ptr, perm, E, N, C, lmax,
+    return forward_impl("zs_forward_scaled", coup, ladder_rows(lmax), rad, row_ptr, perm, E, N, C, lmax,
                         NodeOut{out, out_raw, node_scale}, workspace, workspace_bytes, stream);
 }
 
@@ -740,7 +753,7 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     if (N == 0) return ZS_OK;
     // the same split as zs_forward; the scratch holds one pair of partials per window
     const NodeOut o{out, nullptr, nullptr};
-    const FwdPlan p = fwd_plan(coup, rad, o, E, C, lmax);
+    const FwdPlan p = fwd_plan(rad, o, E, C, lmax);
     const size_t need = scratch_bytes(p.windows, C, p.R);
     if (need > kNoAllocScratchBytes)
         return fail(ZS_ERR_INVALID_ARG,
@@ -749,7 +762,7 @@ extern "C" zs_status zs_forward_noalloc(const float* coup, const float* rad,
     float* base = nullptr;
     const zs_status st = forward_scratch_address(&base);
     if (st != ZS_OK) return st;
-    launch_forward(p, coup, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(base, p.windows, C, p.R),
+    launch_forward(p, coup, ladder_rows(lmax), rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(base, p.windows, C, p.R),
                    reinterpret_cast<cudaStream_t>(stream));
     return check_launch("zs_forward_noalloc");
 }

@@ -6,8 +6,8 @@
 //     384 bytes, 16-byte aligned), completion counted in bytes on the
 //     stage's mbarrier, and
 //   - four or five 16-byte cp.async copies of the aligned span holding the
-//     coupling row coup[e] (60 bytes at byte offset 60e), completion signalled
-//     to the same mbarrier by cp.async.mbarrier.arrive.
+//     coupling row coup[e] (60 bytes, rows cld floats apart), completion
+//     signalled to the same mbarrier by cp.async.mbarrier.arrive.
 // Tiles are issued S - 1 ahead of the one being consumed, so a warp keeps
 // (S - 1) * T * ~450 bytes of HBM reads in flight without holding registers
 // for them.  A position whose perm entry is not a valid edge id gets zero
@@ -142,7 +142,9 @@ struct TileRing {
     }
 
     // Issue the next tile into its stage (its previous tile must be consumed).
-    __device__ __forceinline__ void issue(const int32_t* __restrict__ perm, const float* __restrict__ coup_g,
+    // Coupling row e starts at coup_g + e * cld (cld >= 15 floats, any 4-byte
+    // alignment): its span is copied from the 16-byte boundary at or before it.
+    __device__ __forceinline__ void issue(const int32_t* __restrict__ perm, const float* __restrict__ coup_g, int cld,
                                           const float* __restrict__ rad_g, int E, int lane) {
         if (issued >= ntiles) return;
         const int st = issued % S;
@@ -154,26 +156,27 @@ struct TileRing {
             blk_next = load_block(perm, issued / kPB + 1, lane);
         }
         const bool valid = lane < T && (uint32_t)e < (uint32_t)E;
+        const int64_t mis = (int64_t)(reinterpret_cast<uintptr_t>(coup_g) & 15u);   // bytes past a 16-byte boundary
         int64_t cstart = 0;
         int off = 0, nch = 0;
         bool tail = false;
         if (valid) {
-            const int64_t b0 = (int64_t)e * 60;
+            const int64_t b0 = mis + (int64_t)e * cld * 4;
             cstart = b0 & ~(int64_t)15;
             off = (int)(b0 - cstart) >> 2;          // 0..3
             nch = (off * 4 + 75) >> 4;              // 16-byte pieces covering the row: 4 or 5
-            tail = cstart + 16 * nch > (int64_t)E * 60;
+            tail = cstart + 16 * nch > mis + ((int64_t)(E - 1) * cld + 15) * 4;
         }
         const uint32_t bar = bar0 + 8 * st;
         float* cslot = coup + (st * T + lane) * kCoupSlotFloats;
         float* rslot = rad + (st * T + lane) * 96;
         if (lane < T) {
             if (!valid || tail) {
-                // rare: no edge here, or the span would run past the end of coup.
+                // rare: no edge here, or the span would run past the last row.
                 // Generic-proxy writes, ordered before the consumer by the
                 // syncwarps below and after the consumer's wait.
                 if (valid) {
-                    const float* src = coup_g + (int64_t)e * 15;
+                    const float* src = coup_g + (int64_t)e * cld;
 #pragma unroll
                     for (int r = 0; r < 15; ++r) cslot[r] = __ldg(src + r);
                 } else {
@@ -191,7 +194,7 @@ struct TileRing {
         if (valid) {
             bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * 96, kRadRowBytes, bar, pol);
             if (!tail) {
-                const char* src = reinterpret_cast<const char*>(coup_g) + cstart;
+                const char* src = reinterpret_cast<const char*>(coup_g) - mis + cstart;
                 const uint32_t dst = smem_u32(cslot);
                 cp_async16(dst, src, pol);
                 cp_async16(dst + 16, src + 16, pol);
@@ -213,10 +216,10 @@ struct TileRing {
     }
 
     // The last acquired tile is finished: reuse its stage for the next tile.
-    __device__ __forceinline__ void refill(const int32_t* __restrict__ perm, const float* __restrict__ coup_g,
+    __device__ __forceinline__ void refill(const int32_t* __restrict__ perm, const float* __restrict__ coup_g, int cld,
                                            const float* __restrict__ rad_g, int E, int lane) {
         __syncwarp();
-        issue(perm, coup_g, rad_g, E, lane);
+        issue(perm, coup_g, cld, rad_g, E, lane);
     }
 
     // Wait for every issued tile, so the ring's memory may be reused.

@@ -63,6 +63,10 @@ def load(build_if_missing: bool = True):
         lib.zs_forward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
         lib.zs_backward.restype = ctypes.c_int
         lib.zs_backward.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P]
+        lib.zs_forward_ld.restype = ctypes.c_int
+        lib.zs_forward_ld.argtypes = [P, I64, P, P, P, I64, I32, I32, I32, P, P, SZ, P]
+        lib.zs_backward_ld.restype = ctypes.c_int
+        lib.zs_backward_ld.argtypes = [P, P, I64, P, P, I64, I32, I32, I32, P, I64, P, P]
         lib.zs_forward_scaled.restype = ctypes.c_int
         lib.zs_forward_scaled.argtypes = [P, P, P, P, P, I64, I32, I32, I32, P, P, P, SZ, P]
         lib.zs_backward_scaled.restype = ctypes.c_int
@@ -117,6 +121,20 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _need_rows(t: torch.Tensor, name: str, shape: tuple) -> int:
+    """A float32 CUDA matrix whose rows are contiguous and evenly spaced (a
+    view into a wider array allowed): returns the row stride in elements."""
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be torch.float32, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.numel() and (t.stride(1) != 1 or (t.shape[0] > 1 and t.stride(0) < t.shape[1])):
+        raise ValueError(f"{name} must have contiguous rows (stride (ld, 1) with ld >= {t.shape[1]})")
+    return max(int(t.stride(0)), int(t.shape[1])) if t.shape[0] > 1 else int(t.shape[1])
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
@@ -185,6 +203,49 @@ def zs_forward(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, per
     _check("zs_forward", load().zs_forward(_ptr(coup), _ptr(rad), _ptr(row_ptr), _ptr(perm), E, N, C, lmax,
                                            _ptr(out), _ptr(workspace), wbytes, _stream(stream)))
     return out
+
+
+def zs_forward_ld(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,
+                  out=None, workspace=None, stream=None, lmax: int | None = None):
+    """zs_forward with coup a row-strided view (for example the m = 0 segment of a
+    packed (E, 3D-2) Wigner band): coup[e] = coup.data_ptr() + e * coup.stride(0)."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    ld = _need_rows(coup, "coup", (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
+    _need(row_ptr, "row_ptr", torch.int32, (N + 1,))
+    _need(perm, "perm", torch.int32, (E,))
+    out = torch.empty((N, D, C), dtype=torch.float32, device=dev) if out is None else out
+    _need(out, "out", torch.float32, (N, D, C))
+    if workspace is None:
+        workspace = _workspace(zs_forward_workspace_bytes(E, N, C, lmax), dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("zs_forward_ld", load().zs_forward_ld(_ptr(coup), ld, _ptr(rad), _ptr(row_ptr), _ptr(perm), E, N, C, lmax,
+                                                 _ptr(out), _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+def zs_backward_ld(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor, N: int,
+                   d_coup: torch.Tensor, d_rad=None, stream=None, lmax: int | None = None):
+    """zs_backward with coup and d_coup row-strided views (d_coup must be given)."""
+    lmax = _lmax(rad, lmax)
+    D, R = ladder(lmax)
+    E = coup.shape[0]
+    C = rad.shape[2]
+    dev = coup.device
+    _need(g, "g", torch.float32, (N, D, C))
+    ld = _need_rows(coup, "coup", (E, R))
+    dld = _need_rows(d_coup, "d_coup", (E, R))
+    _need(rad, "rad", torch.float32, (E, lmax, C))
+    _need(dst, "dst", torch.int32, (E,))
+    d_rad = torch.empty((E, lmax, C), dtype=torch.float32, device=dev) if d_rad is None else d_rad
+    _need(d_rad, "d_rad", torch.float32, (E, lmax, C))
+    _check("zs_backward_ld", load().zs_backward_ld(_ptr(g), _ptr(coup), ld, _ptr(rad), _ptr(dst), E, N, C, lmax,
+                                                   _ptr(d_coup), dld, _ptr(d_rad), _stream(stream)))
+    return d_coup, d_rad
 
 
 def zs_forward_scaled(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor,

@@ -144,6 +144,24 @@ ZS_API zs_status zs_forward(const float* coup, const float* rad,
                      zs_stream_t stream);
 
 /*
+ * zs_forward with coupling rows coup_ld floats apart (coup_ld >= D-1; row e
+ * at coup + e * coup_ld, any 4-byte alignment): for instance the m = 0
+ * segment of a packed Wigner band, read in place.  The banded storage of
+ * the pull request "banded Wigner-D storage for the fused inference
+ * consumers" keeps, per edge, three segments of the (E, 3*D-2) band, and
+ * the GIE zonal coupling reads its m = 0 segment (section "What"); the
+ * pages print no segment offsets, so the caller passes the pointer to the
+ * first zonal row (the degree-1 entries after the degree-0 one) and the
+ * band's row length, 3*D-2.  Results are bit-identical to zs_forward on the
+ * same values stored contiguously.  Other arguments as zs_forward;
+ * ZS_ERR_INVALID_ARG for coup_ld < D-1.
+ */
+ZS_API zs_status zs_forward_ld(const float* coup, int64_t coup_ld, const float* rad,
+                               const int32_t* row_ptr, const int32_t* perm,
+                               int64_t E, int32_t N, int32_t C, int32_t lmax,
+                               float* out, void* workspace, size_t workspace_bytes, zs_stream_t stream);
+
+/*
  * Forward with the degree normalisation fused in.  The pages apply an
  * inverse-square-root degree normalisation to the operator's output in the
  * traced graph, so that its own cotangent keeps flowing (pull request
@@ -196,6 +214,17 @@ ZS_API zs_status zs_backward_scaled(const float* g, const float* coup, const flo
 ZS_API zs_status zs_backward(const float* g, const float* coup, const float* rad,
                       const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
                       float* d_coup, float* d_rad, zs_stream_t stream);
+
+/*
+ * zs_backward with coupling rows coup_ld floats apart and coupling-gradient
+ * rows d_coup_ld floats apart (both >= D-1, any 4-byte alignment), so that
+ * both can live in a packed band's m = 0 segment (see zs_forward_ld); only
+ * the D-1 entries of each d_coup row are written.  Bit-identical to
+ * zs_backward on contiguous copies.
+ */
+ZS_API zs_status zs_backward_ld(const float* g, const float* coup, int64_t coup_ld, const float* rad,
+                                const int32_t* dst, int64_t E, int32_t N, int32_t C, int32_t lmax,
+                                float* d_coup, int64_t d_coup_ld, float* d_rad, zs_stream_t stream);
 
 /*
  * Backward of the zonal scatter with the edges visited in destination (CSR)
