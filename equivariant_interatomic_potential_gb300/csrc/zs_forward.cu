@@ -192,19 +192,144 @@ __device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, f
     }
 }
 
-// C == 32 forward with TMA-fed warps.  W warps per CTA, one CTA per SM; warp
-// gw owns the window [gw*KW, gw*KW + KW) of CSR positions and walks it in
-// position order, closing a node when its last position is reached.
-template <int W, int S, int T>
+// Lane layouts of the single-wave forward at C = 32.  A layout owns the
+// per-lane accumulator of one node and knows how to add an edge from the
+// ring, finish a node and move partial sums.
+//
+// QuadLayout (lmax = 3): group g = lane/8 owns zonal rows 4g..4g+3 (row 15 is
+// padding), quad q = lane%8 channels 4q..4q+3: per edge 2 LDS.128 + 4 LDS.32
+// + 16 FFMA per lane.
+struct QuadLayout {
+    static constexpr int kRadFloats = 3 * kC32, kCoupRow = kRows, kPartFloats = kPartFloats32;
+    static constexpr int kSlot = coup_slot_floats(kCoupRow);
+    struct Acc {
+        float4 v[4];
+    };
+    Lane32 L;
+    const float *rb, *hb, *cb;
+    __device__ __forceinline__ explicit QuadLayout(int lane) : L(lane) {}
+    template <class Ring>
+    __device__ __forceinline__ void bind(const Ring& ring) {
+        rb = ring.rad + L.slo * kC32 + 4 * L.q;
+        hb = ring.rad + L.shi * kC32 + 4 * L.q;
+        cb = ring.coup + 4 * L.g;
+    }
+    template <int T>
+    __device__ __forceinline__ TileView view(int st, const int2* meta) const {
+        return TileView{rb + st * T * kRadFloats, hb + st * T * kRadFloats, cb + st * T * kSlot, meta + st * T};
+    }
+    __device__ __forceinline__ static void zero(Acc& a) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a.v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ __forceinline__ void add(const TileView& v, int j, Acc& a) const { add_edge32(v, j, a.v); }
+    __device__ __forceinline__ void put(const NodeOut& o, int n, const Acc& a) const { put_node32(o, n, a.v, L); }
+    __device__ __forceinline__ void zero_node(const NodeOut& o, int n) const { zero_put32(o, n, L.lane); }
+    __device__ __forceinline__ void store(float* p, const Acc& a) const { store_part32(p, a.v, L); }
+    __device__ __forceinline__ void load(const float* p, Acc& a) const { load_part32(p, a.v, L); }
+    __device__ __forceinline__ void load_cg(const float* p, Acc& a) const { load_part32_cg(p, a.v, L); }
+    __device__ __forceinline__ static void add_to(Acc& a, const Acc& b) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a.v[i] = f4_add(a.v[i], b.v[i]);
+    }
+};
+
+// ChanLayout (any ladder): lane = channel, all R rows per lane; per edge
+// lmax LDS.32 of radial values, R broadcast LDS.32 of coupling values and R
+// FFMA per lane.  Node rows are written as 128-byte lines.
+template <int LM>
+struct ChanLayout {
+    static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
+    static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
+    static constexpr int kSlot = coup_slot_floats(kCoupRow);
+    struct Acc {
+        float v[R];
+    };
+    struct View {
+        const float* ra;    // radial row of edge 0 of the stage, at this lane's channel
+        const float* cp;    // coupling span of edge 0 of the stage
+        const int2* mt;
+    };
+    int lane;
+    const float *rb, *cb;
+    __device__ __forceinline__ explicit ChanLayout(int l) : lane(l) {}
+    template <class Ring>
+    __device__ __forceinline__ void bind(const Ring& ring) {
+        rb = ring.rad + lane;
+        cb = ring.coup;
+    }
+    template <int T>
+    __device__ __forceinline__ View view(int st, const int2* meta) const {
+        return View{rb + st * T * kRadFloats, cb + st * T * kSlot, meta + st * T};
+    }
+    __device__ __forceinline__ static void zero(Acc& a) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = 0.f;
+    }
+    __device__ __forceinline__ void add(const View& v, int j, Acc& a) const {
+        const float* cr = v.cp + j * kSlot + v.mt[j].y;
+        float rv[LM];
+#pragma unroll
+        for (int k = 0; k < LM; ++k) rv[k] = v.ra[j * kRadFloats + k * kC32];
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = fmaf(cr[r], rv[ladder_slot(r)], a.v[r]);
+    }
+    __device__ __forceinline__ void put(const NodeOut& o, int n, const Acc& a) const {
+        const int64_t at = (int64_t)n * kNodeFloats + lane;
+        const float sc = o.scale ? __ldg(o.scale + n) : 1.f;
+        o.out[at] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) o.out[at + (1 + r) * kC32] = o.scale ? a.v[r] * sc : a.v[r];
+        if (o.raw) {
+            o.raw[at] = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) o.raw[at + (1 + r) * kC32] = a.v[r];
+        }
+    }
+    __device__ __forceinline__ void zero_node(const NodeOut& o, int n) const {
+#pragma unroll
+        for (int i = 0; i < D; ++i) o.out[(int64_t)n * kNodeFloats + i * kC32 + lane] = 0.f;
+        if (o.raw)
+#pragma unroll
+            for (int i = 0; i < D; ++i) o.raw[(int64_t)n * kNodeFloats + i * kC32 + lane] = 0.f;
+    }
+    __device__ __forceinline__ void store(float* p, const Acc& a) const {
+#pragma unroll
+        for (int r = 0; r < R; ++r) p[r * kC32 + lane] = a.v[r];
+    }
+    __device__ __forceinline__ void load(const float* p, Acc& a) const {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = p[r * kC32 + lane];
+    }
+    __device__ __forceinline__ void load_cg(const float* p, Acc& a) const {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = __ldcg(p + r * kC32 + lane);
+    }
+    __device__ __forceinline__ static void add_to(Acc& a, const Acc& b) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] += b.v[r];
+    }
+};
+
+// Single-wave forward at C = 32, fed by TMA rings.  W warps per CTA, one CTA
+// per SM; warp gw owns the window [gw*KW, gw*KW + KW) of CSR positions and
+// walks it in position order, closing a node when its last position is
+// reached; P is the lane layout.
+template <int W, int S, int T, class P>
 __global__ void __launch_bounds__(W * 32, 1)
-fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
-            const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-            int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
-            uint64_t* __restrict__ flags, uint64_t salt) {
+fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
+        const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+        int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
+        uint64_t* __restrict__ flags, uint64_t salt) {
+    using Ring = TileRing<S, T, false, P::kRadFloats, P::kCoupRow>;
+    using Layout = typename Ring::Layout;
+    using Acc = typename P::Acc;
+    static_assert(2 * P::kPartFloats * 4 <= Layout::kRad + Layout::kCoup, "two partials fit a warp's idle ring");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
     const int warp = threadIdx.x >> 5;
-    const Lane32 L(threadIdx.x & 31);
+    const int lane = threadIdx.x & 31;
+    P lay(lane);
     const int gw = blockIdx.x * W + warp;
     const bool active = gw < Wtot;
     pdl_wait();
@@ -214,17 +339,20 @@ fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ r
     const bool is_last = gw == Wtot - 1;
     const int vend = __ldg(row_ptr + N);              // positions from vend on hold no node
     const int pe = imax(p0, imin(p1, vend));
-    TileRing<S, T> ring;
-    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, active ? pe : p0, L.lane);
-    if (L.lane < 2) sp_node[warp][L.lane] = -1;
+    Ring ring;
+    ring.init(smem + (size_t)warp * Layout::kBytes, p0, active ? pe : p0, lane);
+    lay.bind(ring);
+    if (lane < 2) sp_node[warp][lane] = -1;
     __syncwarp();
 
-    float4 acc0[4] = {}, acc[4] = {};
+    Acc acc0, acc;
+    P::zero(acc0);
+    P::zero(acc);
     bool have0 = false, have1 = false;
     if (active) {
-        ring.prefetch_perm(perm, L.lane);
+        ring.prefetch_perm(perm, lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, cld, rad, E, L.lane);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, cld, rad, E, lane);
         // current node n covers positions [a, b); empty nodes this window owns
         // (those starting in it, or all trailing ones for the last window) are zeroed
         // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead
@@ -240,18 +368,14 @@ fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ r
         };
         auto advance = [&]() {
             while (n < N && a == b && (a < p1 || is_last)) {
-                zero_put32(o, n, L.lane);
+                lay.zero_node(o, n);
                 step();
             }
         };
         advance();
-        const float* rbase = ring.rad + L.slo * kC32 + 4 * L.q;
-        const float* hbase = ring.rad + L.shi * kC32 + 4 * L.q;
-        const float* cbase = ring.coup + 4 * L.g;
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
-            const TileView v{rbase + st * T * 96, hbase + st * T * 96, cbase + st * T * kCoupSlotFloats,
-                             ring.meta + st * T};
+            const auto v = lay.template view<T>(st, ring.meta);
             const int tb = p0 + k * T;
             const int jt = imin(T, pe - tb);
             int j = 0;
@@ -259,47 +383,44 @@ fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ r
                 const int stop = imin(b - tb, jt);   // the current node covers position tb + j
                 if (j == 0 && stop == T) {
 #pragma unroll
-                    for (int jj = 0; jj < T; ++jj) add_edge32(v, jj, acc);
+                    for (int jj = 0; jj < T; ++jj) lay.add(v, jj, acc);
                 } else {
 #pragma unroll 4
-                    for (int jj = j; jj < stop; ++jj) add_edge32(v, jj, acc);
+                    for (int jj = j; jj < stop; ++jj) lay.add(v, jj, acc);
                 }
                 j = stop;
                 if (tb + j == b) {                   // node n ends inside this window
                     if (a >= p0) {
-                        put_node32(o, n, acc, L);
+                        lay.put(o, n, acc);
                     } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
+                        acc0 = acc;
                         have0 = true;
-                        if (L.lane == 0) sp_node[warp][0] = n;
+                        if (lane == 0) sp_node[warp][0] = n;
                     }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    P::zero(acc);
                     step();
                     advance();
                 }
             }
-            ring.refill(perm, coup, cld, rad, E, L.lane);
+            ring.refill(perm, coup, cld, rad, E, lane);
         }
         // a node still open at the end runs past p1
         if (n < N && a < pe && b > pe) {
             if (a < p0) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc0[i] = acc[i];
+                acc0 = acc;
                 have0 = true;
-                if (L.lane == 0) sp_node[warp][0] = n;
+                if (lane == 0) sp_node[warp][0] = n;
             } else {
                 have1 = true;
-                if (L.lane == 0) sp_node[warp][1] = n;
+                if (lane == 0) sp_node[warp][1] = n;
             }
         }
     }
     ring.drain();
-    // The ring is idle: its radial area holds this warp's two partials.
+    // The ring is idle: its first bytes hold this warp's two partials.
     float* part = ring.rad;
-    if (have0) store_part32(part, acc0, L);
-    if (have1) store_part32(part + kPartFloats32, acc, L);
+    if (have0) lay.store(part, acc0);
+    if (have1) lay.store(part + P::kPartFloats, acc);
     __syncthreads();
 
     // Combine the warp pieces of nodes cut by window edges inside this CTA:
@@ -308,30 +429,28 @@ fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ r
     const int64_t P0 = imin<int64_t>((int64_t)blockIdx.x * span, E);
     const int64_t P1 = imin<int64_t>(P0 + span, E);
     int pend_node = -1;                      // a node that started in an earlier CTA and ends here
-    float4 pend[4];
+    Acc pend;
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot) {
         const int m = sp_node[warp][slot];
         if (m < 0) continue;
         if (warp > 0 && (sp_node[warp - 1][0] == m || sp_node[warp - 1][1] == m)) continue;
-        float4 sum[4];
-        load_part32(part + slot * kPartFloats32, sum, L);
+        Acc sum;
+        lay.load(part + slot * P::kPartFloats, sum);
         for (int w2 = warp + 1; w2 < W && sp_node[w2][0] == m; ++w2) {
-            float4 t4[4];
-            load_part32(reinterpret_cast<const float*>(smem + (size_t)w2 * RingLayout<S, T>::kBytes), t4, L);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) sum[i] = f4_add(sum[i], t4[i]);
+            Acc t;
+            lay.load(reinterpret_cast<const float*>(smem + (size_t)w2 * Layout::kBytes), t);
+            P::add_to(sum, t);
         }
         const int ma = __ldg(row_ptr + m), mb = __ldg(row_ptr + m + 1);
         if (ma >= P0 && mb <= P1) {
-            put_node32(o, m, sum, L);
+            lay.put(o, m, sum);
         } else if (ma < P0 && mb <= P1) {
             pend_node = m;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pend[i] = sum[i];
+            pend = sum;
         } else {
             // slot 1: starts here and runs past this CTA; slot 0: covers all of it
-            store_part32(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * kPartFloats32, sum, L);
+            lay.store(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * P::kPartFloats, sum);
         }
     }
     // publish this CTA's partials: every writer fences, then one release store
@@ -343,20 +462,18 @@ fwd_c32_tma(const float* __restrict__ coup, int cld, const float* __restrict__ r
     // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
     // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
     const int b0 = (int)(__ldg(row_ptr + pend_node) / span);
-    if (L.lane == 0)
+    if (lane == 0)
         for (int k = b0; k < (int)blockIdx.x; ++k) wait_flag(flags, k, tag);
     __syncwarp();
-    float4 total[4];
-    load_part32_cg(cta_part + ((int64_t)b0 * 2 + 1) * kPartFloats32, total, L);
+    Acc total;
+    lay.load_cg(cta_part + ((int64_t)b0 * 2 + 1) * P::kPartFloats, total);
     for (int k = b0 + 1; k < (int)blockIdx.x; ++k) {
-        float4 t4[4];
-        load_part32_cg(cta_part + (int64_t)k * 2 * kPartFloats32, t4, L);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) total[i] = f4_add(total[i], t4[i]);
+        Acc t;
+        lay.load_cg(cta_part + (int64_t)k * 2 * P::kPartFloats, t);
+        P::add_to(total, t);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) total[i] = f4_add(total[i], pend[i]);
-    put_node32(o, pend_node, total, L);
+    P::add_to(total, pend);
+    lay.put(o, pend_node, total);
 }
 
 // --------------------------------------------------------------------------
@@ -574,11 +691,30 @@ static uint64_t next_salt() {
     return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
 }
 
-// How zs_forward splits a call: the C == 32 single-wave kernel (lmax 3,
-// 16-byte aligned operands) or the per-channel kernel and its fix-up.
+// Warps per CTA of the single-wave forward for a lane layout: 16, or as many
+// rings as one SM's shared memory holds.
+template <class P>
+constexpr int tma_warps() {
+    constexpr int bytes = RingLayout<kTmaStages, kTile, P::kRadFloats, P::kCoupRow>::kBytes;
+    return (232448 / bytes) < kTmaWarps ? (232448 / bytes) : kTmaWarps;
+}
+
+static int tma_warps_for(int lmax) {
+    switch (lmax) {
+        case 1: return tma_warps<ChanLayout<1>>();
+        case 2: return tma_warps<ChanLayout<2>>();
+        case 3: return tma_warps<QuadLayout>();
+        case 4: return tma_warps<ChanLayout<4>>();
+        default: return tma_warps<ChanLayout<5>>();
+    }
+}
+
+// How zs_forward splits a call: the single-wave C == 32 kernel (16-byte
+// aligned radial rows; at lmax 3 also 16-byte aligned outputs for the quad
+// layout's vector stores) or the per-channel kernel and its fix-up.
 struct FwdPlan {
     bool fast;
-    int R;
+    int R, W;
     int64_t KW, Wtot, ctas, windows;
 };
 
@@ -587,16 +723,19 @@ static FwdPlan fwd_plan(const float* rad, const NodeOut& o, int64_t E, int C, in
     p.R = ladder_rows(lmax);
     // the coupling rows may have any 4-byte alignment and stride: the ring
     // copies each one's 16-byte-aligned span
-    p.fast = lmax == 3 && C == kC32 && aligned16(rad) && aligned16(o.out) && (o.raw == nullptr || aligned16(o.raw));
+    p.fast = C == kC32 && aligned16(rad) &&
+             (lmax != 3 || (aligned16(o.out) && (o.raw == nullptr || aligned16(o.raw))));
     if (p.fast) {
-        // Balanced single wave: one CTA of kTmaWarps warps per SM, every warp
-        // the same number of CSR positions (at least one tile).
-        const int64_t warps_max = (int64_t)num_sms() * kTmaWarps;
+        // Balanced single wave: one CTA of W warps per SM, every warp the same
+        // number of CSR positions (at least one tile).
+        p.W = tma_warps_for(lmax);
+        const int64_t warps_max = (int64_t)num_sms() * p.W;
         p.KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
         p.Wtot = imax<int64_t>(ceil_div(E, p.KW), 1);
-        p.ctas = ceil_div(p.Wtot, kTmaWarps);
+        p.ctas = ceil_div(p.Wtot, p.W);
         p.windows = p.ctas;
     } else {
+        p.W = kFwdWarps;
         p.Wtot = ceil_div(E > 0 ? E : 1, kGenWin);
         p.ctas = ceil_div(p.Wtot, kFwdWarps);
         p.windows = p.Wtot;
@@ -614,15 +753,30 @@ static void launch_gen(const FwdPlan& p, const float* coup, int cld, const float
            kGenWin, (const float*)sc.part, o);
 }
 
+template <class P>
+static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
+                       cudaStream_t s) {
+    constexpr int W = tma_warps<P>();
+    auto kernel = fwd_tma<W, kTmaStages, kTile, P>;
+    const int smem = W * RingLayout<kTmaStages, kTile, P::kRadFloats, P::kCoupRow>::kBytes;
+    static std::atomic<bool> attr_done[kMaxDevices];
+    set_smem_limit_once(kernel, smem, attr_done);
+    launch(kernel, (unsigned)p.ctas, W * 32, smem, s, coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW,
+           (int)p.Wtot, o, sc.part, sc.flags, next_salt());
+}
+
 static void launch_forward(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
                            const int32_t* perm, int64_t E, int32_t N, int C, int lmax, const NodeOut& o,
                            const Scratch& sc, cudaStream_t s) {
     if (p.fast) {
-        const int smem = kTmaWarps * RingLayout<kTmaStages, kTile>::kBytes;
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, smem, attr_done);
-        launch(fwd_c32_tma<kTmaWarps, kTmaStages, kTile>, (unsigned)p.ctas, kTmaWarps * 32, smem, s,
-               coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW, (int)p.Wtot, o, sc.part, sc.flags, next_salt());
+        switch (lmax) {
+            case 1: launch_tma<ChanLayout<1>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+            case 2: launch_tma<ChanLayout<2>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+            case 3: launch_tma<QuadLayout>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+            case 4: launch_tma<ChanLayout<4>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+            default: launch_tma<ChanLayout<5>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+        }
         return;
     }
     switch (lmax) {
@@ -638,8 +792,8 @@ extern "C" size_t zs_forward_workspace_bytes_lmax(int64_t E, int32_t N, int32_t 
     if (E < 0 || N < 0 || C < 1 || lmax < 1 || lmax > kMaxLmax) return 0;
     (void)N;
     // Sized for the smaller of the two window lengths: kGenWin positions per
-    // warp on the per-channel path, at least kTmaWarps * kTile per CTA on the
-    // C == 32 path (lmax 3 only).
+    // warp on the per-channel path, at least W * kTile per CTA (W >= 8 warps)
+    // on the single-wave C == 32 path.
     const int64_t win = lmax == 3 ? imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile) : kGenWin;
     const int64_t windows = ceil_div(E > 0 ? E : 1, win) + 1;
     return scratch_bytes(windows, C, ladder_rows(lmax));

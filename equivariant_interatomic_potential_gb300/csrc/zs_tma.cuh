@@ -86,23 +86,36 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
 }
 
-// Shared-memory layout of one warp's ring of S stages of T edges.
-template <int S, int T>
+// Coupling slot of a ring: the widest 16-byte-aligned span of a row of
+// CoupRow floats that starts at any 4-byte offset, in floats (20 for the
+// 15-row ladder), and the 16-byte pieces that span can take.
+__host__ __device__ constexpr int coup_slot_floats(int coup_row) { return (coup_row + 3 + 3) / 4 * 4; }
+__host__ __device__ constexpr int coup_max_chunks(int coup_row) { return (12 + 4 * coup_row + 15) / 16; }
+
+// Shared-memory layout of one warp's ring of S stages of T edges, each edge
+// a radial row of RadFloats floats and a coupling row of CoupRow floats
+// (defaults: the lmax = 3 ladder at C = 32).
+template <int S, int T, int RadFloats = 96, int CoupRow = 15>
 struct RingLayout {
-    static constexpr int kRad = S * T * kRadRowBytes;              // radial rows
-    static constexpr int kCoup = S * T * kCoupSlotFloats * 4;      // coupling spans
-    static constexpr int kMeta = S * T * 8;                        // (edge id, coupling offset)
+    static constexpr int kRad = S * T * RadFloats * 4;                      // radial rows
+    static constexpr int kCoup = S * T * coup_slot_floats(CoupRow) * 4;     // coupling spans
+    static constexpr int kMeta = S * T * 8;                                 // (edge id, coupling offset)
     static constexpr int kBars = S * 8;
     static constexpr int kBytes = (kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
 };
 
 // One warp's stream of tiles over [p0, pe).  kEvictFirst marks every byte
 // the ring brings in as evict-first in L2 (it is read exactly once).
-template <int S, int T, bool kEvictFirst = false>
+template <int S, int T, bool kEvictFirst = false, int RadFloats = 96, int CoupRow = 15>
 struct TileRing {
     static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
-    float* rad;        // [S][T][96]
-    float* coup;       // [S][T][20]
+    static_assert(RadFloats % 4 == 0, "radial rows are whole 16-byte pieces");
+    using Layout = RingLayout<S, T, RadFloats, CoupRow>;
+    static constexpr int kSlot = coup_slot_floats(CoupRow);
+    static constexpr int kChunks = coup_max_chunks(CoupRow);
+    static constexpr uint32_t kRadBytes = RadFloats * 4;
+    float* rad;        // [S][T][RadFloats]
+    float* coup;       // [S][T][kSlot]
     int2* meta;        // [S][T]: x = edge id (-1 if none), y = float offset of the row in its span
     uint32_t bar0;     // shared address of the first mbarrier
     int p0, pe;
@@ -117,9 +130,9 @@ struct TileRing {
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int pe_, int lane) {
         rad = reinterpret_cast<float*>(base);
-        coup = reinterpret_cast<float*>(base + RingLayout<S, T>::kRad);
-        meta = reinterpret_cast<int2*>(base + RingLayout<S, T>::kRad + RingLayout<S, T>::kCoup);
-        bar0 = smem_u32(base + RingLayout<S, T>::kRad + RingLayout<S, T>::kCoup + RingLayout<S, T>::kMeta);
+        coup = reinterpret_cast<float*>(base + Layout::kRad);
+        meta = reinterpret_cast<int2*>(base + Layout::kRad + Layout::kCoup);
+        bar0 = smem_u32(base + Layout::kRad + Layout::kCoup + Layout::kMeta);
         p0 = p0_;
         pe = pe_;
         ntiles = pe > p0 ? (pe - p0 + T - 1) / T : 0;
@@ -164,12 +177,12 @@ struct TileRing {
             const int64_t b0 = mis + (int64_t)e * cld * 4;
             cstart = b0 & ~(int64_t)15;
             off = (int)(b0 - cstart) >> 2;          // 0..3
-            nch = (off * 4 + 75) >> 4;              // 16-byte pieces covering the row: 4 or 5
-            tail = cstart + 16 * nch > mis + ((int64_t)(E - 1) * cld + 15) * 4;
+            nch = (off * 4 + 4 * CoupRow + 15) >> 4;   // 16-byte pieces covering the row
+            tail = cstart + 16 * nch > mis + ((int64_t)(E - 1) * cld + CoupRow) * 4;
         }
         const uint32_t bar = bar0 + 8 * st;
-        float* cslot = coup + (st * T + lane) * kCoupSlotFloats;
-        float* rslot = rad + (st * T + lane) * 96;
+        float* cslot = coup + (st * T + lane) * kSlot;
+        float* rslot = rad + (st * T + lane) * RadFloats;
         if (lane < T) {
             if (!valid || tail) {
                 // rare: no edge here, or the span would run past the last row.
@@ -178,10 +191,10 @@ struct TileRing {
                 if (valid) {
                     const float* src = coup_g + (int64_t)e * cld;
 #pragma unroll
-                    for (int r = 0; r < 15; ++r) cslot[r] = __ldg(src + r);
+                    for (int r = 0; r < CoupRow; ++r) cslot[r] = __ldg(src + r);
                 } else {
-                    for (int r = 0; r < kCoupSlotFloats; ++r) cslot[r] = 0.f;
-                    for (int c = 0; c < 96; ++c) rslot[c] = 0.f;
+                    for (int r = 0; r < kSlot; ++r) cslot[r] = 0.f;
+                    for (int c = 0; c < RadFloats; ++c) rslot[c] = 0.f;
                 }
                 off = 0;
             }
@@ -189,18 +202,16 @@ struct TileRing {
         }
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadRowBytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadBytes);
         __syncwarp();
         if (valid) {
-            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * 96, kRadRowBytes, bar, pol);
+            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * RadFloats, kRadBytes, bar, pol);
             if (!tail) {
                 const char* src = reinterpret_cast<const char*>(coup_g) - mis + cstart;
                 const uint32_t dst = smem_u32(cslot);
-                cp_async16(dst, src, pol);
-                cp_async16(dst + 16, src + 16, pol);
-                cp_async16(dst + 32, src + 32, pol);
-                cp_async16(dst + 48, src + 48, pol);
-                if (nch == 5) cp_async16(dst + 64, src + 64, pol);
+#pragma unroll
+                for (int k = 0; k < kChunks; ++k)
+                    if (k < nch) cp_async16(dst + 16 * k, src + 16 * k, pol);
             }
         }
         cp_async_arrive(bar);
