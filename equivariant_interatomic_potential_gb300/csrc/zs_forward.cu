@@ -699,6 +699,10 @@ constexpr int tma_warps() {
     return (232448 / bytes) < kTmaWarps ? (232448 / bytes) : kTmaWarps;
 }
 
+constexpr int kMinTmaSpan = imin(imin(tma_warps<ChanLayout<1>>(), tma_warps<ChanLayout<2>>()),
+                                  imin(imin(tma_warps<QuadLayout>(), tma_warps<ChanLayout<4>>()),
+                                       tma_warps<ChanLayout<5>>())) * kTile;
+
 static int tma_warps_for(int lmax) {
     switch (lmax) {
         case 1: return tma_warps<ChanLayout<1>>();
@@ -792,9 +796,10 @@ extern "C" size_t zs_forward_workspace_bytes_lmax(int64_t E, int32_t N, int32_t 
     if (E < 0 || N < 0 || C < 1 || lmax < 1 || lmax > kMaxLmax) return 0;
     (void)N;
     // Sized for the smaller of the two window lengths: kGenWin positions per
-    // warp on the per-channel path, at least W * kTile per CTA (W >= 8 warps)
-    // on the single-wave C == 32 path.
-    const int64_t win = lmax == 3 ? imin<int64_t>(kGenWin, (int64_t)kTmaWarps * kTile) : kGenWin;
+    // warp on the per-channel path, at least W * kTile per CTA on the
+    // single-wave C == 32 path (every layout's W * kTile is at least
+    // kMinTmaSpan).
+    const int64_t win = imin<int64_t>(kGenWin, kMinTmaSpan);
     const int64_t windows = ceil_div(E > 0 ? E : 1, win) + 1;
     return scratch_bytes(windows, C, ladder_rows(lmax));
 }
@@ -823,6 +828,9 @@ static zs_status forward_impl(const char* name, const float* coup, int64_t cld, 
         return fail(ZS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
     if (N == 0) return ZS_OK;
     const FwdPlan p = fwd_plan(rad, o, E, C, lmax);
+    if (scratch_bytes(p.windows, C, p.R) > workspace_bytes)   // the plan never outgrows the query's size
+        return fail(ZS_ERR_INVALID_ARG, "%s: plan needs %zu bytes of workspace, %zu given", name,
+                    scratch_bytes(p.windows, C, p.R), workspace_bytes);
     launch_forward(p, coup, (int)cld, rad, row_ptr, perm, E, N, C, lmax, o, scratch_at(workspace, p.windows, C, p.R),
                    reinterpret_cast<cudaStream_t>(stream));
     return check_launch(name);

@@ -143,10 +143,10 @@ def test_workspace_sizes(lib):
     assert lib.zs_forward_workspace_bytes(E, 4096, 32) == ws(E, 32)
     assert lib.zs_forward_workspace_bytes(0, 4096, 32) == ws(0, 32)
     assert lib.zs_forward_workspace_bytes(1000, 10, 40) == ws(1000, 40)
-    # other ladders: per window of 256 positions (plus one), a pair of R x C
-    # partials (R = (lmax+1)^2 - 1), one crossing-node entry and one flag
+    # other ladders: the same windows, a pair of R x C partials (R = (lmax+1)^2 - 1),
+    # one crossing-node entry and one flag each
     def ws_l(E, C, lmax):
-        w = -(-max(E, 1) // 256) + 1
+        w = -(-max(E, 1) // 128) + 1
         R = (lmax + 1) ** 2 - 1
         return -(-(w * 2 * R * C * 4) // 256) * 256 + -(-(w * 4) // 256) * 256 + -(-(w * 8) // 256) * 256
     for lmax in (1, 2, 4, 5):

@@ -62,3 +62,20 @@ def test_ladder_autograd():
     dc, dr, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
     assert_close(d_coup.cpu().numpy(), dc, adc, "d_coup")
     assert_close(d_rad.cpu().numpy(), dr, adr, "d_rad")
+
+
+@pytest.mark.parametrize("lmax", [1, 2, 3, 4, 5])
+def test_forward_stays_inside_its_workspace(lmax):
+    # the workspace query's size is enough for every plan, and nothing is written past it
+    for E in (1, 100, 5000, 20000, 300000):
+        w = workloads.make_random(50, E, 32, seed=E + lmax, lmax=lmax)
+        need = zs.zs_forward_workspace_bytes(E, 50, 32, lmax)
+        buf = torch.full((need + 8192,), 0xAB, dtype=torch.uint8, device="cuda")
+        coup, rad, dst = dev(w.coup), dev(w.rad), dev(w.dst)
+        row_ptr, perm, _ = zs.zs_build_csr(dst, w.N)
+        out = zs.zs_forward(coup, rad, row_ptr, perm, w.N, workspace=buf[:need])
+        torch.cuda.synchronize()
+        assert torch.all(buf[need:] == 0xAB), (lmax, E)
+        rp, pm, _ = oracle.build_csr(w.dst, w.N)
+        ref, absum = oracle.forward(w.coup, w.rad, rp, pm, w.N)
+        assert_close(out.cpu().numpy(), ref, absum, f"forward lmax {lmax} E {E}")
