@@ -290,23 +290,29 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
 // the CSR-order kernel: one edge per 8-lane group, all 15 rows per lane.
 // --------------------------------------------------------------------------
 
-template <int S, int T>
+// Per edge: the destination's cotangent rows 1..R (R x 32 floats), the
+// radial row (LM x 32) and the coupling row (R), for the ladder of degree LM.
+template <int S, int T, int LM = 3>
 struct EdgeRingLayout {
-    static constexpr int kG = S * T * 15 * kC32 * 4;   // cotangent rows 1..15 per edge
-    static constexpr int kRad = S * T * 3 * kC32 * 4;
-    static constexpr int kCoup = S * T * 15 * 4;
+    static constexpr int R = Ladder<LM>::R;
+    static constexpr int kG = S * T * R * kC32 * 4;   // cotangent rows 1..R per edge
+    static constexpr int kRad = S * T * LM * kC32 * 4;
+    static constexpr int kCoup = S * T * R * 4;
     static constexpr int kMeta = S * T * 4;
     static constexpr int kBars = S * 8;
     static constexpr int kBytes = (kG + kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
 };
-
-template <int S, int T>
+template <int S, int T, int LM = 3>
 struct EdgeRing {
-    static_assert(T % 4 == 0 && 32 % T == 0, "tiles of whole quads that divide 32");
+    static_assert(32 % T == 0 && (LM != 3 || T % 4 == 0), "tiles divide 32 (whole quads at lmax 3)");
+    using Layout = EdgeRingLayout<S, T, LM>;
+    static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
+    static constexpr int RF = LM * kC32;                    // radial floats per edge
+    static constexpr uint32_t kGBytes = R * kC32 * 4;       // cotangent bytes per edge
     static constexpr int kPB = 32 / T;
-    float* gs;      // [S][T][15*32]
-    float* rads;    // [S][T][96]
-    float* coups;   // [S][T*15]
+    float* gs;      // [S][T][R*32]
+    float* rads;    // [S][T][LM*32]
+    float* coups;   // [S][T*R]
     int* meta;      // [S][T]: destination, -1 for an edge without a node, -2 past the window
     uint32_t bar0;
     int p0, p1, ntiles, issued, consumed;
@@ -315,12 +321,10 @@ struct EdgeRing {
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int p1_, int lane) {
         gs = reinterpret_cast<float*>(base);
-        rads = reinterpret_cast<float*>(base + EdgeRingLayout<S, T>::kG);
-        coups = reinterpret_cast<float*>(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad);
-        meta = reinterpret_cast<int*>(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad +
-                                      EdgeRingLayout<S, T>::kCoup);
-        bar0 = smem_u32(base + EdgeRingLayout<S, T>::kG + EdgeRingLayout<S, T>::kRad + EdgeRingLayout<S, T>::kCoup +
-                        EdgeRingLayout<S, T>::kMeta);
+        rads = reinterpret_cast<float*>(base + Layout::kG);
+        coups = reinterpret_cast<float*>(base + Layout::kG + Layout::kRad);
+        meta = reinterpret_cast<int*>(base + Layout::kG + Layout::kRad + Layout::kCoup);
+        bar0 = smem_u32(base + Layout::kG + Layout::kRad + Layout::kCoup + Layout::kMeta);
         p0 = p0_;
         p1 = p1_;
         ntiles = p1 > p0 ? (p1 - p0 + T - 1) / T : 0;
@@ -344,7 +348,7 @@ struct EdgeRing {
     }
 
     // Coupling rows are cld floats apart; coup_bulk says they are packed
-    // (cld == 15) from a 16-byte boundary, so a whole tile is one bulk copy.
+    // (cld == R) from a 16-byte boundary, so a whole tile is one bulk copy.
     __device__ __forceinline__ void issue(const int32_t* __restrict__ dst, const float* __restrict__ coup_g, int cld,
                                           bool coup_bulk, const float* __restrict__ rad_g,
                                           const float* __restrict__ g_g, int N, int lane) {
@@ -362,26 +366,27 @@ struct EdgeRing {
         const int cnt = imin(T, p1 - e0);
         const bool in = lane < cnt;
         const bool valid = in && d >= 0 && d < N;
-        const bool full = cnt == T && coup_bulk;
+        const bool full = cnt == T && coup_bulk && (T * R) % 4 == 0;
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-        const uint32_t bytes = (uint32_t)cnt * 384u + (full ? (uint32_t)T * 60u : 0u) + nvalid * 1920u;
+        const uint32_t bytes = (uint32_t)cnt * (RF * 4u) + (full ? (uint32_t)T * R * 4u : 0u) + nvalid * kGBytes;
         const uint32_t bar = bar0 + 8 * st;
-        float* cst = coups + st * T * 15;
+        float* cst = coups + st * T * R;
         if (lane < T) meta[st * T + lane] = valid ? d : (in ? -1 : -2);
         if (!full && in) {   // ragged last tile, or rows not packed: plain loads of each row
             const float* src = coup_g + (int64_t)(e0 + lane) * cld;
 #pragma unroll
-            for (int r = 0; r < 15; ++r) cst[lane * 15 + r] = __ldg(src + r);
+            for (int r = 0; r < R; ++r) cst[lane * R + r] = __ldg(src + r);
         }
         __syncwarp();
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(smem_u32(rads + st * T * 96), rad_g + (int64_t)e0 * 96, (uint32_t)cnt * 384u, bar, pol_stream);
-            if (full) bulk_g2s(smem_u32(cst), coup_g + (int64_t)e0 * 15, (uint32_t)T * 60u, bar, pol_stream);
+            bulk_g2s(smem_u32(rads + st * T * RF), rad_g + (int64_t)e0 * RF, (uint32_t)cnt * (RF * 4u), bar,
+                     pol_stream);
+            if (full) bulk_g2s(smem_u32(cst), coup_g + (int64_t)e0 * R, (uint32_t)T * R * 4u, bar, pol_stream);
         }
         __syncwarp();
         if (valid)
-            bulk_g2s(smem_u32(gs + (st * T + lane) * (15 * kC32)), g_g + (int64_t)d * (16 * kC32) + kC32, 1920u,
+            bulk_g2s(smem_u32(gs + (st * T + lane) * (R * kC32)), g_g + (int64_t)d * (D * kC32) + kC32, kGBytes,
                      bar, pol_g);
     }
 
@@ -488,6 +493,92 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
             }
             __syncwarp();
             ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
+        }
+    }
+    ring.drain();
+}
+
+// --------------------------------------------------------------------------
+// Edge-order backward at C = 32 for the other ladders, fed by the same
+// bulk-copy ring, with no cross-lane reduction: d_rad with lane = channel
+// (d_rad[e,s,c] sums the rows of slot s: R smem loads and FMAs per lane),
+// d_coup with lane = row (d_coup[e,r] is a 32-channel dot product of the
+// cotangent row and the radial row, read as 16-byte pieces in an order
+// rotated by the lane so that a quarter-warp touches eight different bank
+// groups).  Rows beyond 32 take a second pass.
+// --------------------------------------------------------------------------
+
+template <int W, int S, int T, int LM>
+__global__ void __launch_bounds__(W * 32, 1)
+bwd_edge_rows(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+              const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
+              float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale,
+              int cld, int dld, int coup_bulk) {
+    using Ring = EdgeRing<S, T, LM>;
+    constexpr int R = Ring::R, RF = Ring::RF;
+    constexpr int kPasses = (R + 31) / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * W + warp;
+    const bool active = gw < Wtot;
+    pdl_wait();
+    pdl_trigger();
+    const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
+    const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
+    Ring ring;
+    ring.init(smem + (size_t)warp * Ring::Layout::kBytes, p0, p1, lane);
+    const uint64_t pol_out = l2_evict_first();
+    int rslot[kPasses];   // radial slot of this lane's coupling-gradient row in each pass
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) rslot[ps] = ladder_slot(imin(32 * ps + lane, R - 1));
+    if (active) {
+        ring.prefetch(dst, lane);
+#pragma unroll
+        for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, lane);
+        for (int k = 0; k < ring.ntiles; ++k) {
+            const int st = ring.acquire();
+            const int e0 = p0 + k * T;
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                const int m = ring.meta[st * T + j];
+                if (m == -2) continue;
+                const bool ok = m >= 0;
+                const float sc = (scale && ok) ? __ldg(scale + m) : 1.f;
+                const int64_t e = e0 + j;
+                const float* gj = ring.gs + (st * T + j) * (R * kC32);
+                const float* rj = ring.rads + (st * T + j) * RF;
+                const float* cj = ring.coups + st * T * R + j * R;
+                // d_rad: lane = channel
+                float sv[LM];
+#pragma unroll
+                for (int q = 0; q < LM; ++q) sv[q] = 0.f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) sv[ladder_slot(r)] = fmaf(gj[r * kC32 + lane], cj[r], sv[ladder_slot(r)]);
+                float* dr = d_rad + e * RF + lane;
+#pragma unroll
+                for (int q = 0; q < LM; ++q) st_hint(dr + q * kC32, ok ? (scale ? sv[q] * sc : sv[q]) : 0.f, pol_out);
+                // d_coup: lane = row
+#pragma unroll
+                for (int ps = 0; ps < kPasses; ++ps) {
+                    const int row = 32 * ps + lane;
+                    if (kPasses > 1 && 32 * ps >= R) break;
+                    const float4* grow = reinterpret_cast<const float4*>(gj + imin(row, R - 1) * kC32);
+                    const float4* rrow = reinterpret_cast<const float4*>(rj + rslot[ps] * kC32);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int ch = (kk + lane) & 7;
+                        const float4 a = grow[ch], b = rrow[ch];
+                        acc = fmaf(a.x, b.x, acc);
+                        acc = fmaf(a.y, b.y, acc);
+                        acc = fmaf(a.z, b.z, acc);
+                        acc = fmaf(a.w, b.w, acc);
+                    }
+                    if (row < R) st_stream(d_coup + e * dld + row, ok ? (scale ? acc * sc : acc) : 0.f);
+                }
+            }
+            __syncwarp();
+            ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, lane);
         }
     }
     ring.drain();
@@ -611,6 +702,63 @@ bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32
     if (lane == 0) d_scale[n] = acc;
 }
 
+// Ring shape of the other ladders' edge backward (tile edges and stages per
+// ladder degree 1, 2, 4, 5, picked by timing on the n4096 graph); as many
+// warps (up to 16) as one SM's shared memory holds.
+#ifndef ZS_ROWS_T1
+#define ZS_ROWS_T1 8
+#endif
+#ifndef ZS_ROWS_T2
+#define ZS_ROWS_T2 8
+#endif
+#ifndef ZS_ROWS_T4
+#define ZS_ROWS_T4 2
+#endif
+#ifndef ZS_ROWS_T5
+#define ZS_ROWS_T5 4
+#endif
+#ifndef ZS_ROWS_S1
+#define ZS_ROWS_S1 3
+#endif
+#ifndef ZS_ROWS_S2
+#define ZS_ROWS_S2 2
+#endif
+#ifndef ZS_ROWS_S4
+#define ZS_ROWS_S4 3
+#endif
+#ifndef ZS_ROWS_S5
+#define ZS_ROWS_S5 2
+#endif
+template <int LM>
+constexpr int rows_pick(const int (&v)[4]) { return v[LM <= 2 ? LM - 1 : LM - 2]; }
+constexpr int kRowsTiles[4] = {ZS_ROWS_T1, ZS_ROWS_T2, ZS_ROWS_T4, ZS_ROWS_T5};
+constexpr int kRowsStages[4] = {ZS_ROWS_S1, ZS_ROWS_S2, ZS_ROWS_S4, ZS_ROWS_S5};
+template <int LM>
+constexpr int rows_tile() { return rows_pick<LM>(kRowsTiles); }
+template <int LM>
+constexpr int rows_stages() { return rows_pick<LM>(kRowsStages); }
+template <int LM>
+constexpr int rows_warps() {
+    constexpr int bytes = EdgeRingLayout<rows_stages<LM>(), rows_tile<LM>(), LM>::kBytes;
+    return (232448 / bytes) < 16 ? (232448 / bytes) : 16;
+}
+
+template <int LM>
+void launch_edge_rows(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
+                      int32_t N, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
+    constexpr int W = rows_warps<LM>(), T = rows_tile<LM>(), S = rows_stages<LM>();
+    const int64_t warps_max = (int64_t)num_sms() * W;
+    const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
+    const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
+    const int64_t ctas = (Wtot + W - 1) / W;
+    const int smem = W * EdgeRingLayout<S, T, LM>::kBytes;
+    const int bulk = (cld == Ladder<LM>::R && aligned16(coup)) ? 1 : 0;
+    static std::atomic<bool> attr_done[kMaxDevices];
+    set_smem_limit_once(bwd_edge_rows<W, S, T, LM>, smem, attr_done);
+    launch(bwd_edge_rows<W, S, T, LM>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
+           (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+}
+
 template <int L>
 void launch_gen_edges(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
                       int32_t N, int C, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
@@ -649,7 +797,16 @@ static zs_status backward_impl(const char* name, const float* g, const float* co
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "%s: g is NULL with N > 0", name);
     // coupling rows and d_coup may have any stride and 4-byte alignment on every path
     const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad);
-    if (fast) {
+    const bool rows = lmax != 3 && C == kC32 && aligned16(g) && aligned16(rad);
+    if (rows) {
+        const int c = (int)cld, d = (int)dld;
+        switch (lmax) {
+            case 1: launch_edge_rows<1>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            case 2: launch_edge_rows<2>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            case 4: launch_edge_rows<4>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            default: launch_edge_rows<5>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+        }
+    } else if (fast) {
         // While the cotangent block is small enough to stay in L2 next to the
         // streams, more warps with one tile in flight each hide the gather
         // latency best; a larger block misses L2 more often and wants more
