@@ -200,6 +200,7 @@ __device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, f
 // padding), quad q = lane%8 channels 4q..4q+3: per edge 2 LDS.128 + 4 LDS.32
 // + 16 FFMA per lane.
 struct QuadLayout {
+    static constexpr int kTileEdges = kTile;
     static constexpr int kRadFloats = 3 * kC32, kCoupRow = kRows, kPartFloats = kPartFloats32;
     static constexpr int kSlot = coup_slot_floats(kCoupRow);
     struct Acc {
@@ -239,6 +240,9 @@ struct QuadLayout {
 // FFMA per lane.  Node rows are written as 128-byte lines.
 template <int LM>
 struct ChanLayout {
+    // small rows: more edges per tile keep more bytes in flight (measured
+    // better for lmax 1, 2, 4; lmax 5 keeps 8 and its 16 warps)
+    static constexpr int kTileEdges = LM <= 4 ? 16 : 8;
     static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
     static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
     static constexpr int kSlot = coup_slot_floats(kCoupRow);
@@ -695,13 +699,15 @@ static uint64_t next_salt() {
 // rings as one SM's shared memory holds.
 template <class P>
 constexpr int tma_warps() {
-    constexpr int bytes = RingLayout<kTmaStages, kTile, P::kRadFloats, P::kCoupRow>::kBytes;
+    constexpr int bytes = RingLayout<kTmaStages, P::kTileEdges, P::kRadFloats, P::kCoupRow>::kBytes;
     return (232448 / bytes) < kTmaWarps ? (232448 / bytes) : kTmaWarps;
 }
 
-constexpr int kMinTmaSpan = imin(imin(tma_warps<ChanLayout<1>>(), tma_warps<ChanLayout<2>>()),
-                                  imin(imin(tma_warps<QuadLayout>(), tma_warps<ChanLayout<4>>()),
-                                       tma_warps<ChanLayout<5>>())) * kTile;
+template <class P>
+constexpr int tma_span() { return tma_warps<P>() * P::kTileEdges; }
+constexpr int kMinTmaSpan = imin(imin(tma_span<ChanLayout<1>>(), tma_span<ChanLayout<2>>()),
+                                 imin(imin(tma_span<QuadLayout>(), tma_span<ChanLayout<4>>()),
+                                      tma_span<ChanLayout<5>>()));
 
 static int tma_warps_for(int lmax) {
     switch (lmax) {
@@ -710,6 +716,16 @@ static int tma_warps_for(int lmax) {
         case 3: return tma_warps<QuadLayout>();
         case 4: return tma_warps<ChanLayout<4>>();
         default: return tma_warps<ChanLayout<5>>();
+    }
+}
+
+static int tma_tile_for(int lmax) {
+    switch (lmax) {
+        case 1: return ChanLayout<1>::kTileEdges;
+        case 2: return ChanLayout<2>::kTileEdges;
+        case 3: return QuadLayout::kTileEdges;
+        case 4: return ChanLayout<4>::kTileEdges;
+        default: return ChanLayout<5>::kTileEdges;
     }
 }
 
@@ -734,7 +750,7 @@ static FwdPlan fwd_plan(const float* rad, const NodeOut& o, int64_t E, int C, in
         // number of CSR positions (at least one tile).
         p.W = tma_warps_for(lmax);
         const int64_t warps_max = (int64_t)num_sms() * p.W;
-        p.KW = imax<int64_t>(ceil_div(E, warps_max), kTile);   // < 2^31: E < 2^31
+        p.KW = imax<int64_t>(ceil_div(E, warps_max), tma_tile_for(lmax));   // < 2^31: E < 2^31
         p.Wtot = imax<int64_t>(ceil_div(E, p.KW), 1);
         p.ctas = ceil_div(p.Wtot, p.W);
         p.windows = p.ctas;
@@ -762,8 +778,8 @@ static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float
                        const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
                        cudaStream_t s) {
     constexpr int W = tma_warps<P>();
-    auto kernel = fwd_tma<W, kTmaStages, kTile, P>;
-    const int smem = W * RingLayout<kTmaStages, kTile, P::kRadFloats, P::kCoupRow>::kBytes;
+    auto kernel = fwd_tma<W, kTmaStages, P::kTileEdges, P>;
+    const int smem = W * RingLayout<kTmaStages, P::kTileEdges, P::kRadFloats, P::kCoupRow>::kBytes;
     static std::atomic<bool> attr_done[kMaxDevices];
     set_smem_limit_once(kernel, smem, attr_done);
     launch(kernel, (unsigned)p.ctas, W * 32, smem, s, coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW,
@@ -796,9 +812,8 @@ extern "C" size_t zs_forward_workspace_bytes_lmax(int64_t E, int32_t N, int32_t 
     if (E < 0 || N < 0 || C < 1 || lmax < 1 || lmax > kMaxLmax) return 0;
     (void)N;
     // Sized for the smaller of the two window lengths: kGenWin positions per
-    // warp on the per-channel path, at least W * kTile per CTA on the
-    // single-wave C == 32 path (every layout's W * kTile is at least
-    // kMinTmaSpan).
+    // warp on the per-channel path, at least W * (tile edges) per CTA on the
+    // single-wave C == 32 path (at least kMinTmaSpan for every layout).
     const int64_t win = imin<int64_t>(kGenWin, kMinTmaSpan);
     const int64_t windows = ceil_div(E > 0 ? E : 1, win) + 1;
     return scratch_bytes(windows, C, ladder_rows(lmax));
