@@ -369,37 +369,91 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         h_dc = torch.empty_like(d_coup, device="cpu").pin_memory()
         h_dr = torch.empty_like(d_rad, device="cpu").pin_memory()
 
-        def e2e_step():
-            dst.copy_(h_dst, non_blocking=True)
-            coup.copy_(h_coup, non_blocking=True)
-            rad.copy_(h_rad, non_blocking=True)
-            g.copy_(h_g, non_blocking=True)
-            zs.zs_build_csr(dst, N, row_ptr=row_ptr, perm=perm, bad_dst_count=bad, workspace=ws_csr)
+        # Two sets of device buffers: step i+1's inputs arrive (copy stream in) while
+        # step i computes and step i-1's results leave (copy stream out).
+        def buffers():
+            b = dict(dst=torch.empty_like(dst), coup=torch.empty_like(coup), rad=torch.empty_like(rad),
+                     g=torch.empty_like(g), row_ptr=torch.empty_like(row_ptr), perm=torch.empty_like(perm),
+                     bad=torch.empty_like(bad), out=torch.empty_like(out), d_coup=torch.empty_like(d_coup),
+                     d_rad=torch.empty_like(d_rad), ws_csr=torch.empty_like(ws_csr), ws_fwd=torch.empty_like(ws_fwd))
             if args.scaled:
-                zs.zs_forward_scaled(coup, rad, row_ptr, perm, node_scale, N, out=out, out_raw=out_raw,
-                                     workspace=ws_fwd)
-                zs.zs_backward_scaled(g, coup, rad, dst, node_scale, N, out_raw=out_raw, d_coup=d_coup,
-                                      d_rad=d_rad, d_scale=d_scale)
-            elif args.backward == "csr":
-                zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
-                zs.zs_backward_csr(g, coup, rad, row_ptr, perm, N, d_coup=d_coup, d_rad=d_rad)
-            else:
-                zs.zs_forward(coup, rad, row_ptr, perm, N, out=out, workspace=ws_fwd)
-                zs.zs_backward(g, coup, rad, dst, N, d_coup=d_coup, d_rad=d_rad)
-            h_out.copy_(out, non_blocking=True)
-            h_dc.copy_(d_coup, non_blocking=True)
-            h_dr.copy_(d_rad, non_blocking=True)
+                b.update(out_raw=torch.empty_like(out), d_scale=torch.empty_like(d_scale))
+            return b
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        sets = [buffers(), buffers()]
+        n_copy = max(1, args.copy_streams)
+        s_in = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+        s_out = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+        s_comp = torch.cuda.Stream(dev)
+        ev_in = [[torch.cuda.Event() for _ in range(n_copy)] for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [[torch.cuda.Event() for _ in range(n_copy)] for _ in range(2)]
+        used = [False, False]
+
+        def chunked(pairs):
+            # (dst, src) copies split into n_copy slices along dim 0, one slice per copy stream
+            for d, src in pairs:
+                rows = d.shape[0]
+                for c in range(n_copy):
+                    lo, hi = rows * c // n_copy, rows * (c + 1) // n_copy
+                    if hi > lo:
+                        yield c, d[lo:hi], src[lo:hi]
+
+        def e2e_step(i):
+            k = i % 2
+            B = sets[k]
+            for c in range(n_copy):
+                if used[k]:
+                    s_in[c].wait_event(ev_comp[k])     # step i-2 is done with these inputs
+            for c, d, src in chunked(((B["dst"], h_dst), (B["coup"], h_coup), (B["rad"], h_rad), (B["g"], h_g))):
+                with torch.cuda.stream(s_in[c]):
+                    d.copy_(src, non_blocking=True)
+            for c in range(n_copy):
+                ev_in[k][c].record(s_in[c])
+            with torch.cuda.stream(s_comp):
+                for c in range(n_copy):
+                    s_comp.wait_event(ev_in[k][c])
+                if used[k]:
+                    for c in range(n_copy):
+                        s_comp.wait_event(ev_out[k][c])   # step i-2's results have left
+                zs.zs_build_csr(B["dst"], N, row_ptr=B["row_ptr"], perm=B["perm"], bad_dst_count=B["bad"],
+                                workspace=B["ws_csr"])
+                if args.scaled:
+                    zs.zs_forward_scaled(B["coup"], B["rad"], B["row_ptr"], B["perm"], node_scale, N, out=B["out"],
+                                         out_raw=B["out_raw"], workspace=B["ws_fwd"])
+                    zs.zs_backward_scaled(B["g"], B["coup"], B["rad"], B["dst"], node_scale, N, out_raw=B["out_raw"],
+                                          d_coup=B["d_coup"], d_rad=B["d_rad"], d_scale=B["d_scale"])
+                elif args.backward == "csr":
+                    zs.zs_forward(B["coup"], B["rad"], B["row_ptr"], B["perm"], N, out=B["out"], workspace=B["ws_fwd"])
+                    zs.zs_backward_csr(B["g"], B["coup"], B["rad"], B["row_ptr"], B["perm"], N, d_coup=B["d_coup"],
+                                       d_rad=B["d_rad"])
+                else:
+                    zs.zs_forward(B["coup"], B["rad"], B["row_ptr"], B["perm"], N, out=B["out"], workspace=B["ws_fwd"])
+                    zs.zs_backward(B["g"], B["coup"], B["rad"], B["dst"], N, d_coup=B["d_coup"], d_rad=B["d_rad"])
+                ev_comp[k].record(s_comp)
+            for c in range(n_copy):
+                s_out[c].wait_event(ev_comp[k])
+            for c, d, src in chunked(((h_out, B["out"]), (h_dc, B["d_coup"]), (h_dr, B["d_rad"]))):
+                with torch.cuda.stream(s_out[c]):
+                    d.copy_(src, non_blocking=True)
+            for c in range(n_copy):
+                ev_out[k][c].record(s_out[c])
+            used[k] = True
+
+        for i in range(max(2, args.warmup)):
+            e2e_step(i)
         torch.cuda.synchronize()
         barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
+        a.record(s_in[0])
+        for c in range(1, n_copy):
+            s_in[c].wait_event(a)
+        for i in range(args.steps):
+            e2e_step(i)
+        for c in range(1, n_copy):
+            s_out[0].wait_stream(s_out[c])
+        b.record(s_out[0])
         torch.cuda.synchronize()
         barrier()
         e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
@@ -407,7 +461,9 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dc, h_dr))
         e2e = {"value": job_throughput(E, args.steps, e2e_ms, world), "unit": "edges/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.steps}
+               "ms_per_step": e2e_ms / args.steps,
+               "pipeline": f"two buffer sets: step i+1's host-to-device copies and step i-1's device-to-host "
+                           f"copies overlap step i; each copy split over {n_copy} stream(s) per direction"}
 
     total_ms = reduce_max(total_ms, world, dev)
     if rank != 0:
@@ -508,6 +564,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end measurement")
     ap.add_argument("--scaled", action="store_true",
                     help="step with the degree normalisation fused in (zs_forward_scaled, zs_backward_scaled)")
     ap.add_argument("--lmax", type=int, default=3, choices=[1, 2, 3, 4, 5],
