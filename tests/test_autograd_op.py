@@ -101,11 +101,13 @@ def test_compiled_function_matches_eager():
 
 
 @pytest.mark.gpu
-def test_cuda_graph_replay_with_new_inputs():
+@pytest.mark.parametrize("lmax", [3, 2])
+def test_cuda_graph_replay_with_new_inputs(lmax):
     # the C = 32 forward combines nodes that cross CTA windows with per-launch
     # tags; replays of one captured graph must each see their own partials
+    # (lmax 3: quad layout; lmax 2: lane-per-channel layout)
     N, E, C = 64, 120000, 32
-    ws = [workloads.make_random(N, E, C, seed=s, hot_node=5, hot_fraction=0.6) for s in (21, 22, 23)]
+    ws = [workloads.make_random(N, E, C, seed=s, hot_node=5, hot_fraction=0.6, lmax=lmax) for s in (21, 22, 23)]
     coup, rad, dst, g = (dev(ws[0].coup), dev(ws[0].rad), dev(ws[0].dst), dev(ws[0].grad_out))
     row_ptr, perm = ag.build_csr(dst, N)          # warm-up outside the capture
     ag.zonal_scatter(coup, rad, dst, row_ptr, perm, N)
