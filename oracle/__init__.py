@@ -39,7 +39,7 @@ def build(force: bool = False) -> str:
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
                                "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -61,6 +61,9 @@ def _load():
                                             ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64, P, P, P, P]
             lib.oracle_slot_of_row.restype = ctypes.c_int
             lib.oracle_slot_of_row.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads.restype = None
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads(1)
             _lib = lib
     return _lib
 
@@ -173,6 +176,12 @@ def backward_scaled(g, coup, rad, dst, N: int, scale, out_raw):
     d_scale = np.einsum("nrc,nrc->n", g64[:, 1:], raw[:, 1:])
     abs_ds = np.einsum("nrc,nrc->n", np.abs(g64[:, 1:]), np.abs(raw[:, 1:]))
     return dc, dr, d_scale, adc, adr, abs_ds
+
+
+def set_threads(n: int) -> None:
+    """Threads of the C oracle's node and edge loops (1 by default); results do
+    not depend on it (every node's and edge's arithmetic runs on one thread)."""
+    _load().oracle_set_threads(int(n))
 
 
 def slot_of_row(r: int) -> int:

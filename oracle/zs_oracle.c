@@ -37,6 +37,9 @@
  */
 #include <math.h>
 #include <stddef.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -97,6 +100,10 @@ void oracle_forward(const float* coup, const float* rad,
     size_t block = (size_t)D * (size_t)C;
     memset(out, 0, sizeof(double) * block * (size_t)n_out);
     if (absum) memset(absum, 0, sizeof(double) * block * (size_t)n_out);
+    /* nodes are independent: each is summed by one thread in CSR order */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16)
+#endif
     for (int64_t k = 0; k < n_out; ++k) {
         int32_t n = nodes ? nodes[k] : (int32_t)k;
         double* o = out + block * (size_t)k;
@@ -133,6 +140,10 @@ void oracle_backward(const float* g, const float* coup, const float* rad,
                      double* abs_dcoup, double* abs_drad) {
     const int D = (lmax + 1) * (lmax + 1), R = D - 1, S = lmax;
     int64_t n_out = edges ? n_edges : E;
+    /* edges are independent: each one's gradients by one thread */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t k = 0; k < n_out; ++k) {
         int64_t e = edges ? edges[k] : k;
         double* dc = d_coup + (size_t)k * R;
@@ -166,3 +177,13 @@ void oracle_backward(const float* g, const float* coup, const float* rad,
 
 /* Row-to-slot map as the oracle uses it, for the tests' cross-checks. */
 int oracle_slot_of_row(int r) { return slot_of_row(r); }
+
+/* Threads the forward and backward loops may use (1 unless raised); the
+ * arithmetic of every node and edge is the same whatever the count. */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}

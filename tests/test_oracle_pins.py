@@ -364,3 +364,16 @@ def test_node_factor_planted_mistakes_caught(mistake):
     with pytest.raises((pins.PinFailure, FloatingPointError)):
         with np.errstate(invalid="raise"):
             pins.pin_node_factor(fwd, bwd)
+
+
+def test_oracle_threads_do_not_change_results():
+    w = workloads.make_random(300, 20000, 8, seed=91, hot_node=4, hot_fraction=0.3)
+    rp, pm, _ = oracle.build_csr(w.dst, w.N)
+    one = oracle.forward(w.coup, w.rad, rp, pm, w.N), oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
+    oracle.set_threads(4)
+    try:
+        many = oracle.forward(w.coup, w.rad, rp, pm, w.N), oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
+    finally:
+        oracle.set_threads(1)
+    for a, b in zip(one[0] + one[1], many[0] + many[1]):
+        assert np.array_equal(a, b)
