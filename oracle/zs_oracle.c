@@ -33,7 +33,7 @@
  * and counts them; the backward gives such edges zero gradients.
  *
  * Alongside every value the oracle returns the sum of |terms| that formed
- * it, the denominator of the normalised error used to judge fp32 results.
+ * it, the denominator of the normalised error used to assess fp32 results.
  */
 #include <math.h>
 #include <stddef.h>
