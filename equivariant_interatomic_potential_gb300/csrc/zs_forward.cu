@@ -1,10 +1,13 @@
-// Forward zonal scatter, lmax = 3:
+// Forward zonal scatter (lmax = 3 shown; the ladders lmax = 1..5 the same way
+// with D = (lmax+1)^2 rows):
 //   out[n,0,:] = 0,  out[n,1+r,c] = sum over n's CSR positions j (in order)
 //                                   of coup[e,r] * rad[e,slot(r),c], e = perm[j]
 // (deepmd-kit pull request "fused Triton zonal scatter for the GIE head",
 // section "What", forward bullet: a node-parallel walk of the stable
 // destination CSR, message accumulated in registers, the (E,15,C) message
-// never materialised, padded (N,16,C) output with a zero scalar row).
+// never materialised, padded (N,16,C) output with a zero scalar row).  An
+// optional per-node factor (the degree normalisation the pages apply after
+// the operator) is applied as each node is written.
 //
 // Work split.  The pages use one program per node; on a 152-SM part with a
 // skewed in-degree (one node can own 1/6 of all edges) that leaves most SMs

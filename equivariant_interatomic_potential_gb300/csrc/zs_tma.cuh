@@ -2,16 +2,17 @@
 //
 // A warp streams the edges at CSR positions [p0, pe) in tiles of T edges
 // (T <= 32, one lane per edge).  For edge e = perm[j] its lane issues
-//   - one cp.async.bulk (TMA) copy of the radial row rad[e] (3*32 floats,
-//     384 bytes, 16-byte aligned), completion counted in bytes on the
-//     stage's mbarrier, and
-//   - four or five 16-byte cp.async copies of the aligned span holding the
-//     coupling row coup[e] (60 bytes, rows cld floats apart), completion
+//   - one cp.async.bulk (TMA) copy of the radial row rad[e] (RadFloats
+//     floats: lmax rows of 32 channels, 384 bytes at lmax 3, 16-byte
+//     aligned), completion counted in bytes on the stage's mbarrier, and
+//   - the 16-byte cp.async copies of the aligned span holding the coupling
+//     row coup[e] (CoupRow floats, rows cld floats apart, any 4-byte
+//     alignment: four or five pieces for the 15-float row), completion
 //     signalled to the same mbarrier by cp.async.mbarrier.arrive.
 // Tiles are issued S - 1 ahead of the one being consumed, so a warp keeps
-// (S - 1) * T * ~450 bytes of HBM reads in flight without holding registers
-// for them.  A position whose perm entry is not a valid edge id gets zero
-// rows, so consumers need no branch.
+// (S - 1) * T edges of HBM reads in flight without holding registers for
+// them.  A position whose perm entry is not a valid edge id gets zero rows,
+// so consumers need no branch.
 //
 // Every wait is bounded: after kMaxSpins unsuccessful tries the wait counts a
 // timeout in g_zs_timeouts and returns, so a lost completion can never hang
@@ -33,8 +34,7 @@ static inline unsigned int take_timeouts_local() {
     return v;
 }
 
-constexpr int kRadRowBytes = 3 * 32 * 4;    // 384
-constexpr int kCoupSlotFloats = 20;         // 80 bytes: the widest aligned span of one coupling row
+constexpr int kCoupSlotFloats = 20;         // coupling slot of the 15-row ladder (coup_slot_floats(15))
 constexpr uint32_t kMaxSpins = 1u << 22;
 constexpr uint32_t kRingArrivals = 33;      // the expect-tx arrival plus one cp.async arrival per lane
 
@@ -91,6 +91,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // 15-row ladder), and the 16-byte pieces that span can take.
 __host__ __device__ constexpr int coup_slot_floats(int coup_row) { return (coup_row + 3 + 3) / 4 * 4; }
 __host__ __device__ constexpr int coup_max_chunks(int coup_row) { return (12 + 4 * coup_row + 15) / 16; }
+static_assert(coup_slot_floats(15) == kCoupSlotFloats, "the 15-row ladder's coupling slot");
 
 // Shared-memory layout of one warp's ring of S stages of T edges, each edge
 // a radial row of RadFloats floats and a coupling row of CoupRow floats
