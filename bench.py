@@ -24,6 +24,7 @@ import statistics
 import subprocess
 import sys
 import time
+from types import SimpleNamespace
 
 import numpy as np
 
@@ -212,38 +213,57 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     dev = torch.device("cuda", local)
     lib = zs.load()
 
-    dst = torch.from_numpy(w.dst).to(dev)
-    coup = torch.from_numpy(w.coup).to(dev)
-    rad = torch.from_numpy(w.rad).to(dev)
-    g = torch.from_numpy(w.grad_out).to(dev)
-    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(E, dtype=torch.int32, device=dev)
-    bad = torch.empty(1, dtype=torch.int32, device=dev)
-    ws_csr = torch.empty(max(1, zs.zs_build_csr_workspace_bytes(E, N)), dtype=torch.uint8, device=dev)
-    ws_fwd = torch.empty(max(1, zs.zs_forward_workspace_bytes(E, N, C, L)), dtype=torch.uint8, device=dev)
-    out = torch.empty((N, D, C), dtype=torch.float32, device=dev)
-    d_coup = torch.empty((E, R), dtype=torch.float32, device=dev)
-    d_rad = torch.empty((E, L, C), dtype=torch.float32, device=dev)
+    # Resident input/output sets, rotated step by step, so that no step finds
+    # lines an earlier step left in L2 (a new batch every step, as in training):
+    # enough sets that their arrays exceed L2 several times over.
+    def make_set(src=None):
+        b = SimpleNamespace()
+        if src is None:
+            b.dst = torch.from_numpy(w.dst).to(dev)
+            b.coup = torch.from_numpy(w.coup).to(dev)
+            b.rad = torch.from_numpy(w.rad).to(dev)
+            b.g = torch.from_numpy(w.grad_out).to(dev)
+        else:
+            b.dst, b.coup, b.rad, b.g = (t.clone() for t in (src.dst, src.coup, src.rad, src.g))
+        b.row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+        b.perm = torch.empty(E, dtype=torch.int32, device=dev)
+        b.bad = torch.empty(1, dtype=torch.int32, device=dev)
+        b.ws_csr = torch.empty(max(1, zs.zs_build_csr_workspace_bytes(E, N)), dtype=torch.uint8, device=dev)
+        b.ws_fwd = torch.empty(max(1, zs.zs_forward_workspace_bytes(E, N, C, L)), dtype=torch.uint8, device=dev)
+        b.out = torch.empty((N, D, C), dtype=torch.float32, device=dev)
+        b.d_coup = torch.empty((E, R), dtype=torch.float32, device=dev)
+        b.d_rad = torch.empty((E, L, C), dtype=torch.float32, device=dev)
+        if args.scaled:
+            b.out_raw = torch.empty_like(b.out)
+            b.d_scale = torch.empty(N, dtype=torch.float32, device=dev)
+        return b
+
+    first = make_set()
+    set_bytes = sum(t.numel() * t.element_size() for t in vars(first).values())
+    n_sets = args.sets or max(3, min(64, -(-4 * L2_BYTES // max(1, set_bytes))))
+    sets = [first] + [make_set(first) for _ in range(n_sets - 1)]
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
     P = lambda t: t.data_ptr()  # noqa: E731
-    csr_ws_bytes, fwd_ws_bytes = ws_csr.numel(), ws_fwd.numel()
+    csr_ws_bytes, fwd_ws_bytes = first.ws_csr.numel(), first.ws_fwd.numel()
 
-    def csr():
-        st = lib.zs_build_csr(P(dst), E, N, P(row_ptr), P(perm), P(bad), P(ws_csr), csr_ws_bytes, sp)
+    def csr(b):
+        st = lib.zs_build_csr(P(b.dst), E, N, P(b.row_ptr), P(b.perm), P(b.bad), P(b.ws_csr), csr_ws_bytes, sp)
         assert st == 0, lib.zs_last_error()
 
-    def fwd():
-        st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(out), P(ws_fwd), fwd_ws_bytes, sp)
+    def fwd(b):
+        st = lib.zs_forward(P(b.coup), P(b.rad), P(b.row_ptr), P(b.perm), E, N, C, L, P(b.out), P(b.ws_fwd),
+                            fwd_ws_bytes, sp)
         assert st == 0, lib.zs_last_error()
 
-    def bwd_edge():
-        st = lib.zs_backward(P(g), P(coup), P(rad), P(dst), E, N, C, L, P(d_coup), P(d_rad), sp)
+    def bwd_edge(b):
+        st = lib.zs_backward(P(b.g), P(b.coup), P(b.rad), P(b.dst), E, N, C, L, P(b.d_coup), P(b.d_rad), sp)
         assert st == 0, lib.zs_last_error()
 
-    def bwd_csr():
-        st = lib.zs_backward_csr(P(g), P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(d_coup), P(d_rad), sp)
+    def bwd_csr(b):
+        st = lib.zs_backward_csr(P(b.g), P(b.coup), P(b.rad), P(b.row_ptr), P(b.perm), E, N, C, L, P(b.d_coup),
+                                 P(b.d_rad), sp)
         assert st == 0, lib.zs_last_error()
 
     bwd, bwd_other, other_name = (bwd_csr, bwd_edge, "bwd_edge") if args.backward == "csr" else \
@@ -254,32 +274,30 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         indeg = np.bincount(w.dst[(w.dst >= 0) & (w.dst < N)], minlength=N)
         s_host = np.where(indeg > 0, 1.0 / np.sqrt(np.maximum(indeg, 1)), 0.0).astype(np.float32)
         node_scale = torch.from_numpy(s_host).to(dev)
-        out_raw = torch.empty_like(out)
-        d_scale = torch.empty(N, dtype=torch.float32, device=dev)
 
-        def fwd():
-            st = lib.zs_forward_scaled(P(coup), P(rad), P(row_ptr), P(perm), P(node_scale), E, N, C, L, P(out),
-                                       P(out_raw), P(ws_fwd), fwd_ws_bytes, sp)
+        def fwd(b):
+            st = lib.zs_forward_scaled(P(b.coup), P(b.rad), P(b.row_ptr), P(b.perm), P(node_scale), E, N, C, L,
+                                       P(b.out), P(b.out_raw), P(b.ws_fwd), fwd_ws_bytes, sp)
             assert st == 0, lib.zs_last_error()
 
-        def bwd():
-            st = lib.zs_backward_scaled(P(g), P(coup), P(rad), P(dst), P(node_scale), P(out_raw), E, N, C, L,
-                                        P(d_coup), P(d_rad), P(d_scale), sp)
+        def bwd(b):
+            st = lib.zs_backward_scaled(P(b.g), P(b.coup), P(b.rad), P(b.dst), P(node_scale), P(b.out_raw), E, N,
+                                        C, L, P(b.d_coup), P(b.d_rad), P(b.d_scale), sp)
             assert st == 0, lib.zs_last_error()
 
-        def fwd_unfused():
-            plain_fwd()
-            torch.mul(out_raw, node_scale[:, None, None], out=out)
+        def fwd_unfused(b):
+            plain_fwd(b)
+            torch.mul(b.out_raw, node_scale[:, None, None], out=b.out)
 
-        def bwd_unfused():
-            gs = g * node_scale[:, None, None]
-            st = lib.zs_backward(P(gs), P(coup), P(rad), P(dst), E, N, C, L, P(d_coup), P(d_rad), sp)
+        def bwd_unfused(b):
+            gs = b.g * node_scale[:, None, None]
+            st = lib.zs_backward(P(gs), P(b.coup), P(b.rad), P(b.dst), E, N, C, L, P(b.d_coup), P(b.d_rad), sp)
             assert st == 0, lib.zs_last_error()
-            torch.sum(g[:, 1:] * out_raw[:, 1:], dim=(1, 2), out=d_scale)
+            torch.sum(b.g[:, 1:] * b.out_raw[:, 1:], dim=(1, 2), out=b.d_scale)
 
-        def plain_fwd():
-            st = lib.zs_forward(P(coup), P(rad), P(row_ptr), P(perm), E, N, C, L, P(out_raw), P(ws_fwd),
-                                fwd_ws_bytes, sp)
+        def plain_fwd(b):
+            st = lib.zs_forward(P(b.coup), P(b.rad), P(b.row_ptr), P(b.perm), E, N, C, L, P(b.out_raw),
+                                P(b.ws_fwd), fwd_ws_bytes, sp)
             assert st == 0, lib.zs_last_error()
 
     # zs_build_csr: three launches on its one-pass counting path (N + 1 <= 5120),
@@ -296,8 +314,9 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     if args.scaled:
         launches_per_step += 1   # the scale's gradient
 
-    for _ in range(args.warmup):
-        csr(); fwd(); bwd()
+    for i in range(max(args.warmup, n_sets)):
+        b = sets[i % n_sets]
+        csr(b); fwd(b); bwd(b)
     torch.cuda.synchronize()
 
     def barrier():
@@ -313,49 +332,70 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         torch.cuda.synchronize()
         t0.record(stream)
         for i in range(args.steps):
-            csr()
-            fwd()
-            bwd()
+            b = sets[i % n_sets]
+            csr(b)
+            fwd(b)
+            bwd(b)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
     total_ms = t0.elapsed_time(t1)
     clock = clocks.summary()
-    # per-kernel durations, each launch bracketed by events on the same stream
+    # per-kernel durations (1): each launch of a step bracketed by events on the same stream
     ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)] for k in ("csr", "fwd", "bwd")}
     for i in range(args.steps):
+        b = sets[i % n_sets]
         for k, fn in (("csr", csr), ("fwd", fwd), ("bwd", bwd)):
             ev[k][i][0].record(stream)
-            fn()
+            fn(b)
             ev[k][i][1].record(stream)
     torch.cuda.synchronize()
     per = {k: [a.elapsed_time(b) * 1e3 for a, b in ev[k]] for k in ev}   # microseconds
     # the other backward entry point, timed on its own for comparison
     oth = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in oth:
+    for i, (a, b) in enumerate(oth):
         a.record(stream)
-        bwd_other()
+        bwd_other(sets[i % n_sets])
         b.record(stream)
     torch.cuda.synchronize()
     per[other_name] = [a.elapsed_time(b) * 1e3 for a, b in oth]
+    # per-kernel durations (2): K launches of one entry point back to back over
+    # the rotating sets, events at the ends: the steady-state cost of a launch,
+    # its own write-backs included and its launch latency overlapped
+    b2b = {}
+    for k, fn in (("csr", csr), ("fwd", fwd), ("bwd", bwd), (other_name, bwd_other)):
+        for i in range(3):
+            fn(sets[i % n_sets])
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(args.steps):
+            fn(sets[i % n_sets])
+        z.record(stream)
+        torch.cuda.synchronize()
+        b2b[k] = a.elapsed_time(z) * 1e3 / args.steps
     unfused = None
     if args.scaled:
         # the same step with the factor applied by separate torch ops
         ev_u = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                     for _ in range(args.steps)] for k in ("fwd", "bwd")}
-        for _ in range(args.warmup):
-            csr(); fwd_unfused(); bwd_unfused()
+        for i in range(args.warmup):
+            b = sets[i % n_sets]
+            csr(b); fwd_unfused(b); bwd_unfused(b)
         torch.cuda.synchronize()
         for i in range(args.steps):
-            csr()
+            b = sets[i % n_sets]
+            csr(b)
             for k, fn in (("fwd", fwd_unfused), ("bwd", bwd_unfused)):
                 ev_u[k][i][0].record(stream)
-                fn()
+                fn(b)
                 ev_u[k][i][1].record(stream)
         torch.cuda.synchronize()
         unfused = {k + "_us": statistics.median(a.elapsed_time(b) * 1e3 for a, b in ev_u[k]) for k in ev_u}
         unfused["how"] = "zs_forward + torch.mul; g*s in torch, zs_backward, torch sum for d_scale"
+        unfused["fused_us_same_protocol"] = {k: statistics.median(per[k]) for k in ("fwd", "bwd")}
     zs.zs_check_timeouts()
 
     # end to end through the public API: pinned host buffers in, results out
@@ -365,22 +405,17 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         h_coup = torch.from_numpy(w.coup).pin_memory()
         h_rad = torch.from_numpy(w.rad).pin_memory()
         h_g = torch.from_numpy(w.grad_out).pin_memory()
-        h_out = torch.empty_like(out, device="cpu").pin_memory()
-        h_dc = torch.empty_like(d_coup, device="cpu").pin_memory()
-        h_dr = torch.empty_like(d_rad, device="cpu").pin_memory()
+        h_out = torch.empty_like(first.out, device="cpu").pin_memory()
+        h_dc = torch.empty_like(first.d_coup, device="cpu").pin_memory()
+        h_dr = torch.empty_like(first.d_rad, device="cpu").pin_memory()
 
         # Two sets of device buffers: step i+1's inputs arrive (copy stream in) while
         # step i computes and step i-1's results leave (copy stream out).
         def buffers():
-            b = dict(dst=torch.empty_like(dst), coup=torch.empty_like(coup), rad=torch.empty_like(rad),
-                     g=torch.empty_like(g), row_ptr=torch.empty_like(row_ptr), perm=torch.empty_like(perm),
-                     bad=torch.empty_like(bad), out=torch.empty_like(out), d_coup=torch.empty_like(d_coup),
-                     d_rad=torch.empty_like(d_rad), ws_csr=torch.empty_like(ws_csr), ws_fwd=torch.empty_like(ws_fwd))
-            if args.scaled:
-                b.update(out_raw=torch.empty_like(out), d_scale=torch.empty_like(d_scale))
-            return b
+            return {k: torch.empty_like(v) for k, v in vars(first).items()}
 
-        sets = [buffers(), buffers()]
+        del sets[1:]
+        bufs = [buffers(), buffers()]
         n_copy = max(1, args.copy_streams)
         s_in = [torch.cuda.Stream(dev) for _ in range(n_copy)]
         s_out = [torch.cuda.Stream(dev) for _ in range(n_copy)]
@@ -401,7 +436,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
         def e2e_step(i):
             k = i % 2
-            B = sets[k]
+            B = bufs[k]
             for c in range(n_copy):
                 if used[k]:
                     s_in[c].wait_event(ev_comp[k])     # step i-2 is done with these inputs
@@ -478,12 +513,17 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
     kernels = {}
     ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
     for k in ("csr", "fwd", "bwd", other_name):
-        us = statistics.mean(per[k])
+        # roofline figures from the back-to-back launches; the bracketed
+        # in-step launches (launch latency and the previous kernel's L2
+        # write-backs included) alongside
+        us = b2b[k]
+        us_step = statistics.mean(per[k])
         gbs = ab[k] / (us * 1e-6) / 1e9
-        kernels[k] = {"us_mean": us, "us_median": statistics.median(per[k]), "algorithmic_bytes": ab[k],
-                      "GBs": gbs, "frac_of_" + peak_kind: gbs / peak,
-                      "edges_per_s": E / (us * 1e-6)}
-    dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_mean"])
+        kernels[k] = {"us_back_to_back": us, "algorithmic_bytes": ab[k],
+                      "GBs": gbs, "frac_of_" + peak_kind: gbs / peak, "edges_per_s": E / (us * 1e-6),
+                      "us_in_step_mean": us_step, "us_in_step_median": statistics.median(per[k]),
+                      "frac_in_step": ab[k] / (us_step * 1e-6) / 1e9 / peak}
+    dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_back_to_back"])
     bwd_entry = "zs_backward_csr" if args.backward == "csr" else "zs_backward"
     roof = {"kernel": {"fwd": "zs_forward", "bwd": bwd_entry}[dom], "bound": "hbm",
             "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
@@ -491,7 +531,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
             "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config) if L == 3 else None,
             "algorithmic_bytes_per_launch": ab[dom]}
     ms_per_step = total_ms / args.steps
-    fwd_bwd_us = kernels["fwd"]["us_mean"] + kernels["bwd"]["us_mean"]
+    fwd_bwd_us = kernels["fwd"]["us_back_to_back"] + kernels["bwd"]["us_back_to_back"]
     res = {
         "metric": metric_for(L, args.scaled),
         "value": job_throughput(E, args.steps, total_ms, world),
@@ -506,7 +546,9 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         "dtype": "f32",
         "data": "synthetic",
         "config": dict(workload_config(w, args.backward, args.scaled),
-                       parallelism="replicas" if world > 1 else "single GPU"),
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       l2=f"{n_sets} resident input/output sets of {set_bytes / 1e6:.0f} MB rotated step by step "
+                          f"({n_sets * set_bytes / 1e6:.0f} MB against a {L2_BYTES / 1e6:.0f} MB L2); no flush"),
         "fwd_bwd_edges_per_s": E / (fwd_bwd_us * 1e-6),
         "kernels": kernels,
         "roofline": roof,
@@ -571,6 +613,8 @@ def main():
                     help="streams per copy direction in the end-to-end measurement")
     ap.add_argument("--scaled", action="store_true",
                     help="step with the degree normalisation fused in (zs_forward_scaled, zs_backward_scaled)")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="resident input/output sets the timed loops rotate through (0: enough to exceed 4x L2)")
     ap.add_argument("--lmax", type=int, default=3, choices=[1, 2, 3, 4, 5],
                     help="ladder degree of the operands (3: the 3/5/7 rows of the headline workload)")
     args = ap.parse_args()

@@ -13,6 +13,12 @@
 #include "zs_common.cuh"
 #include "zs_tma.cuh"
 
+// L2 policy of the CSR-order backward's coupling spans: normal, since a span
+// shares its sectors with the neighbouring edges' rows, which the CSR-order
+// walk reaches later (the ring's radial rows and perm are evict-first).
+#ifndef ZS_BWDC_COUP_POL
+#define ZS_BWDC_COUP_POL kL2Normal
+#endif
 namespace zs {
 namespace {
 
@@ -183,7 +189,7 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
-    TileRing<S, T, true> ring;
+    TileRing<S, T, kL2EvictFirst, 96, 15, ZS_BWDC_COUP_POL> ring;
     ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, Q.lane);
     const uint64_t pol_first = l2_evict_first(), pol_last = l2_evict_last();
     if (active) {

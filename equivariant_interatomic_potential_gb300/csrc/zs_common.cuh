@@ -93,6 +93,11 @@ __device__ __forceinline__ uint64_t l2_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// Ring copies name their L2 policy at compile time.
+enum : int { kL2Normal = 0, kL2EvictFirst = 1, kL2EvictLast = 2 };
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+    return hint == kL2EvictFirst ? l2_evict_first() : hint == kL2EvictLast ? l2_evict_last() : l2_evict_normal();
+}
 __device__ __forceinline__ void st_hint4(float* p, float4 v, uint64_t pol) {
     asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;"
                  :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol) : "memory");

@@ -48,6 +48,19 @@ constexpr int kFwdThreads = kFwdWarps * 32;
 constexpr int kTmaWarps = ZS_FWD_WARPS;
 constexpr int kTmaStages = ZS_FWD_STAGES;
 constexpr int kTile = ZS_FWD_TILE;
+// L2 policies of the forward's ring: radial rows (and perm) are read once,
+// evict-first, so the stream does not push the rest of L2 out; a coupling
+// row shares its 32-byte sectors with its neighbours in edge order, which the
+// CSR-order gather reaches later, so coupling spans keep the normal policy
+// (evict-first on them measured slower).
+#ifndef ZS_FWD_RAD_POL
+#define ZS_FWD_RAD_POL kL2EvictFirst
+#endif
+#ifndef ZS_FWD_COUP_POL
+#define ZS_FWD_COUP_POL kL2Normal
+#endif
+constexpr int kFwdRadPol = ZS_FWD_RAD_POL;
+constexpr int kFwdCoupPol = ZS_FWD_COUP_POL;
 constexpr int kGenWin = 256;                   // CSR positions per warp (per-channel path)
 constexpr int kC32 = 32;
 constexpr int kNodeFloats32 = kD * kC32;       // 512 floats per node at C = 32
@@ -328,7 +341,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
         int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
         uint64_t* __restrict__ flags, uint64_t salt) {
-    using Ring = TileRing<S, T, false, P::kRadFloats, P::kCoupRow>;
+    using Ring = TileRing<S, T, kFwdRadPol, P::kRadFloats, P::kCoupRow, kFwdCoupPol>;
     using Layout = typename Ring::Layout;
     using Acc = typename P::Acc;
     static_assert(2 * P::kPartFloats * 4 <= Layout::kRad + Layout::kCoup, "two partials fit a warp's idle ring");

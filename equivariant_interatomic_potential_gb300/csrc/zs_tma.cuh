@@ -105,9 +105,12 @@ struct RingLayout {
     static constexpr int kBytes = (kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
 };
 
-// One warp's stream of tiles over [p0, pe).  kEvictFirst marks every byte
-// the ring brings in as evict-first in L2 (it is read exactly once).
-template <int S, int T, bool kEvictFirst = false, int RadFloats = 96, int CoupRow = 15>
+// One warp's stream of tiles over [p0, pe).  kPol is the L2 policy of the
+// perm entries and radial rows the ring brings in, kCoupPol that of the
+// coupling spans (kL2EvictFirst for bytes read exactly once; a coupling span
+// shares its 32-byte sectors with the neighbouring edges' rows, which a
+// gather in CSR order reads later).
+template <int S, int T, int kPol = kL2Normal, int RadFloats = 96, int CoupRow = 15, int kCoupPol = kPol>
 struct TileRing {
     static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
     static_assert(RadFloats % 4 == 0, "radial rows are whole 16-byte pieces");
@@ -127,7 +130,8 @@ struct TileRing {
     // ahead: blk_cur holds the block of tile `issued`, blk_next the one after
     static constexpr int kPB = 32 / T;
     int blk_cur, blk_next;
-    uint64_t pol;      // L2 policy of the ring's copies
+    uint64_t pol;      // L2 policy of the perm entries and radial rows
+    uint64_t pol_c;    // L2 policy of the coupling spans
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int pe_, int lane) {
         rad = reinterpret_cast<float*>(base);
@@ -139,7 +143,8 @@ struct TileRing {
         ntiles = pe > p0 ? (pe - p0 + T - 1) / T : 0;
         issued = 0;
         consumed = 0;
-        pol = kEvictFirst ? l2_evict_first() : l2_evict_normal();
+        pol = l2_policy(kPol);
+        pol_c = l2_policy(kCoupPol);
         if (lane < S) mbar_init(bar0 + 8 * lane, kRingArrivals);
         mbar_fence_init();
         __syncwarp();
@@ -212,7 +217,7 @@ struct TileRing {
                 const uint32_t dst = smem_u32(cslot);
 #pragma unroll
                 for (int k = 0; k < kChunks; ++k)
-                    if (k < nch) cp_async16(dst + 16 * k, src + 16 * k, pol);
+                    if (k < nch) cp_async16(dst + 16 * k, src + 16 * k, pol_c);
             }
         }
         cp_async_arrive(bar);
