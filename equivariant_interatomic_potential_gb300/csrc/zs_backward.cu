@@ -296,6 +296,54 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
 // the CSR-order kernel: one edge per 8-lane group, all 15 rows per lane.
 // --------------------------------------------------------------------------
 
+// Hot destination.  On a skewed graph one node can be the destination of a
+// large share of the edges (a sixth on the Zipf(1.1) graph), and every SM
+// then gathers the same 15 cotangent lines, so the few L2 slices holding them
+// serialise the gathers.  A CTA that sees one destination often among the
+// first 32 edges of its warps' windows copies that node's rows once into a
+// hot slot of its shared memory, and its rings skip the node's gathers.  The
+// consumers read every edge of that node from the slot (the rows are the same
+// bytes wherever they sit, so the results are too).
+#ifndef ZS_BWD_HOT
+#define ZS_BWD_HOT 1
+#endif
+constexpr bool kHotSlot = ZS_BWD_HOT != 0;
+constexpr int kNoHot = -3;                 // matches no destination and no meta marker (-1, -2)
+constexpr int kHotMinSamples = 16;         // of the CTA's 32 x W samples (uniform graphs: about 1)
+constexpr int kHotBytes = 15 * 32 * 4;     // cotangent rows 1..15 at C = 32
+
+// The CTA's hot destination, or kNoHot: each warp votes for the most frequent
+// destination among its 32 samples (sample < 0: none) with that count; the
+// candidate with the largest summed count wins if it reaches kHotMinSamples.
+// Every thread of the CTA must call it (it synchronises the CTA).
+template <int W>
+__device__ int cta_hot_node(int sample, int lane, int warp, int (*cand)[2]) {
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) cnt += __shfl_sync(0xffffffffu, sample, k) == sample ? 1 : 0;
+    if (sample < 0) cnt = 0;
+    const int best = __reduce_max_sync(0xffffffffu, cnt);
+    const unsigned who = __ballot_sync(0xffffffffu, cnt == best);
+    const int val = __shfl_sync(0xffffffffu, sample, __ffs(who) - 1);
+    if (lane == 0) {
+        cand[warp][0] = best > 0 ? val : -1;
+        cand[warp][1] = best;
+    }
+    __syncthreads();
+    // lane w < W sums the counts of the warps voting like warp w; the first
+    // lane with the largest sum names the winner (every warp finds the same)
+    int v = -1, c = 0;
+    if (lane < W) {
+        v = cand[lane][0];
+        if (v >= 0)
+            for (int u = 0; u < W; ++u) c += cand[u][0] == v ? cand[u][1] : 0;
+    }
+    const int top = __reduce_max_sync(0xffffffffu, c);
+    const unsigned lead = __ballot_sync(0xffffffffu, v >= 0 && c == top);
+    const int hv = lead ? __shfl_sync(0xffffffffu, v, __ffs(lead) - 1) : -1;
+    return top >= kHotMinSamples && hv >= 0 ? hv : kNoHot;
+}
+
 // Per edge: the destination's cotangent rows 1..R (R x 32 floats), the
 // radial row (LM x 32) and the coupling row (R), for the ladder of degree LM.
 template <int S, int T, int LM = 3>
@@ -324,6 +372,7 @@ struct EdgeRing {
     int p0, p1, ntiles, issued, consumed;
     int blk_cur, blk_next;   // dst of the 32 edges of the current / next block
     uint64_t pol_stream, pol_g;
+    int hot;        // destination whose cotangent rows the CTA holds in its hot slot, kNoHot for none
 
     __device__ __forceinline__ void init(unsigned char* base, int p0_, int p1_, int lane) {
         gs = reinterpret_cast<float*>(base);
@@ -338,6 +387,7 @@ struct EdgeRing {
         consumed = 0;
         pol_stream = l2_evict_first();
         pol_g = l2_evict_last();
+        hot = kNoHot;
         if (lane < S) mbar_init(bar0 + 8 * lane, 1);
         mbar_fence_init();
         __syncwarp();
@@ -372,9 +422,10 @@ struct EdgeRing {
         const int cnt = imin(T, p1 - e0);
         const bool in = lane < cnt;
         const bool valid = in && d >= 0 && d < N;
+        const bool fetch = valid && d != hot;
         const bool full = cnt == T && coup_bulk && (T * R) % 4 == 0;
-        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-        const uint32_t bytes = (uint32_t)cnt * (RF * 4u) + (full ? (uint32_t)T * R * 4u : 0u) + nvalid * kGBytes;
+        const uint32_t nfetch = __popc(__ballot_sync(0xffffffffu, fetch));
+        const uint32_t bytes = (uint32_t)cnt * (RF * 4u) + (full ? (uint32_t)T * R * 4u : 0u) + nfetch * kGBytes;
         const uint32_t bar = bar0 + 8 * st;
         float* cst = coups + st * T * R;
         if (lane < T) meta[st * T + lane] = valid ? d : (in ? -1 : -2);
@@ -391,7 +442,7 @@ struct EdgeRing {
             if (full) bulk_g2s(smem_u32(cst), coup_g + (int64_t)e0 * R, (uint32_t)T * R * 4u, bar, pol_stream);
         }
         __syncwarp();
-        if (valid)
+        if (fetch)
             bulk_g2s(smem_u32(gs + (st * T + lane) * (R * kC32)), g_g + (int64_t)d * (D * kC32) + kC32, kGBytes,
                      bar, pol_g);
     }
@@ -427,6 +478,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
     const int cld = kGeneral ? cld_arg : 15, dld = kGeneral ? dld_arg : 15;
     const int coup_bulk = kGeneral ? coup_bulk_arg : 1;
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int hot_cand[W][2];
     const int warp = threadIdx.x >> 5;
     const QuadLane Q(threadIdx.x & 31);
     const int gw = blockIdx.x * W + warp;
@@ -437,11 +489,24 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
     EdgeRing<S, T> ring;
     ring.init(smem + (size_t)warp * EdgeRingLayout<S, T>::kBytes, p0, p1, Q.lane);
+    float* hot_g = reinterpret_cast<float*>(smem + (size_t)W * EdgeRingLayout<S, T>::kBytes);
     const uint64_t pol_out = l2_evict_first();
+    int sample = -1;
     if (active) {
         ring.prefetch(dst, Q.lane);
+        sample = ring.blk_cur;
 #pragma unroll
         for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
+    }
+    // the first tiles are in flight (gathered as usual); pick the hot destination meanwhile
+    const int hot = kHotSlot ? cta_hot_node<W>(sample, Q.lane, warp, hot_cand) : kNoHot;
+    if (hot >= 0) {
+        const float4* src = reinterpret_cast<const float4*>(g + (int64_t)hot * (16 * kC32) + kC32);
+        for (int t = threadIdx.x; t < kHotBytes / 16; t += W * 32) reinterpret_cast<float4*>(hot_g)[t] = __ldg(src + t);
+        __syncthreads();
+    }
+    ring.hot = hot;
+    if (active) {
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
             const int e0 = p0 + k * T;
@@ -450,7 +515,7 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 const int j = 4 * i + Q.grp;
                 const int m = ring.meta[st * T + j];
                 const float sc = (scale && m >= 0) ? __ldg(scale + m) : 1.f;   // issued early, used at the stores
-                const float* gj = ring.gs + (st * T + j) * (15 * kC32) + 4 * Q.q;
+                const float* gj = (m == hot ? hot_g : ring.gs + (st * T + j) * (15 * kC32)) + 4 * Q.q;
                 float4 G[15];
 #pragma unroll
                 for (int r = 0; r < 15; ++r) G[r] = *reinterpret_cast<const float4*>(gj + r * kC32);
@@ -629,7 +694,8 @@ void launch_edge_tma(const float* g, const float* coup, int cld, const float* ra
     const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
     const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
     const int64_t ctas = (Wtot + W - 1) / W;
-    const int smem = W * EdgeRingLayout<S, T>::kBytes;
+    const int smem = W * EdgeRingLayout<S, T>::kBytes + kHotBytes;
+    static_assert(W * EdgeRingLayout<S, T>::kBytes + kHotBytes + W * 8 <= 232448, "rings and hot slot fit an SM");
     const int bulk = (cld == 15 && aligned16(coup)) ? 1 : 0;
     if (scale == nullptr && dld == 15 && bulk) {
         static std::atomic<bool> attr_done[kMaxDevices];
