@@ -1,5 +1,5 @@
 // Backward of the zonal scatter, one edge-parallel pass (lmax = 3 ladder shown;
-// the per-channel kernels take any ladder degree 1..5 the same way):
+// every kernel takes the ladders of degree 1..5 the same way):
 //   d_coup[e,r]  = sum_c g[dst[e],1+r,c] * rad[e,slot(r),c]
 //   d_rad[e,s,c] = sum over rows r of slot s of g[dst[e],1+r,c] * coup[e,r]
 // (deepmd-kit pull request "fused Triton zonal scatter for the GIE head",
@@ -173,6 +173,32 @@ __device__ __forceinline__ void group_reduce16(float v[16], const QuadLane& Q, f
     }
 }
 
+// The same transposed butterfly for 8K values: each lane ends with the
+// totals of values 4K*b2 + 2K*b1 + K*b0 + {0..K-1} (K = 2: group_reduce16).
+template <int K>
+__device__ __forceinline__ void group_reduce(const float (&v)[8 * K], const QuadLane& Q, float (&out)[K]) {
+    float w[4 * K];
+#pragma unroll
+    for (int k = 0; k < 4 * K; ++k) {
+        const float keep = Q.b2 ? v[k + 4 * K] : v[k];
+        const float send = Q.b2 ? v[k] : v[k + 4 * K];
+        w[k] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    float x[2 * K];
+#pragma unroll
+    for (int k = 0; k < 2 * K; ++k) {
+        const float keep = Q.b1 ? w[k + 2 * K] : w[k];
+        const float send = Q.b1 ? w[k] : w[k + 2 * K];
+        x[k] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float keep = Q.b0 ? x[k + K] : x[k];
+        const float send = Q.b0 ? x[k] : x[k + K];
+        out[k] = keep + __shfl_xor_sync(kFull, send, 1);
+    }
+}
+
 template <int W, int S, int T>
 __global__ void __launch_bounds__(W * 32, 1)
 bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
@@ -287,13 +313,12 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
 
 // --------------------------------------------------------------------------
 // Edge-order C == 32 backward fed by bulk copies.  A warp owns a window of
-// consecutive edges and streams it in tiles of T edges (T a multiple of 4,
-// tiles start at multiples of 4 so every block below is 16-byte aligned):
-// per tile one bulk copy of the T radial rows, one of the T coupling rows,
-// and per edge one bulk copy of its destination's cotangent rows 1..15
-// (1920 bytes, gathered from L2).  dst is read ahead with plain loads, 32
-// edges at a time, since the gathers need it.  The lane layout is the one of
-// the CSR-order kernel: one edge per 8-lane group, all 15 rows per lane.
+// consecutive edges and streams it in tiles of T edges (tiles start at
+// multiples of T so every block below is 16-byte aligned): per tile one bulk
+// copy of the T radial rows, one of the T coupling rows, and per edge one
+// bulk copy of its destination's cotangent rows 1..R (1920 bytes at lmax 3,
+// gathered from L2).  dst is read ahead with plain loads, 32 edges at a
+// time, since the gathers need it.
 // --------------------------------------------------------------------------
 
 // Hot destination.  On a skewed graph one node can be the destination of a
@@ -310,7 +335,6 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
 constexpr bool kHotSlot = ZS_BWD_HOT != 0;
 constexpr int kNoHot = -3;                 // matches no destination and no meta marker (-1, -2)
 constexpr int kHotMinSamples = 16;         // of the CTA's 32 x W samples (uniform graphs: about 1)
-constexpr int kHotBytes = 15 * 32 * 4;     // cotangent rows 1..15 at C = 32
 
 // The CTA's hot destination, or kNoHot: each warp votes for the most frequent
 // destination among its 32 samples (sample < 0: none) with that count; the
@@ -465,17 +489,28 @@ struct EdgeRing {
     }
 };
 
-// kGeneral: the scaled or strided variant (a node factor, coupling and
-// coupling-gradient rows cld / dld floats apart); the plain operator's
-// instance keeps those at their compile-time defaults.
-template <int W, int S, int T, bool kGeneral>
+// --------------------------------------------------------------------------
+// The edge-order C == 32 backward for the ladder of degree LM in the quad
+// lane layout: one edge per 8-lane group, lane q owns channels 4q..4q+3 of
+// all R rows, each cotangent row is read once from shared memory and feeds
+// both gradients (the radial slot's running sum and the row's dot product
+// with the radial row), and the R coupling-gradient dot products are summed
+// over the group by one transposed butterfly of 8K values, K = ceil(R / 8).
+// --------------------------------------------------------------------------
+
+template <int W, int S, int T, int LM, bool kGeneral>
 __global__ void __launch_bounds__(W * 32, 1)
-bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
-                 const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
-                 float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale_arg,
-                 int cld_arg, int dld_arg, int coup_bulk_arg) {
+bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+              const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
+              float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale_arg,
+              int cld_arg, int dld_arg, int coup_bulk_arg) {
+    static_assert(T % 4 == 0, "tiles hold whole groups of four edges");
+    constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D, RF = LM * kC32;
+    constexpr int K = (R + 7) / 8;
+    using Ring = EdgeRing<S, T, LM>;
+    using Layout = EdgeRingLayout<S, T, LM>;
     const float* __restrict__ scale = kGeneral ? scale_arg : nullptr;
-    const int cld = kGeneral ? cld_arg : 15, dld = kGeneral ? dld_arg : 15;
+    const int cld = kGeneral ? cld_arg : R, dld = kGeneral ? dld_arg : R;
     const int coup_bulk = kGeneral ? coup_bulk_arg : 1;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int hot_cand[W][2];
@@ -487,9 +522,9 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
-    EdgeRing<S, T> ring;
-    ring.init(smem + (size_t)warp * EdgeRingLayout<S, T>::kBytes, p0, p1, Q.lane);
-    float* hot_g = reinterpret_cast<float*>(smem + (size_t)W * EdgeRingLayout<S, T>::kBytes);
+    Ring ring;
+    ring.init(smem + (size_t)warp * Layout::kBytes, p0, p1, Q.lane);
+    float* hot_g = reinterpret_cast<float*>(smem + (size_t)W * Layout::kBytes);
     const uint64_t pol_out = l2_evict_first();
     int sample = -1;
     if (active) {
@@ -498,11 +533,10 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
 #pragma unroll
         for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
     }
-    // the first tiles are in flight (gathered as usual); pick the hot destination meanwhile
     const int hot = kHotSlot ? cta_hot_node<W>(sample, Q.lane, warp, hot_cand) : kNoHot;
     if (hot >= 0) {
-        const float4* src = reinterpret_cast<const float4*>(g + (int64_t)hot * (16 * kC32) + kC32);
-        for (int t = threadIdx.x; t < kHotBytes / 16; t += W * 32) reinterpret_cast<float4*>(hot_g)[t] = __ldg(src + t);
+        const float4* src = reinterpret_cast<const float4*>(g + (int64_t)hot * (D * kC32) + kC32);
+        for (int t = threadIdx.x; t < R * kC32 / 4; t += W * 32) reinterpret_cast<float4*>(hot_g)[t] = __ldg(src + t);
         __syncthreads();
     }
     ring.hot = hot;
@@ -515,141 +549,52 @@ bwd_edge_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, co
                 const int j = 4 * i + Q.grp;
                 const int m = ring.meta[st * T + j];
                 const float sc = (scale && m >= 0) ? __ldg(scale + m) : 1.f;   // issued early, used at the stores
-                const float* gj = (m == hot ? hot_g : ring.gs + (st * T + j) * (15 * kC32)) + 4 * Q.q;
-                float4 G[15];
+                const float* gj = (m == hot ? hot_g : ring.gs + (st * T + j) * (R * kC32)) + 4 * Q.q;
+                const float* rrow = ring.rads + (st * T + j) * RF + 4 * Q.q;
+                float4 a[LM];
 #pragma unroll
-                for (int r = 0; r < 15; ++r) G[r] = *reinterpret_cast<const float4*>(gj + r * kC32);
-                const float* rrow = ring.rads + (st * T + j) * 96 + 4 * Q.q;
-                const float4 a0 = *reinterpret_cast<const float4*>(rrow);
-                const float4 a1 = *reinterpret_cast<const float4*>(rrow + kC32);
-                const float4 a2 = *reinterpret_cast<const float4*>(rrow + 2 * kC32);
-                const float* crow = ring.coups + st * T * 15 + j * 15;
-                float c[15];
+                for (int l = 0; l < LM; ++l) a[l] = *reinterpret_cast<const float4*>(rrow + l * kC32);
+                const float* crow = ring.coups + st * T * R + j * R;
+                float c[R];
 #pragma unroll
-                for (int r = 0; r < 15; ++r) c[r] = crow[r];
-                float4 s0 = make_float4(c[0] * G[0].x, c[0] * G[0].y, c[0] * G[0].z, c[0] * G[0].w);
-                s0 = f4_fma(c[1], G[1], s0);
-                s0 = f4_fma(c[2], G[2], s0);
-                float4 s1 = make_float4(c[3] * G[3].x, c[3] * G[3].y, c[3] * G[3].z, c[3] * G[3].w);
+                for (int r = 0; r < R; ++r) c[r] = crow[r];
+                float4 sl[LM];
+                float pr[8 * K];
 #pragma unroll
-                for (int r = 4; r < 8; ++r) s1 = f4_fma(c[r], G[r], s1);
-                float4 s2 = make_float4(c[8] * G[8].x, c[8] * G[8].y, c[8] * G[8].z, c[8] * G[8].w);
+                for (int r = 0; r < R; ++r) {
+                    const float4 G = *reinterpret_cast<const float4*>(gj + r * kC32);
+                    const int l = ladder_slot(r);
+                    if ((l + 1) * (l + 1) - 1 == r)   // first row of its degree
+                        sl[l] = make_float4(c[r] * G.x, c[r] * G.y, c[r] * G.z, c[r] * G.w);
+                    else
+                        sl[l] = f4_fma(c[r], G, sl[l]);
+                    pr[r] = f4_dot(G, a[l]);
+                }
 #pragma unroll
-                for (int r = 9; r < 15; ++r) s2 = f4_fma(c[r], G[r], s2);
-                float pr[16];
-#pragma unroll
-                for (int r = 0; r < 15; ++r) pr[r] = f4_dot(G[r], r < 3 ? a0 : (r < 8 ? a1 : a2));
-                pr[15] = 0.f;
-                float t0, t1;
-                group_reduce16(pr, Q, t0, t1);
+                for (int r = R; r < 8 * K; ++r) pr[r] = 0.f;
+                float t[K];
+                group_reduce<K>(pr, Q, t);
                 if (m == -2) continue;
                 const bool ok = m >= 0;
                 const int64_t e = e0 + j;
-                const int row = 8 * Q.b2 + 4 * Q.b1 + 2 * Q.b0;
+                const int row = 4 * K * Q.b2 + 2 * K * Q.b1 + K * Q.b0;
                 float* dc = d_coup + e * dld + row;
-                float* dr = d_rad + e * (3 * kC32) + 4 * Q.q;
+                float* dr = d_rad + e * RF + 4 * Q.q;
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (scale && ok) {   // gradients of the scaled output: the destination's scale times these
-                    s0 = make_float4(s0.x * sc, s0.y * sc, s0.z * sc, s0.w * sc);
-                    s1 = make_float4(s1.x * sc, s1.y * sc, s1.z * sc, s1.w * sc);
-                    s2 = make_float4(s2.x * sc, s2.y * sc, s2.z * sc, s2.w * sc);
-                    t0 *= sc;
-                    t1 *= sc;
+#pragma unroll
+                    for (int l = 0; l < LM; ++l) sl[l] = make_float4(sl[l].x * sc, sl[l].y * sc, sl[l].z * sc, sl[l].w * sc);
+#pragma unroll
+                    for (int q = 0; q < K; ++q) t[q] *= sc;
                 }
-                st_hint4(dr, ok ? s0 : z, pol_out);
-                st_hint4(dr + kC32, ok ? s1 : z, pol_out);
-                st_hint4(dr + 2 * kC32, ok ? s2 : z, pol_out);
-                st_stream(dc, ok ? t0 : 0.f);
-                if (row + 1 < 15) st_stream(dc + 1, ok ? t1 : 0.f);
+#pragma unroll
+                for (int l = 0; l < LM; ++l) st_hint4(dr + l * kC32, ok ? sl[l] : z, pol_out);
+#pragma unroll
+                for (int q = 0; q < K; ++q)
+                    if (row + q < R) st_stream(dc + q, ok ? t[q] : 0.f);
             }
             __syncwarp();
             ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
-        }
-    }
-    ring.drain();
-}
-
-// --------------------------------------------------------------------------
-// Edge-order backward at C = 32 for the other ladders, fed by the same
-// bulk-copy ring, with no cross-lane reduction: d_rad with lane = channel
-// (d_rad[e,s,c] sums the rows of slot s: R smem loads and FMAs per lane),
-// d_coup with lane = row (d_coup[e,r] is a 32-channel dot product of the
-// cotangent row and the radial row, read as 16-byte pieces in an order
-// rotated by the lane so that a quarter-warp touches eight different bank
-// groups).  Rows beyond 32 take a second pass.
-// --------------------------------------------------------------------------
-
-template <int W, int S, int T, int LM>
-__global__ void __launch_bounds__(W * 32, 1)
-bwd_edge_rows(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
-              const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
-              float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale,
-              int cld, int dld, int coup_bulk) {
-    using Ring = EdgeRing<S, T, LM>;
-    constexpr int R = Ring::R, RF = Ring::RF;
-    constexpr int kPasses = (R + 31) / 32;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * W + warp;
-    const bool active = gw < Wtot;
-    pdl_wait();
-    pdl_trigger();
-    const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
-    const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
-    Ring ring;
-    ring.init(smem + (size_t)warp * Ring::Layout::kBytes, p0, p1, lane);
-    const uint64_t pol_out = l2_evict_first();
-    int rslot[kPasses];   // radial slot of this lane's coupling-gradient row in each pass
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) rslot[ps] = ladder_slot(imin(32 * ps + lane, R - 1));
-    if (active) {
-        ring.prefetch(dst, lane);
-#pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, lane);
-        for (int k = 0; k < ring.ntiles; ++k) {
-            const int st = ring.acquire();
-            const int e0 = p0 + k * T;
-#pragma unroll
-            for (int j = 0; j < T; ++j) {
-                const int m = ring.meta[st * T + j];
-                if (m == -2) continue;
-                const bool ok = m >= 0;
-                const float sc = (scale && ok) ? __ldg(scale + m) : 1.f;
-                const int64_t e = e0 + j;
-                const float* gj = ring.gs + (st * T + j) * (R * kC32);
-                const float* rj = ring.rads + (st * T + j) * RF;
-                const float* cj = ring.coups + st * T * R + j * R;
-                // d_rad: lane = channel
-                float sv[LM];
-#pragma unroll
-                for (int q = 0; q < LM; ++q) sv[q] = 0.f;
-#pragma unroll
-                for (int r = 0; r < R; ++r) sv[ladder_slot(r)] = fmaf(gj[r * kC32 + lane], cj[r], sv[ladder_slot(r)]);
-                float* dr = d_rad + e * RF + lane;
-#pragma unroll
-                for (int q = 0; q < LM; ++q) st_hint(dr + q * kC32, ok ? (scale ? sv[q] * sc : sv[q]) : 0.f, pol_out);
-                // d_coup: lane = row
-#pragma unroll
-                for (int ps = 0; ps < kPasses; ++ps) {
-                    const int row = 32 * ps + lane;
-                    if (kPasses > 1 && 32 * ps >= R) break;
-                    const float4* grow = reinterpret_cast<const float4*>(gj + imin(row, R - 1) * kC32);
-                    const float4* rrow = reinterpret_cast<const float4*>(rj + rslot[ps] * kC32);
-                    float acc = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const int ch = (kk + lane) & 7;
-                        const float4 a = grow[ch], b = rrow[ch];
-                        acc = fmaf(a.x, b.x, acc);
-                        acc = fmaf(a.y, b.y, acc);
-                        acc = fmaf(a.z, b.z, acc);
-                        acc = fmaf(a.w, b.w, acc);
-                    }
-                    if (row < R) st_stream(d_coup + e * dld + row, ok ? (scale ? acc * sc : acc) : 0.f);
-                }
-            }
-            __syncwarp();
-            ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, lane);
         }
     }
     ring.drain();
@@ -686,29 +631,6 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
 constexpr int64_t kSmallCotangentBytes = int64_t(16) << 20;   // 16 MiB
 constexpr int kEdgeWarpsSmall = 12;   // 2-stage rings of 4 edges: 12 warps fit one SM's shared memory
 constexpr int kEdgeWarpsLarge = 8;    // 3-stage rings of 4 edges: 8 warps
-
-template <int W, int S, int T>
-void launch_edge_tma(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
-                     int32_t N, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
-    const int64_t warps_max = (int64_t)num_sms() * W;
-    const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
-    const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
-    const int64_t ctas = (Wtot + W - 1) / W;
-    const int smem = W * EdgeRingLayout<S, T>::kBytes + kHotBytes;
-    static_assert(W * EdgeRingLayout<S, T>::kBytes + kHotBytes + W * 8 <= 232448, "rings and hot slot fit an SM");
-    const int bulk = (cld == 15 && aligned16(coup)) ? 1 : 0;
-    if (scale == nullptr && dld == 15 && bulk) {
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(bwd_edge_c32_tma<W, S, T, false>, smem, attr_done);
-        launch(bwd_edge_c32_tma<W, S, T, false>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
-               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
-    } else {
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(bwd_edge_c32_tma<W, S, T, true>, smem, attr_done);
-        launch(bwd_edge_c32_tma<W, S, T, true>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
-               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
-    }
-}
 
 // One warp waits on an mbarrier that nothing arrives on, with a limit of
 // max_spins tries: the wait gives up, counts a timeout and the kernel ends.
@@ -774,61 +696,84 @@ bwd_scale_grad(const float* __restrict__ g, const float* __restrict__ raw, int32
     if (lane == 0) d_scale[n] = acc;
 }
 
-// Ring shape of the other ladders' edge backward (tile edges and stages per
-// ladder degree 1, 2, 4, 5, picked by timing on the n4096 graph); as many
-// warps (up to 16) as one SM's shared memory holds.
-#ifndef ZS_ROWS_T1
-#define ZS_ROWS_T1 8
-#endif
-#ifndef ZS_ROWS_T2
-#define ZS_ROWS_T2 8
-#endif
-#ifndef ZS_ROWS_T4
-#define ZS_ROWS_T4 2
-#endif
-#ifndef ZS_ROWS_T5
-#define ZS_ROWS_T5 4
-#endif
-#ifndef ZS_ROWS_S1
-#define ZS_ROWS_S1 3
-#endif
-#ifndef ZS_ROWS_S2
-#define ZS_ROWS_S2 2
-#endif
-#ifndef ZS_ROWS_S4
-#define ZS_ROWS_S4 3
-#endif
-#ifndef ZS_ROWS_S5
-#define ZS_ROWS_S5 2
-#endif
 template <int LM>
 constexpr int rows_pick(const int (&v)[4]) { return v[LM <= 2 ? LM - 1 : LM - 2]; }
-constexpr int kRowsTiles[4] = {ZS_ROWS_T1, ZS_ROWS_T2, ZS_ROWS_T4, ZS_ROWS_T5};
-constexpr int kRowsStages[4] = {ZS_ROWS_S1, ZS_ROWS_S2, ZS_ROWS_S4, ZS_ROWS_S5};
+
+// Quad-layout edge backward of the other ladders: tiles of whole quads;
+// stages and tile per ladder (chosen by timing), as many warps as the rings
+// and the hot slot leave room for, at most 16.  lmax 3 uses the fixed
+// configurations below (kEdgeWarpsSmall / kEdgeWarpsLarge).
+#ifndef ZS_QUAD_T1
+#define ZS_QUAD_T1 8
+#endif
+#ifndef ZS_QUAD_T2
+#define ZS_QUAD_T2 4
+#endif
+#ifndef ZS_QUAD_T4
+#define ZS_QUAD_T4 4
+#endif
+#ifndef ZS_QUAD_T5
+#define ZS_QUAD_T5 4
+#endif
+#ifndef ZS_QUAD_S1
+#define ZS_QUAD_S1 3
+#endif
+#ifndef ZS_QUAD_S2
+#define ZS_QUAD_S2 3
+#endif
+#ifndef ZS_QUAD_S4
+#define ZS_QUAD_S4 2
+#endif
+#ifndef ZS_QUAD_S5
+#define ZS_QUAD_S5 2
+#endif
+// per ladder degree 1, 2, 4, 5
+constexpr int kQuadTiles[4] = {ZS_QUAD_T1, ZS_QUAD_T2, ZS_QUAD_T4, ZS_QUAD_T5};
+constexpr int kQuadStages[4] = {ZS_QUAD_S1, ZS_QUAD_S2, ZS_QUAD_S4, ZS_QUAD_S5};
 template <int LM>
-constexpr int rows_tile() { return rows_pick<LM>(kRowsTiles); }
+constexpr int quad_tile() { return rows_pick<LM>(kQuadTiles); }
 template <int LM>
-constexpr int rows_stages() { return rows_pick<LM>(kRowsStages); }
+constexpr int quad_stages() { return rows_pick<LM>(kQuadStages); }
 template <int LM>
-constexpr int rows_warps() {
-    constexpr int bytes = EdgeRingLayout<rows_stages<LM>(), rows_tile<LM>(), LM>::kBytes;
-    return (232448 / bytes) < 16 ? (232448 / bytes) : 16;
+constexpr int quad_hot_bytes() { return Ladder<LM>::R * kC32 * 4; }
+template <int LM>
+constexpr int quad_warps() {
+    constexpr int bytes = EdgeRingLayout<quad_stages<LM>(), quad_tile<LM>(), LM>::kBytes;
+    constexpr int avail = 232448 - quad_hot_bytes<LM>() - 16 * 8;   // the hot slot, the votes
+    return avail / bytes < 16 ? avail / bytes : 16;
 }
 
-template <int LM>
-void launch_edge_rows(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
+template <int LM, int W, int S, int T>
+void launch_edge_quad(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst, int64_t E,
                       int32_t N, float* d_coup, int dld, float* d_rad, const float* scale, cudaStream_t s) {
-    constexpr int W = rows_warps<LM>(), T = rows_tile<LM>(), S = rows_stages<LM>();
+    constexpr int R = Ladder<LM>::R;
     const int64_t warps_max = (int64_t)num_sms() * W;
     const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max + T - 1, T) / T * T;   // whole tiles
     const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
     const int64_t ctas = (Wtot + W - 1) / W;
-    const int smem = W * EdgeRingLayout<S, T, LM>::kBytes;
-    const int bulk = (cld == Ladder<LM>::R && aligned16(coup)) ? 1 : 0;
-    static std::atomic<bool> attr_done[kMaxDevices];
-    set_smem_limit_once(bwd_edge_rows<W, S, T, LM>, smem, attr_done);
-    launch(bwd_edge_rows<W, S, T, LM>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N, (int)KW,
-           (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+    const int smem = W * EdgeRingLayout<S, T, LM>::kBytes + quad_hot_bytes<LM>();
+    static_assert(W * EdgeRingLayout<S, T, LM>::kBytes + quad_hot_bytes<LM>() + W * 8 <= 232448,
+                  "rings and hot slot fit an SM");
+    const int bulk = (cld == R && aligned16(coup)) ? 1 : 0;
+    if (scale == nullptr && dld == R && bulk) {
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_edge_quad<W, S, T, LM, false>, smem, attr_done);
+        launch(bwd_edge_quad<W, S, T, LM, false>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+    } else {
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_smem_limit_once(bwd_edge_quad<W, S, T, LM, true>, smem, attr_done);
+        launch(bwd_edge_quad<W, S, T, LM, true>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+    }
+}
+
+template <int LM>
+void launch_edge_quad_auto(const float* g, const float* coup, int cld, const float* rad, const int32_t* dst,
+                           int64_t E, int32_t N, float* d_coup, int dld, float* d_rad, const float* scale,
+                           cudaStream_t s) {
+    launch_edge_quad<LM, quad_warps<LM>(), quad_stages<LM>(), quad_tile<LM>()>(g, coup, cld, rad, dst, E, N, d_coup,
+                                                                                dld, d_rad, scale, s);
 }
 
 template <int L>
@@ -869,14 +814,14 @@ static zs_status backward_impl(const char* name, const float* g, const float* co
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "%s: g is NULL with N > 0", name);
     // coupling rows and d_coup may have any stride and 4-byte alignment on every path
     const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad);
-    const bool rows = lmax != 3 && C == kC32 && aligned16(g) && aligned16(rad);
+    const bool rows = lmax != 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad);
     if (rows) {
         const int c = (int)cld, d = (int)dld;
         switch (lmax) {
-            case 1: launch_edge_rows<1>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
-            case 2: launch_edge_rows<2>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
-            case 4: launch_edge_rows<4>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
-            default: launch_edge_rows<5>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            case 1: launch_edge_quad_auto<1>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            case 2: launch_edge_quad_auto<2>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            case 4: launch_edge_quad_auto<4>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
+            default: launch_edge_quad_auto<5>(g, coup, c, rad, dst, E, N, d_coup, d, d_rad, scale, s); break;
         }
     } else if (fast) {
         // While the cotangent block is small enough to stay in L2 next to the
@@ -885,9 +830,9 @@ static zs_status backward_impl(const char* name, const float* g, const float* co
         // tiles in flight per warp.
         const bool small_g = (int64_t)N * 16 * kC32 * 4 <= kSmallCotangentBytes;
         if (small_g)
-            launch_edge_tma<kEdgeWarpsSmall, 2, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
+            launch_edge_quad<3, kEdgeWarpsSmall, 2, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
         else
-            launch_edge_tma<kEdgeWarpsLarge, 3, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
+            launch_edge_quad<3, kEdgeWarpsLarge, 3, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
     } else {
         const int c = (int)cld, d = (int)dld;
         switch (lmax) {
