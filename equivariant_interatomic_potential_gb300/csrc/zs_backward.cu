@@ -148,33 +148,9 @@ struct QuadLane {
         : lane(l), grp(l >> 3), q(l & 7), b2((l & 4) != 0), b1((l & 2) != 0), b0((l & 1) != 0) {}
 };
 
-// Sum of v over the 8 lanes of the group for 16 values at once: each lane
-// ends with the totals of rows 8*b2 + 4*b1 + 2*b0 + {0, 1}.
-__device__ __forceinline__ void group_reduce16(float v[16], const QuadLane& Q, float& r0, float& r1) {
-    float w[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float keep = Q.b2 ? v[k + 8] : v[k];
-        const float send = Q.b2 ? v[k] : v[k + 8];
-        w[k] = keep + __shfl_xor_sync(kFull, send, 4);
-    }
-    float x[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float keep = Q.b1 ? w[k + 4] : w[k];
-        const float send = Q.b1 ? w[k] : w[k + 4];
-        x[k] = keep + __shfl_xor_sync(kFull, send, 2);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float keep = Q.b0 ? x[k + 2] : x[k];
-        const float send = Q.b0 ? x[k] : x[k + 2];
-        (k == 0 ? r0 : r1) = keep + __shfl_xor_sync(kFull, send, 1);
-    }
-}
-
-// The same transposed butterfly for 8K values: each lane ends with the
-// totals of values 4K*b2 + 2K*b1 + K*b0 + {0..K-1} (K = 2: group_reduce16).
+// Sum of v over the 8 lanes of the group for 8K values at once, by a
+// transposed butterfly (each step halves the values a lane carries): each
+// lane ends with the totals of values 4K*b2 + 2K*b1 + K*b0 + {0..K-1}.
 template <int K>
 __device__ __forceinline__ void group_reduce(const float (&v)[8 * K], const QuadLane& Q, float (&out)[K]) {
     float w[4 * K];
@@ -199,13 +175,20 @@ __device__ __forceinline__ void group_reduce(const float (&v)[8 * K], const Quad
     }
 }
 
-template <int W, int S, int T>
+template <int W, int S, int T, int LM>
 __global__ void __launch_bounds__(W * 32, 1)
-bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
-                const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-                int E, int32_t N, int KW, int Wtot,
-                float* __restrict__ d_coup, float* __restrict__ d_rad) {
+bwd_csr_quad(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
+             const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+             int E, int32_t N, int KW, int Wtot,
+             float* __restrict__ d_coup, float* __restrict__ d_rad) {
     static_assert(T % 4 == 0, "tiles hold whole groups of four edges");
+    constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D, RF = LM * kC32;
+    constexpr int K = (R + 7) / 8;                   // coupling-gradient values per lane
+    constexpr int kSlot = coup_slot_floats(R);
+    // a node's R cotangent rows: in registers up to 24 rows, else in this
+    // lane's own column of shared memory ([row][lane] float4, no sharing)
+    constexpr bool kSmemG = R > 24;
+    using Ring = TileRing<S, T, kL2EvictFirst, RF, R, ZS_BWDC_COUP_POL>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const QuadLane Q(threadIdx.x & 31);
@@ -215,24 +198,33 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
     pdl_trigger();
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
-    TileRing<S, T, kL2EvictFirst, 96, 15, ZS_BWDC_COUP_POL> ring;
-    ring.init(smem + (size_t)warp * RingLayout<S, T>::kBytes, p0, p1, Q.lane);
+    Ring ring;
+    ring.init(smem + (size_t)warp * Ring::Layout::kBytes, p0, p1, Q.lane);
     const uint64_t pol_first = l2_evict_first(), pol_last = l2_evict_last();
     if (active) {
         ring.prefetch_perm(perm, Q.lane);
 #pragma unroll
-        for (int i = 0; i < S; ++i) ring.issue(perm, coup, 15, rad, E, Q.lane);
+        for (int i = 0; i < S; ++i) ring.issue(perm, coup, R, rad, E, Q.lane);
         const int vend = __ldg(row_ptr + N);
-        // this group's node: n covers positions [.., b); G holds its rows 1..15
+        // this group's node: n covers positions [.., b); G holds its rows 1..R
         int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
         int b = n < N ? __ldg(row_ptr + n + 1) : 0;
         int c = 0;   // row_ptr[n + 2], fetched one node ahead
-        float4 G[15];
+        float4 G[kSmemG ? 1 : R];
+        float4* gsm = reinterpret_cast<float4*>(smem + (size_t)W * Ring::Layout::kBytes) + (size_t)warp * R * 32 + Q.lane;
+        auto put_g = [&](int r, float4 v) {
+            if constexpr (kSmemG) gsm[r * 32] = v;
+            else G[r] = v;
+        };
+        auto get_g = [&](int r) -> float4 {
+            if constexpr (kSmemG) return gsm[r * 32];
+            else return G[r];
+        };
         const float* gq = g + 4 * Q.q;
         auto load_g = [&]() {
-            const float* gn = gq + (int64_t)n * (16 * kC32);
+            const float* gn = gq + (int64_t)n * (D * kC32);
 #pragma unroll
-            for (int r = 0; r < 15; ++r) G[r] = ld_ro4(gn + (1 + r) * kC32);
+            for (int r = 0; r < R; ++r) put_g(r, ld_ro4(gn + (1 + r) * kC32));
         };
         if (p0 < vend) {
             while (b <= p0) b = __ldg(row_ptr + (++n) + 1);
@@ -240,14 +232,14 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
             load_g();
         } else {
 #pragma unroll
-            for (int r = 0; r < 15; ++r) G[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < R; ++r) put_g(r, make_float4(0.f, 0.f, 0.f, 0.f));
         }
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
             const int tb = p0 + k * T;
             const int jt = imin(T, p1 - tb);
-            const float* radst = ring.rad + st * T * 96 + 4 * Q.q;
-            const float* coupst = ring.coup + st * T * kCoupSlotFloats;
+            const float* radst = ring.rad + st * T * RF + 4 * Q.q;
+            const float* coupst = ring.coup + st * T * kSlot;
             const int2* metast = ring.meta + st * T;
 #pragma unroll 1
             for (int i = 0; i < T / 4; ++i) {
@@ -264,48 +256,47 @@ bwd_csr_c32_tma(const float* __restrict__ g, const float* __restrict__ coup, con
                     load_g();
                 }
                 const int2 m = metast[j];
-                const float* rrow = radst + j * 96;
-                const float4 a0 = *reinterpret_cast<const float4*>(rrow);
-                const float4 a1 = *reinterpret_cast<const float4*>(rrow + kC32);
-                const float4 a2 = *reinterpret_cast<const float4*>(rrow + 2 * kC32);
-                const float* crow = coupst + j * kCoupSlotFloats + m.y;
-                float c[15];
+                const float* rrow = radst + j * RF;
+                float4 a[LM];
 #pragma unroll
-                for (int r = 0; r < 15; ++r) c[r] = crow[r];
-                // radial gradient, one slot per degree group of rows
-                float4 s0 = make_float4(c[0] * G[0].x, c[0] * G[0].y, c[0] * G[0].z, c[0] * G[0].w);
-                s0 = f4_fma(c[1], G[1], s0);
-                s0 = f4_fma(c[2], G[2], s0);
-                float4 s1 = make_float4(c[3] * G[3].x, c[3] * G[3].y, c[3] * G[3].z, c[3] * G[3].w);
-#pragma unroll
-                for (int r = 4; r < 8; ++r) s1 = f4_fma(c[r], G[r], s1);
-                float4 s2 = make_float4(c[8] * G[8].x, c[8] * G[8].y, c[8] * G[8].z, c[8] * G[8].w);
-#pragma unroll
-                for (int r = 9; r < 15; ++r) s2 = f4_fma(c[r], G[r], s2);
+                for (int l = 0; l < LM; ++l) a[l] = *reinterpret_cast<const float4*>(rrow + l * kC32);
+                const float* crow = coupst + j * kSlot + m.y;
+                // radial gradient: one running sum per degree slot, rows in order;
                 // coupling gradient: per-row dot products over this lane's channels,
                 // then summed over the group's 8 lanes
-                float pr[16];
+                float4 sl[LM];
+                float pr[8 * K];
 #pragma unroll
-                for (int r = 0; r < 15; ++r) pr[r] = f4_dot(G[r], r < 3 ? a0 : (r < 8 ? a1 : a2));
-                pr[15] = 0.f;
-                float t0, t1;
-                group_reduce16(pr, Q, t0, t1);
+                for (int r = 0; r < R; ++r) {
+                    const float cr = crow[r];
+                    const float4 Gr = get_g(r);
+                    const int l = ladder_slot(r);
+                    if ((l + 1) * (l + 1) - 1 == r)   // first row of its degree
+                        sl[l] = make_float4(cr * Gr.x, cr * Gr.y, cr * Gr.z, cr * Gr.w);
+                    else
+                        sl[l] = f4_fma(cr, Gr, sl[l]);
+                    pr[r] = f4_dot(Gr, a[l]);
+                }
+#pragma unroll
+                for (int r = R; r < 8 * K; ++r) pr[r] = 0.f;
+                float t[K];
+                group_reduce<K>(pr, Q, t);
                 const int e = m.x;
                 if (in && e >= 0) {
-                    const int row = 8 * Q.b2 + 4 * Q.b1 + 2 * Q.b0;
-                    float* dc = d_coup + (int64_t)e * 15 + row;
-                    float* dr = d_rad + (int64_t)e * (3 * kC32) + 4 * Q.q;
+                    const int row = 4 * K * Q.b2 + 2 * K * Q.b1 + K * Q.b0;
+                    float* dc = d_coup + (int64_t)e * R + row;
+                    float* dr = d_rad + (int64_t)e * RF + 4 * Q.q;
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    // d_rad rows are whole lines: stream them out.  d_coup rows are 60 bytes in
+                    // d_rad rows are whole lines: stream them out.  d_coup rows are 4R bytes in
                     // random order: keep their lines in L2 until neighbouring rows fill them
-                    st_hint4(dr, has_node ? s0 : z, pol_first);
-                    st_hint4(dr + kC32, has_node ? s1 : z, pol_first);
-                    st_hint4(dr + 2 * kC32, has_node ? s2 : z, pol_first);
-                    st_hint(dc, has_node ? t0 : 0.f, pol_last);
-                    if (row + 1 < 15) st_hint(dc + 1, has_node ? t1 : 0.f, pol_last);
+#pragma unroll
+                    for (int l = 0; l < LM; ++l) st_hint4(dr + l * kC32, has_node ? sl[l] : z, pol_first);
+#pragma unroll
+                    for (int q = 0; q < K; ++q)
+                        if (row + q < R) st_hint(dc + q, has_node ? t[q] : 0.f, pol_last);
                 }
             }
-            ring.refill(perm, coup, 15, rad, E, Q.lane);
+            ring.refill(perm, coup, R, rad, E, Q.lane);
         }
     }
     ring.drain();
@@ -784,6 +775,30 @@ void launch_gen_edges(const float* g, const float* coup, int cld, const float* r
     launch(bwd_gen<L>, grid, kBwdThreads, 0, s, g, coup, rad, dst, E, N, C, d_coup, d_rad, scale, cld, dld);
 }
 
+// CSR-order quad kernel: lmax 4 keeps 24 cotangent rows (96 registers) per
+// lane, so fewer warps (more registers each) than the other ladders; lmax 5
+// keeps its 35 rows in shared memory (17.5 KB a warp), so fewer, smaller tiles.
+constexpr int kCsrQuadWarps4 = 8;
+constexpr int kCsrQuadWarps5 = 8, kCsrQuadTile5 = 4;
+
+template <int LM, int W, int S, int T>
+void launch_csr_quad(const float* g, const float* coup, const float* rad, const int32_t* row_ptr,
+                     const int32_t* perm, int64_t E, int32_t N, float* d_coup, float* d_rad, cudaStream_t s) {
+    constexpr int R = Ladder<LM>::R;
+    using Layout = RingLayout<S, T, LM * kC32, R>;
+    const int64_t warps_max = (int64_t)num_sms() * W;
+    const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max, T);
+    const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
+    const int64_t ctas = (Wtot + W - 1) / W;
+    constexpr int kGBytes = R > 24 ? R * 32 * 16 : 0;   // shared-memory cotangent rows per warp
+    static_assert(W * (Layout::kBytes + kGBytes) <= 232448, "rings and cotangent rows fit an SM");
+    const int smem = W * (Layout::kBytes + kGBytes);
+    static std::atomic<bool> attr_done[kMaxDevices];
+    set_smem_limit_once(bwd_csr_quad<W, S, T, LM>, smem, attr_done);
+    launch(bwd_csr_quad<W, S, T, LM>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
+           (int)KW, (int)Wtot, d_coup, d_rad);
+}
+
 template <int L>
 void launch_gen_csr(const float* g, const float* coup, const float* rad, const int32_t* row_ptr,
                     const int32_t* perm, int64_t E, int32_t N, int C, float* d_coup, float* d_rad, cudaStream_t s) {
@@ -897,18 +912,18 @@ extern "C" zs_status zs_backward_csr(const float* g, const float* coup, const fl
     if (!coup || !rad || !perm || !d_coup || !d_rad) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: NULL array with E > 0");
     if (N > 0 && !g) return fail(ZS_ERR_INVALID_ARG, "zs_backward_csr: g is NULL with N > 0");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool fast = lmax == 3 && C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
+    const bool fast = C == kC32 && aligned16(g) && aligned16(rad) && aligned16(d_rad) && aligned16(coup);
     if (fast) {
-        constexpr int W = ZS_BWD_WARPS, S = ZS_BWD_STAGES, T = ZS_BWD_TILE;
-        const int64_t warps_max = (int64_t)num_sms() * W;
-        const int64_t KW = imax<int64_t>((E + warps_max - 1) / warps_max, T);
-        const int64_t Wtot = imax<int64_t>((E + KW - 1) / KW, 1);
-        const int64_t ctas = (Wtot + W - 1) / W;
-        const int smem = W * RingLayout<S, T>::kBytes;
-        static std::atomic<bool> attr_done[kMaxDevices];
-        set_smem_limit_once(bwd_csr_c32_tma<W, S, T>, smem, attr_done);
-        launch(bwd_csr_c32_tma<W, S, T>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
-               (int)KW, (int)Wtot, d_coup, d_rad);
+        constexpr int S = ZS_BWD_STAGES, T = ZS_BWD_TILE;
+        switch (lmax) {
+            case 1: launch_csr_quad<1, ZS_BWD_WARPS, S, T>(g, coup, rad, row_ptr, perm, E, N, d_coup, d_rad, s); break;
+            case 2: launch_csr_quad<2, ZS_BWD_WARPS, S, T>(g, coup, rad, row_ptr, perm, E, N, d_coup, d_rad, s); break;
+            case 3: launch_csr_quad<3, ZS_BWD_WARPS, S, T>(g, coup, rad, row_ptr, perm, E, N, d_coup, d_rad, s); break;
+            case 4: launch_csr_quad<4, kCsrQuadWarps4, S, T>(g, coup, rad, row_ptr, perm, E, N, d_coup, d_rad, s); break;
+            default:
+                launch_csr_quad<5, kCsrQuadWarps5, S, kCsrQuadTile5>(g, coup, rad, row_ptr, perm, E, N, d_coup, d_rad, s);
+                break;
+        }
     } else {
         switch (lmax) {
             case 1: launch_gen_csr<1>(g, coup, rad, row_ptr, perm, E, N, C, d_coup, d_rad, s); break;
