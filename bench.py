@@ -494,11 +494,31 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (h_dst, h_coup, h_rad, h_g))
         d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dc, h_dr))
+        # what the host link allows: the same copies, both directions at once, no kernels
+        a2 = torch.cuda.Event(enable_timing=True)
+        b2 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a2.record(s_in[0])
+        s_out[0].wait_event(a2)
+        for i in range(args.steps):
+            B = bufs[i % 2]
+            with torch.cuda.stream(s_in[0]):
+                for d, src in ((B["dst"], h_dst), (B["coup"], h_coup), (B["rad"], h_rad), (B["g"], h_g)):
+                    d.copy_(src, non_blocking=True)
+            with torch.cuda.stream(s_out[0]):
+                for d, src in ((h_out, B["out"]), (h_dc, B["d_coup"]), (h_dr, B["d_rad"])):
+                    d.copy_(src, non_blocking=True)
+        s_in[0].wait_stream(s_out[0])
+        b2.record(s_in[0])
+        torch.cuda.synchronize()
+        link_ms = a2.elapsed_time(b2) / args.steps
         e2e = {"value": job_throughput(E, args.steps, e2e_ms, world), "unit": "edges/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps,
                "pipeline": f"two buffer sets: step i+1's host-to-device copies and step i-1's device-to-host "
-                           f"copies overlap step i; each copy split over {n_copy} stream(s) per direction"}
+                           f"copies overlap step i; each copy split over {n_copy} stream(s) per direction",
+               "host_link": {"ms_per_step": link_ms, "GBs": (h2d + d2h) / (link_ms * 1e-3) / 1e9,
+                             "how": "the same copies alone, host to device and device to host at once"}}
 
     total_ms = reduce_max(total_ms, world, dev)
     if rank != 0:
