@@ -22,9 +22,9 @@
  * Every entry point with an lmax argument also takes the other ladders
  * lmax = 1..5 (an extension of the pages' operator, same definitions):
  * D = (lmax+1)^2, R = D - 1, degree l holding rows [l^2 - 1, (l+1)^2 - 1),
- * coup (E, R), rad (E, lmax, C), out and g (N, D, C).  lmax = 3 with C = 32
- * and 16-byte aligned operands takes the tuned kernels; every other shape
- * takes per-channel kernels.
+ * coup (E, R), rad (E, lmax, C), out and g (N, D, C).  C = 32 with 16-byte
+ * aligned operands takes the vectorised kernels at every lmax (tuned at
+ * lmax = 3); every other shape takes per-channel kernels.
  *   forward:  out[n,0,c] = 0,
  *             out[n,1+r,c] = sum over CSR positions j of node n, in order,
  *                            of coup[e,r] * rad[e,s(r),c], e = perm[j]
