@@ -252,8 +252,9 @@ struct QuadLayout {
 };
 
 // ChanLayout (any ladder): lane = channel, all R rows per lane; per edge
-// lmax LDS.32 of radial values, R broadcast LDS.32 of coupling values and R
-// FFMA per lane.  Node rows are written as 128-byte lines.
+// lmax LDS.32 of radial values, R broadcast LDS.32 of coupling values (at
+// lmax 4, (R + 6) / 4 broadcast LDS.128) and R FFMA per lane.  Node rows are
+// written as 128-byte lines.
 template <int LM>
 struct ChanLayout {
     // small rows: more edges per tile keep more bytes in flight (measured
@@ -286,13 +287,45 @@ struct ChanLayout {
 #pragma unroll
         for (int r = 0; r < R; ++r) a.v[r] = 0.f;
     }
+    // At lmax 4 the coupling span is read as kSlot / 4 broadcast 16-byte
+    // loads; the row starts O floats into it (O = 0..3, the same for every
+    // lane), so the FMAs are unrolled once per O and picked by a warp-uniform
+    // switch.  Each accumulator still takes one FMA per edge in edge order.
+    // Measured on the n4096 graph: lmax 4 98 -> 88 us; lmax 2 unchanged and
+    // lmax 1 slower (3 rows do not pay for the switch); lmax 5 would spill
+    // (35 accumulators), so those keep one broadcast LDS.32 per row.
+    static constexpr bool kVecCoup = R >= 16 && R <= 24;
+    template <int O>
+    __device__ __forceinline__ static void fma_rows(const float (&cf)[kSlot], const float (&rv)[LM], Acc& a) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = fmaf(cf[O + r], rv[ladder_slot(r)], a.v[r]);
+    }
     __device__ __forceinline__ void add(const View& v, int j, Acc& a) const {
-        const float* cr = v.cp + j * kSlot + v.mt[j].y;
         float rv[LM];
 #pragma unroll
         for (int k = 0; k < LM; ++k) rv[k] = v.ra[j * kRadFloats + k * kC32];
+        if constexpr (kVecCoup) {
+            const float4* cq = reinterpret_cast<const float4*>(v.cp + j * kSlot);
+            float cf[kSlot];
 #pragma unroll
-        for (int r = 0; r < R; ++r) a.v[r] = fmaf(cr[r], rv[ladder_slot(r)], a.v[r]);
+            for (int k = 0; k < kSlot / 4; ++k) {
+                const float4 q = cq[k];
+                cf[4 * k] = q.x;
+                cf[4 * k + 1] = q.y;
+                cf[4 * k + 2] = q.z;
+                cf[4 * k + 3] = q.w;
+            }
+            switch (v.mt[j].y) {
+                case 0: fma_rows<0>(cf, rv, a); break;
+                case 1: fma_rows<1>(cf, rv, a); break;
+                case 2: fma_rows<2>(cf, rv, a); break;
+                default: fma_rows<3>(cf, rv, a); break;
+            }
+        } else {
+            const float* cr = v.cp + j * kSlot + v.mt[j].y;
+#pragma unroll
+            for (int r = 0; r < R; ++r) a.v[r] = fmaf(cr[r], rv[ladder_slot(r)], a.v[r]);
+        }
     }
     __device__ __forceinline__ void put(const NodeOut& o, int n, const Acc& a) const {
         const int64_t at = (int64_t)n * kNodeFloats + lane;
