@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "zonal-scatter fwd+bwd edges/s at N=4096,E=647170,C=32; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0     # nominal HBM3e rate of the part (about 8 TB/s), reported beside the peak in use
 L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = {
     "fwd": "equivariant_interatomic_potential_gb300/csrc/zs_forward.cu",
@@ -54,6 +55,25 @@ def algorithmic_bytes(N: int, E: int, C: int, lmax: int = 3) -> dict:
     bwd = E * (4 + 4 * R + 4 * lmax * C + 4 * R + 4 * lmax * C) + 4 * D * N * C
     csr = E * (4 + 4) + 4 * (N + 1)
     return {"fwd": fwd, "bwd": bwd, "csr": csr}
+
+
+def kernel_figures(ab: dict, b2b: dict, per: dict, E: int, peak: float, peak_kind: str, names) -> dict:
+    """Per entry point: the roofline figures from the back-to-back launches
+    (b2b: mean microseconds per launch) and, alongside, the launches
+    bracketed inside a step (per: microseconds of each; launch latency and
+    the previous kernel's L2 write-backs included).  Fractions of the peak
+    in use and of the nominal 8 TB/s HBM3e rate."""
+    kernels = {}
+    for k in names:
+        us = b2b[k]
+        us_step = statistics.mean(per[k])
+        gbs = ab[k] / (us * 1e-6) / 1e9
+        kernels[k] = {"us_back_to_back": us, "algorithmic_bytes": ab[k],
+                      "GBs": gbs, "frac_of_" + peak_kind: gbs / peak, "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
+                      "edges_per_s": E / (us * 1e-6),
+                      "us_in_step_mean": us_step, "us_in_step_median": statistics.median(per[k]),
+                      "frac_in_step": ab[k] / (us_step * 1e-6) / 1e9 / peak}
+    return kernels
 
 
 def metric_for(lmax: int, scaled: bool = False) -> str:
@@ -530,24 +550,14 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         ab["fwd"] += extra["fwd"]
         ab["bwd"] += extra["bwd"]
     peak, peak_kind = measured_peaks()
-    kernels = {}
     ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
-    for k in ("csr", "fwd", "bwd", other_name):
-        # roofline figures from the back-to-back launches; the bracketed
-        # in-step launches (launch latency and the previous kernel's L2
-        # write-backs included) alongside
-        us = b2b[k]
-        us_step = statistics.mean(per[k])
-        gbs = ab[k] / (us * 1e-6) / 1e9
-        kernels[k] = {"us_back_to_back": us, "algorithmic_bytes": ab[k],
-                      "GBs": gbs, "frac_of_" + peak_kind: gbs / peak, "edges_per_s": E / (us * 1e-6),
-                      "us_in_step_mean": us_step, "us_in_step_median": statistics.median(per[k]),
-                      "frac_in_step": ab[k] / (us_step * 1e-6) / 1e9 / peak}
+    kernels = kernel_figures(ab, b2b, per, E, peak, peak_kind, ("csr", "fwd", "bwd", other_name))
     dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_back_to_back"])
     bwd_entry = "zs_backward_csr" if args.backward == "csr" else "zs_backward"
     roof = {"kernel": {"fwd": "zs_forward", "bwd": bwd_entry}[dom], "bound": "hbm",
             "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
             "frac": kernels[dom]["GBs"] / peak, "peak_kind": peak_kind,
+            "frac_of_nominal_8000": kernels[dom]["GBs"] / NOMINAL_HBM_GBS,
             "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config) if L == 3 else None,
             "algorithmic_bytes_per_launch": ab[dom]}
     ms_per_step = total_ms / args.steps

@@ -51,3 +51,16 @@ def test_metric_names():
 def test_job_throughput_counts_all_ranks():
     # units of every rank over the slowest rank's time
     assert bench.job_throughput(1000, 10, 2.0, 4) == 1000 * 10 * 4 / 2e-3
+
+
+def test_kernel_figures():
+    # 1 GB in 200 us is 5000 GB/s: 0.5 of a 10000 GB/s peak, 0.625 of 8000
+    ab = {"fwd": 10 ** 9}
+    k = bench.kernel_figures(ab, {"fwd": 200.0}, {"fwd": [250.0, 250.0, 400.0]}, 1000, 10000.0, "measured", ("fwd",))
+    f = k["fwd"]
+    assert abs(f["GBs"] - 5000.0) < 1e-9
+    assert abs(f["frac_of_measured"] - 0.5) < 1e-12
+    assert abs(f["frac_of_nominal_8000"] - 0.625) < 1e-12
+    assert abs(f["edges_per_s"] - 1000 / 200e-6) < 1e-3
+    assert f["us_in_step_mean"] == 300.0 and f["us_in_step_median"] == 250.0
+    assert abs(f["frac_in_step"] - 10 ** 9 / 300e-6 / 1e9 / 10000.0) < 1e-12
