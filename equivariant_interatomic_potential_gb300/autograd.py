@@ -12,12 +12,18 @@ and "Tests").  Here that operator is a ``torch.library`` custom op:
   after the operator (section "What", third bullet), fused: out[n] =
   node_scale[n] * the operator's sum, differentiable in node_scale too
 
-``zonal_scatter``'s backward is ``zs_gie::zonal_scatter_backward`` (the
-edge-order ``zs_backward``), itself an operator without a derivative, so a
-second backward raises.  Every operator has a fake (meta) implementation,
-so ``torch.compile`` traces through them with shapes only; the launch grid
-is chosen inside libzs from the runtime sizes.  The operators run libzs's
-CUDA kernels and nothing else: CPU tensors are rejected.
+``zonal_scatter``'s backward is ``zs_gie::zonal_scatter_backward``, itself
+an operator without a derivative, so a second backward raises.  It takes the
+faster of libzs's two backward entry points for the ladder (measured on the
+4096-node graph at C = 32): the CSR-order ``zs_backward_csr`` (the forward's
+CSR is at hand) at lmax 2, 4 and 5, the edge-order ``zs_backward`` at lmax 1
+and 3 and for every other channel count.  Every operator has a fake (meta)
+implementation, so ``torch.compile`` traces through them with shapes only;
+the launch grid is chosen inside libzs from the runtime sizes.  The
+operators run libzs's CUDA kernels and nothing else: CPU tensors are
+rejected.  Each call first reads the device's timeout flag (page-locked host
+memory, no synchronisation) and raises if a bounded wait of an earlier
+launch ran out.
 """
 from __future__ import annotations
 
@@ -32,6 +38,16 @@ def _cuda_only(name: str, *tensors: torch.Tensor) -> None:
     for t in tensors:
         if t.device.type != "cuda":
             raise ValueError(f"{_NS}::{name} runs on CUDA tensors only (got a {t.device.type} tensor)")
+    zs.raise_on_timeout_flag(tensors[0].device)
+
+
+# Ladders whose CSR-order backward is the faster one at C = 32.
+CSR_BACKWARD_LADDERS = (2, 4, 5)
+
+
+def uses_csr_backward(lmax: int, C: int) -> bool:
+    """Whether zs_gie::zonal_scatter_backward takes zs_backward_csr for this shape."""
+    return C == 32 and lmax in CSR_BACKWARD_LADDERS
 
 
 @torch.library.custom_op(f"{_NS}::build_csr", mutates_args=())
@@ -65,26 +81,33 @@ def _(coup, rad, dst, row_ptr, perm, num_nodes):
 
 @torch.library.custom_op(f"{_NS}::zonal_scatter_backward", mutates_args=())
 def zonal_scatter_backward(grad_out: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, dst: torch.Tensor,
+                           row_ptr: torch.Tensor, perm: torch.Tensor,
                            num_nodes: int) -> tuple[torch.Tensor, torch.Tensor]:
-    """(d_coup (E, D-1), d_rad (E, lmax, C)) for the cotangent grad_out (N, D, C); edge order."""
-    _cuda_only("zonal_scatter_backward", grad_out, coup, rad, dst)
+    """(d_coup (E, D-1), d_rad (E, lmax, C)) for the cotangent grad_out (N, D, C).
+
+    row_ptr and perm are the CSR of dst (the forward's); the ladder and channel
+    count pick the entry point (``uses_csr_backward``)."""
+    _cuda_only("zonal_scatter_backward", grad_out, coup, rad, dst, row_ptr, perm)
+    if uses_csr_backward(rad.shape[1], rad.shape[2]):
+        return zs.zs_backward_csr(grad_out.contiguous(), coup.contiguous(), rad.contiguous(), row_ptr.contiguous(),
+                                  perm.contiguous(), num_nodes)
     return zs.zs_backward(grad_out.contiguous(), coup.contiguous(), rad.contiguous(), dst.contiguous(), num_nodes)
 
 
 @zonal_scatter_backward.register_fake
-def _(grad_out, coup, rad, dst, num_nodes):
+def _(grad_out, coup, rad, dst, row_ptr, perm, num_nodes):
     return coup.new_empty(coup.shape), rad.new_empty(rad.shape)
 
 
 def _setup_context(ctx, inputs, output):
     coup, rad, dst, row_ptr, perm, num_nodes = inputs
-    ctx.save_for_backward(coup, rad, dst)
+    ctx.save_for_backward(coup, rad, dst, row_ptr, perm)
     ctx.num_nodes = num_nodes
 
 
 def _backward(ctx, grad_out):
-    coup, rad, dst = ctx.saved_tensors
-    d_coup, d_rad = zonal_scatter_backward(grad_out, coup, rad, dst, ctx.num_nodes)
+    coup, rad, dst, row_ptr, perm = ctx.saved_tensors
+    d_coup, d_rad = zonal_scatter_backward(grad_out, coup, rad, dst, row_ptr, perm, ctx.num_nodes)
     return d_coup, d_rad, None, None, None, None
 
 

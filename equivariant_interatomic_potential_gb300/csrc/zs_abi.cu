@@ -28,7 +28,42 @@ zs_status check_launch(const char* what) {
 
 unsigned int take_timeouts_forward();
 unsigned int take_timeouts_backward();
+cudaError_t set_timeout_flag_forward(unsigned int* flag);
+cudaError_t set_timeout_flag_backward(unsigned int* flag);
 zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, resolved once through the
+// runtime (no link against the driver library).
+namespace {
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+struct CtxFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+    CtxFns() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+    }
+};
+}  // namespace
+
+uint64_t current_context_id() {
+    static const CtxFns fns;
+    if (!fns.get_current || !fns.get_id) return 0;
+    void* ctx = nullptr;
+    if (fns.get_current(&ctx) != 0 || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (fns.get_id(ctx, &id) != 0) return 0;
+    return (uint64_t)id + 1;   // never 0 for a live context
+}
 
 }  // namespace zs
 
@@ -43,6 +78,30 @@ zs_status zs_check_timeouts(void) {
     return ZS_OK;
 }
 
+
+zs_status zs_set_timeout_flag(uint32_t* flag) {
+    if (flag) {
+        cudaPointerAttributes attr;
+        const cudaError_t err = cudaPointerGetAttributes(&attr, flag);
+        if (err != cudaSuccess) {
+            cudaGetLastError();
+            return zs::fail(ZS_ERR_INVALID_ARG, "zs_set_timeout_flag: %s", cudaGetErrorString(err));
+        }
+        const bool reachable = (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged ||
+                                attr.type == cudaMemoryTypeHost) && attr.devicePointer == flag;
+        if (!reachable)
+            return zs::fail(ZS_ERR_INVALID_ARG,
+                            "zs_set_timeout_flag: the word is not device memory or page-locked host memory that "
+                            "the device reaches at the same address");
+        if (reinterpret_cast<uintptr_t>(flag) & 3u)
+            return zs::fail(ZS_ERR_INVALID_ARG, "zs_set_timeout_flag: the word is not 4-byte aligned");
+    }
+    unsigned int* f = reinterpret_cast<unsigned int*>(flag);
+    cudaError_t err = zs::set_timeout_flag_forward(f);
+    if (err == cudaSuccess) err = zs::set_timeout_flag_backward(f);
+    if (err != cudaSuccess) return zs::fail(ZS_ERR_CUDA, "zs_set_timeout_flag: %s", cudaGetErrorString(err));
+    return ZS_OK;
+}
 
 zs_status zs_selftest_bounded_wait(uint32_t max_spins, zs_stream_t stream) {
     if (max_spins == 0 || max_spins > (1u << 16))

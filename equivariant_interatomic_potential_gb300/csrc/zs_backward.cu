@@ -638,6 +638,7 @@ __global__ void __launch_bounds__(32) selftest_wait(uint32_t max_spins) {
 }  // namespace
 
 unsigned int take_timeouts_backward() { return take_timeouts_local(); }
+cudaError_t set_timeout_flag_backward(unsigned int* flag) { return set_timeout_flag_local(flag); }
 
 zs_status selftest_bounded_wait(uint32_t max_spins, cudaStream_t s) {
     selftest_wait<<<1, 32, 0, s>>>(max_spins);
@@ -747,12 +748,12 @@ void launch_edge_quad(const float* g, const float* coup, int cld, const float* r
                   "rings and hot slot fit an SM");
     const int bulk = (cld == R && aligned16(coup)) ? 1 : 0;
     if (scale == nullptr && dld == R && bulk) {
-        static std::atomic<bool> attr_done[kMaxDevices];
+        static std::atomic<uint64_t> attr_done[kMaxDevices];
         set_smem_limit_once(bwd_edge_quad<W, S, T, LM, false>, smem, attr_done);
         launch(bwd_edge_quad<W, S, T, LM, false>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
                (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
     } else {
-        static std::atomic<bool> attr_done[kMaxDevices];
+        static std::atomic<uint64_t> attr_done[kMaxDevices];
         set_smem_limit_once(bwd_edge_quad<W, S, T, LM, true>, smem, attr_done);
         launch(bwd_edge_quad<W, S, T, LM, true>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
                (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
@@ -793,7 +794,7 @@ void launch_csr_quad(const float* g, const float* coup, const float* rad, const 
     constexpr int kGBytes = R > 24 ? R * 32 * 16 : 0;   // shared-memory cotangent rows per warp
     static_assert(W * (Layout::kBytes + kGBytes) <= 232448, "rings and cotangent rows fit an SM");
     const int smem = W * (Layout::kBytes + kGBytes);
-    static std::atomic<bool> attr_done[kMaxDevices];
+    static std::atomic<uint64_t> attr_done[kMaxDevices];
     set_smem_limit_once(bwd_csr_quad<W, S, T, LM>, smem, attr_done);
     launch(bwd_csr_quad<W, S, T, LM>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, row_ptr, perm, (int)E, N,
            (int)KW, (int)Wtot, d_coup, d_rad);

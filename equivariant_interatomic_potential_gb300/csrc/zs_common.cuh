@@ -170,13 +170,21 @@ inline int num_sms() {
     return v;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device.
+// Unique id (never 0) of the calling thread's current CUDA context, 0 when
+// there is none or the driver cannot say.  A setting made in one context (a
+// kernel attribute, a device symbol's address) does not outlive it: after
+// cudaDeviceReset the device's primary context is a new one, with a new id.
+uint64_t current_context_id();
+
+// Raise a kernel's dynamic shared-memory limit once per context (again after
+// a cudaDeviceReset).  done[dev] holds the id of the context it was set in.
 template <typename K>
-inline void set_smem_limit_once(K kernel, int bytes, std::atomic<bool>* done) {
+inline void set_smem_limit_once(K kernel, int bytes, std::atomic<uint64_t>* done) {
     const int dev = current_device();
-    if (!done[dev].load(std::memory_order_acquire)) {
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || done[dev].load(std::memory_order_acquire) != ctx) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        done[dev].store(true, std::memory_order_release);
+        done[dev].store(current_context_id(), std::memory_order_release);
     }
 }
 

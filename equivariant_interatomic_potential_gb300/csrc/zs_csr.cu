@@ -561,7 +561,7 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     if (p.counting) {
-        static std::atomic<bool> rank_smem_set[kMaxDevices];
+        static std::atomic<uint64_t> rank_smem_set[kMaxDevices];
         int32_t* M = reinterpret_cast<int32_t*>(ws + p.off_hist);
         int32_t* tot = reinterpret_cast<int32_t*>(ws + p.off_tot);
         uint16_t* rank = reinterpret_cast<uint16_t*>(ws + p.off_rank);
@@ -569,10 +569,10 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
         set_smem_limit_once(csr_count_rank, smem, rank_smem_set);
         const int S = 2 * count_pairs(N + 1);
         launch(csr_count_rank, p.T, kCntThreads, count_rank_smem(N + 1, p.rounds), s, dst, E, N, p.rounds, M, rank);
-        static std::atomic<bool> scan_smem_set[kMaxDevices];
+        static std::atomic<uint64_t> scan_smem_set[kMaxDevices];
         set_smem_limit_once(csr_scan_cols, kOneCtaPerSmSmem, scan_smem_set);
         launch(csr_scan_cols, (N + 1 + 31) / 32, kCntThreads, kOneCtaPerSmSmem, s, M, p.T, S, N + 1, tot);
-        static std::atomic<bool> scatter_smem_set[kMaxDevices];
+        static std::atomic<uint64_t> scatter_smem_set[kMaxDevices];
         set_smem_limit_once(csr_count_scatter, imax(kOneCtaPerSmSmem, count_scatter_smem(kCntMaxKeys, kCntMaxRounds)), scatter_smem_set);
         launch(csr_count_scatter, p.T, kCntThreads, imax(kOneCtaPerSmSmem, count_scatter_smem(N + 1, p.rounds)), s, dst, (const uint16_t*)rank,
                (const int32_t*)M, (const int32_t*)tot, E, N, p.rounds, perm, row_ptr, bad_dst_count);

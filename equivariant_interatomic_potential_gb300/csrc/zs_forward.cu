@@ -190,12 +190,12 @@ __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
     return v;
 }
 
-// Bounded wait until flags[k] == tag; false (and one count in g_zs_timeouts)
-// if it never comes.
+// Bounded wait until flags[k] == tag; false (and one timeout noted) if it
+// never comes.
 __device__ __forceinline__ bool wait_flag(const uint64_t* flags, int k, uint64_t tag) {
     for (uint32_t i = 0; i < kMaxSpins; ++i)
         if (ld_acquire_u64(flags + k) == tag) return true;
-    atomicAdd(&g_zs_timeouts, 1u);
+    note_timeout();
     return false;
 }
 
@@ -706,6 +706,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 }  // namespace
 
 unsigned int take_timeouts_forward() { return take_timeouts_local(); }
+cudaError_t set_timeout_flag_forward(unsigned int* flag) { return set_timeout_flag_local(flag); }
 
 }  // namespace zs
 
@@ -829,7 +830,7 @@ static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float
     constexpr int W = tma_warps<P>();
     auto kernel = fwd_tma<W, kTmaStages, P::kTileEdges, P>;
     const int smem = W * RingLayout<kTmaStages, P::kTileEdges, P::kRadFloats, P::kCoupRow>::kBytes;
-    static std::atomic<bool> attr_done[kMaxDevices];
+    static std::atomic<uint64_t> attr_done[kMaxDevices];
     set_smem_limit_once(kernel, smem, attr_done);
     launch(kernel, (unsigned)p.ctas, W * 32, smem, s, coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW,
            (int)p.Wtot, o, sc.part, sc.flags, next_salt());
@@ -942,24 +943,32 @@ static __device__ __align__(256) unsigned char g_forward_scratch[kNoAllocScratch
 
 namespace {
 
-// Device address of g_forward_scratch on the current device, looked up once per
-// device.  In host code the array's name is only a stand-in for the symbol.
+// Device address of g_forward_scratch in the current device's context, looked
+// up once per context with that device current (and again after a
+// cudaDeviceReset, whose new primary context may place the array elsewhere).
+// In host code the array's name is only a stand-in for the symbol, never an
+// address a kernel may use.
 zs_status forward_scratch_address(float** out_ptr) {
+    struct Entry {
+        uint64_t ctx;
+        void* ptr;
+    };
     static std::mutex mu;
-    static void* cached[128] = {};
+    static Entry cached[kMaxDevices] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return fail(ZS_ERR_CUDA, "zs_forward_noalloc: cudaGetDevice: %s", cudaGetErrorString(err));
-    if (dev < 0 || dev >= 128) return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: device ordinal %d", dev);
+    if (dev < 0 || dev >= kMaxDevices) return fail(ZS_ERR_UNSUPPORTED, "zs_forward_noalloc: device ordinal %d", dev);
     std::lock_guard<std::mutex> lock(mu);
-    if (!cached[dev]) {
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || cached[dev].ctx != ctx || !cached[dev].ptr) {
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_forward_scratch);
         if (err != cudaSuccess || !p)
             return fail(ZS_ERR_CUDA, "zs_forward_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(err));
-        cached[dev] = p;
+        cached[dev] = Entry{current_context_id(), p};
     }
-    *out_ptr = static_cast<float*>(cached[dev]);
+    *out_ptr = static_cast<float*>(cached[dev].ptr);
     return ZS_OK;
 }
 

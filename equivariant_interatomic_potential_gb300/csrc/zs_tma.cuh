@@ -15,8 +15,9 @@
 // so consumers need no branch.
 //
 // Every wait is bounded: after kMaxSpins unsuccessful tries the wait counts a
-// timeout in g_zs_timeouts and returns, so a lost completion can never hang
-// the GPU; zs_check_timeouts() reports it.
+// timeout in g_zs_timeouts (and sets the caller's flag word, if one is
+// registered) and returns, so a lost completion can never hang the GPU;
+// zs_check_timeouts() and the flag word report it.
 #pragma once
 
 #include "zs_common.cuh"
@@ -25,6 +26,9 @@ namespace zs {
 
 // Count of bounded waits that ran out in this translation unit's kernels.
 static __device__ unsigned int g_zs_timeouts;
+// Caller-registered word (device memory or host memory the device can reach)
+// set to 1 when a bounded wait runs out; NULL when none is registered.
+static __device__ unsigned int* g_zs_timeout_flag;
 
 // Host: read and clear this translation unit's count (synchronises the device).
 static inline unsigned int take_timeouts_local() {
@@ -32,6 +36,22 @@ static inline unsigned int take_timeouts_local() {
     if (cudaMemcpyFromSymbol(&v, g_zs_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
     if (v) cudaMemcpyToSymbol(g_zs_timeouts, &zero, sizeof(zero));
     return v;
+}
+
+// Host: register the flag word of the current device for this translation
+// unit's kernels (synchronous copy to the device symbol).
+static inline cudaError_t set_timeout_flag_local(unsigned int* flag) {
+    return cudaMemcpyToSymbol(g_zs_timeout_flag, &flag, sizeof(flag));
+}
+
+// Device: record one bounded wait that ran out.
+__device__ __forceinline__ void note_timeout() {
+    atomicAdd(&g_zs_timeouts, 1u);
+    unsigned int* f = g_zs_timeout_flag;
+    if (f) {
+        *reinterpret_cast<volatile unsigned int*>(f) = 1u;
+        __threadfence_system();
+    }
 }
 
 constexpr int kCoupSlotFloats = 20;         // coupling slot of the 15-row ladder (coup_slot_floats(15))
@@ -63,12 +83,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity; false (and one count in
-// g_zs_timeouts) when max_spins tries all fail.
+// Bounded wait for the phase with the given parity; false (and one timeout
+// noted) when max_spins tries all fail.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t max_spins = kMaxSpins) {
     for (uint32_t i = 0; i < max_spins; ++i)
         if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_zs_timeouts, 1u);
+    note_timeout();
     return false;
 }
 

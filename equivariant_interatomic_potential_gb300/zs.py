@@ -79,6 +79,8 @@ def load(build_if_missing: bool = True):
         lib.zs_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
         lib.zs_check_timeouts.restype = ctypes.c_int
         lib.zs_check_timeouts.argtypes = []
+        lib.zs_set_timeout_flag.restype = ctypes.c_int
+        lib.zs_set_timeout_flag.argtypes = [P]
         _lib = lib
         return lib
 
@@ -356,6 +358,60 @@ def zs_backward_csr(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, row_
 def zs_check_timeouts() -> None:
     """Raise ZsError if a bounded device wait ran out since the last check (synchronises)."""
     _check("zs_check_timeouts", load().zs_check_timeouts())
+
+
+def zs_set_timeout_flag(flag: torch.Tensor | None) -> None:
+    """Register (or, with None, unregister) the current device's timeout flag
+    word: an int32 tensor of one element, on the device or in page-locked
+    host memory, that the kernels set to 1 when a bounded wait runs out."""
+    if flag is not None:
+        if flag.dtype != torch.int32 or flag.numel() != 1:
+            raise ValueError("the timeout flag is a one-element int32 tensor")
+        if flag.device.type == "cpu" and not flag.is_pinned():
+            raise ValueError("a host timeout flag must be in page-locked (pinned) memory")
+    _check("zs_set_timeout_flag", load().zs_set_timeout_flag(_ptr(flag)))
+
+
+_flags: dict[int, torch.Tensor] = {}
+_flags_lock = threading.Lock()
+
+
+def _device_index(device) -> int:
+    idx = None if device is None else torch.device(device).index
+    return torch.cuda.current_device() if idx is None else idx
+
+
+def timeout_flag(device=None) -> torch.Tensor:
+    """The page-locked host word registered for ``device`` (the current CUDA
+    device by default), registering it on first use (not during stream
+    capture: the registration is a synchronous copy).  It reads 1 once a
+    bounded wait of a kernel launched after the registration has run out;
+    reading it does not synchronise anything."""
+    idx = _device_index(device)
+    with _flags_lock:
+        f = _flags.get(idx)
+        if f is None:
+            f = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+            with torch.cuda.device(idx):
+                zs_set_timeout_flag(f)
+            _flags[idx] = f
+        return f
+
+
+def raise_on_timeout_flag(device=None) -> None:
+    """Raise ZsError (ZS_ERR_TIMEOUT) if the device's timeout flag is set, and
+    clear it.  A host read only: a timeout inside a kernel that has not
+    finished yet shows up at a later check.  Registers the flag on first use,
+    except while the current stream is being captured."""
+    idx = _device_index(device)
+    f = _flags.get(idx)
+    if f is None:
+        if torch.cuda.is_current_stream_capturing():
+            return
+        f = timeout_flag(idx)
+    if int(f[0]) != 0:
+        f[0] = 0
+        raise ZsError("timeout flag", 4, "a bounded device wait ran out in an earlier launch; its outputs are undefined")
 
 
 def zs_forward_noalloc(coup: torch.Tensor, rad: torch.Tensor, row_ptr: torch.Tensor, perm: torch.Tensor, N: int,

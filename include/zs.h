@@ -256,12 +256,16 @@ ZS_API zs_status zs_backward_csr(const float* g, const float* coup, const float*
  *   Arguments, results and errors as zs_forward (caller still passes the
  *   inputs and out).  The partial sums zs_forward keeps in its workspace
  *   live instead in one static device array of 4 MiB that every GPU
- *   loading the library holds until the process exits.  C == 32 with
- *   16-byte aligned rad, out and coup needs about 3.8 KB per SM whatever E
- *   is; other channel counts need 120*C + 12 bytes per 256 edges.  A call
- *   that would need more returns ZS_ERR_INVALID_ARG and enqueues nothing.
- *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   loading the library holds until the process exits.  The single-kernel
+ *   path (C == 32, rad 16-byte aligned, and out 16-byte aligned when
+ *   lmax == 3; coup may have any 4-byte alignment) needs about 8 * R * 32
+ *   bytes per SM whatever E is (R = (lmax+1)^2 - 1 rows, 3.8 KB at
+ *   lmax 3); every other shape needs 8 * R * C + 12 bytes per 256 edges.
+ *   A call that would need more returns ZS_ERR_INVALID_ARG and enqueues
+ *   nothing.
+ *   The first call on each device (and the first after a cudaDeviceReset)
+ *   looks up the array's device address with cudaGetSymbolAddress, with
+ *   that device current; make that first call before any stream capture.
  *   Every call shares the array: calls whose kernels overlap on the GPU
  *   (other streams, other host threads) race and give wrong results.
  *   Nothing in the array needs to start at zero.
@@ -272,11 +276,30 @@ ZS_API zs_status zs_forward_noalloc(const float* coup, const float* rad,
                                     float* out, zs_stream_t stream);
 
 /*
+ * Registers a caller-owned 32-bit word that the kernels set to 1 when a
+ * bounded wait runs out (see zs_check_timeouts), so that a caller can see a
+ * timeout without synchronising the device: for instance page-locked host
+ * memory that the host reads at any time, or device memory that it copies
+ * back asynchronously.  The word is only written (never cleared) by the
+ * library; the caller clears it.
+ *   flag   device memory, or page-locked host memory the device reaches at
+ *          the same address (cudaHostAlloc / cudaMallocHost on a system
+ *          with unified addressing), 4-byte aligned; NULL unregisters
+ * Applies to the current device and to kernels enqueued after the call
+ * (a synchronous copy to a device symbol: call it at set-up, not during
+ * stream capture).  The word must stay valid until it is unregistered.
+ * ZS_ERR_INVALID_ARG for memory the device cannot reach at that address.
+ * The pages have no counterpart.
+ */
+ZS_API zs_status zs_set_timeout_flag(uint32_t* flag);
+
+/*
  * Reads and clears the device-side count of bounded waits that ran out.
  * The kernels that stream operands with asynchronous bulk copies wait for
  * them with an iteration limit; a wait that reaches its limit is counted
  * and the kernel returns instead of hanging the GPU (its outputs are then
- * undefined).  Synchronises the device.  Returns ZS_ERR_TIMEOUT when any
+ * undefined), and the word registered with zs_set_timeout_flag, if any, is
+ * set.  Synchronises the device.  Returns ZS_ERR_TIMEOUT when any
  * wait ran out since the previous call, ZS_OK otherwise.
  */
 ZS_API zs_status zs_check_timeouts(void);

@@ -21,7 +21,7 @@ def test_header_declares_the_boundary():
     names = zs.declared_functions()
     for fn in ("zs_build_csr", "zs_forward", "zs_backward", "zs_backward_csr", "zs_build_csr_workspace_bytes",
                "zs_forward_workspace_bytes", "zs_forward_workspace_bytes_lmax", "zs_status_string", "zs_last_error", "zs_version",
-               "zs_check_timeouts", "zs_selftest_bounded_wait", "zs_forward_noalloc"):
+               "zs_check_timeouts", "zs_selftest_bounded_wait", "zs_forward_noalloc", "zs_set_timeout_flag"):
         assert fn in names
 
 
@@ -101,6 +101,13 @@ def test_backward_csr_argument_checks(lib):
 def test_selftest_argument_checks(lib):
     assert lib.zs_selftest_bounded_wait(0, None) == INVALID
     assert lib.zs_selftest_bounded_wait((1 << 16) + 1, None) == INVALID
+
+
+def test_timeout_flag_rejects_memory_the_device_cannot_reach(lib):
+    # ordinary (pageable) host memory is not a flag word the kernels may write
+    buf = ctypes.create_string_buffer(16)
+    assert lib.zs_set_timeout_flag(ctypes.addressof(buf)) == INVALID
+    assert b"zs_set_timeout_flag" in lib.zs_last_error()
 
 
 def test_build_csr_argument_checks(lib):

@@ -111,7 +111,7 @@ def test_cuda_graph_replay_with_new_inputs(lmax):
     coup, rad, dst, g = (dev(ws[0].coup), dev(ws[0].rad), dev(ws[0].dst), dev(ws[0].grad_out))
     row_ptr, perm = ag.build_csr(dst, N)          # warm-up outside the capture
     ag.zonal_scatter(coup, rad, dst, row_ptr, perm, N)
-    ag.zonal_scatter_backward(g, coup, rad, dst, N)
+    ag.zonal_scatter_backward(g, coup, rad, dst, row_ptr, perm, N)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -119,7 +119,7 @@ def test_cuda_graph_replay_with_new_inputs(lmax):
     with torch.cuda.stream(s), torch.cuda.graph(graph, stream=s):
         rp, pm = ag.build_csr(dst, N)
         out = ag.zonal_scatter(coup, rad, dst, rp, pm, N)
-        d_coup, d_rad = ag.zonal_scatter_backward(g, coup, rad, dst, N)
+        d_coup, d_rad = ag.zonal_scatter_backward(g, coup, rad, dst, rp, pm, N)
     torch.cuda.synchronize()
     for w in ws[1:] + ws[:1]:
         coup.copy_(torch.from_numpy(w.coup))
@@ -135,3 +135,35 @@ def test_cuda_graph_replay_with_new_inputs(lmax):
         dc, dr, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, N)
         assert_close(d_coup.cpu().numpy(), dc, adc, "d_coup")
         assert_close(d_rad.cpu().numpy(), dr, adr, "d_rad")
+
+
+def test_backward_entry_point_per_ladder():
+    # the CSR-order backward where it measured faster (lmax 2, 4, 5 at C = 32)
+    assert [ag.uses_csr_backward(l, 32) for l in (1, 2, 3, 4, 5)] == [False, True, False, True, True]
+    assert not any(ag.uses_csr_backward(l, 40) for l in (1, 2, 3, 4, 5))
+
+
+@pytest.mark.gpu
+def test_operator_raises_on_timeout_flag():
+    # a bounded wait that runs out sets the registered page-locked flag; the
+    # next operator call raises, and the flag stays clear after normal calls
+    from equivariant_interatomic_potential_gb300 import zs
+    w = workloads.make_random(50, 3000, 32, seed=5)
+    coup, rad, dst = dev(w.coup), dev(w.rad), dev(w.dst)
+    flag = zs.timeout_flag()
+    zs.zs_check_timeouts()
+    flag[0] = 0
+    out = ag.zonal_scatter_from_dst(coup, rad, dst, w.N)
+    torch.cuda.synchronize()
+    assert int(flag[0]) == 0
+    lib = zs.load()
+    assert lib.zs_selftest_bounded_wait(8, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert int(flag[0]) == 1
+    with pytest.raises(zs.ZsError, match="ZS_ERR_TIMEOUT"):
+        ag.zonal_scatter_from_dst(coup, rad, dst, w.N)
+    assert int(flag[0]) == 0                       # the raise cleared it
+    assert lib.zs_check_timeouts() == 4            # the counter saw it too
+    out2 = ag.zonal_scatter_from_dst(coup, rad, dst, w.N)
+    torch.cuda.synchronize()
+    assert int(flag[0]) == 0 and torch.equal(out, out2)

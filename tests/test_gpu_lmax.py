@@ -1,5 +1,7 @@
 """Ladders of other degrees (lmax = 1..5, an extension of the pages' lmax = 3
 operator with the same definitions) on the GPU, against the oracle."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -23,6 +25,21 @@ def test_ladder_matches_oracle(lmax, C):
     row_ptr, perm = check_csr(w, res)
     check_forward(w, res, row_ptr, perm)
     check_backward(w, res)
+
+
+@pytest.mark.parametrize("lmax", [1, 2, 4, 5])
+def test_ladder_full_size_n4096(lmax):
+    # the benchmarked shapes: the 4096-node, 647170-edge graph at C = 32, so the
+    # kernels' rings, windows and CTA combines run exactly as timed
+    w = workloads.make_workload("n4096", lmax=lmax)
+    res = run_gpu(w)
+    row_ptr, perm = check_csr(w, res)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        check_forward(w, res, row_ptr, perm)
+        check_backward(w, res)
+    finally:
+        oracle.set_threads(1)
 
 
 @pytest.mark.parametrize("lmax", [1, 5])
@@ -52,12 +69,16 @@ def test_ladder_noalloc_matches_workspace_forward():
     assert torch.equal(a, b)
 
 
-def test_ladder_autograd():
-    w = workloads.make_random(90, 12000, 16, seed=8, lmax=2)
+@pytest.mark.parametrize("lmax", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("C", [32, 16])
+def test_ladder_autograd(lmax, C):
+    # the operator's backward takes the CSR-order entry point at lmax 2, 4, 5
+    # (C = 32) and the edge-order one otherwise: both against the oracle
+    w = workloads.make_random(90, 12000, C, seed=8 + lmax, hot_node=4, hot_fraction=0.4, lmax=lmax)
     coup = dev(w.coup).requires_grad_(True)
     rad = dev(w.rad).requires_grad_(True)
     out = ag.zonal_scatter_from_dst(coup, rad, dev(w.dst), w.N)
-    assert out.shape == (90, 9, 16)
+    assert out.shape == (90, (lmax + 1) ** 2, C)
     d_coup, d_rad = torch.autograd.grad(out, (coup, rad), dev(w.grad_out))
     dc, dr, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
     assert_close(d_coup.cpu().numpy(), dc, adc, "d_coup")
