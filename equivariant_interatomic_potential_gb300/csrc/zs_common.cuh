@@ -188,6 +188,13 @@ inline void set_smem_limit_once(K kernel, int bytes, std::atomic<uint64_t>* done
     }
 }
 
+// Per-call value mixed into the launch tags of kernels whose CTAs signal one
+// another through tagged flags (see launch_tag).
+inline uint64_t next_salt() {
+    static std::atomic<uint64_t> counter{0x2545F4914F6CDD1Dull};
+    return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
+}
+
 template <class T>
 __host__ __device__ __forceinline__ constexpr T imin(T a, T b) { return a < b ? a : b; }
 template <class T>

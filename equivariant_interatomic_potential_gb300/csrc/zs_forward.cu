@@ -171,34 +171,6 @@ __device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, i
     return n_lb;
 }
 
-// Tag that marks a partial as written by this launch: %gridid numbers the
-// launches of a context (a new value for every launch, graph replays
-// included), mixed with a per-call value from the host.
-__device__ __forceinline__ uint64_t launch_tag(uint64_t salt) {
-    uint64_t id;
-    asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
-    return (id * 0x9E3779B97F4A7C15ull) ^ salt;
-}
-
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Bounded wait until flags[k] == tag; false (and one timeout noted) if it
-// never comes.
-__device__ __forceinline__ bool wait_flag(const uint64_t* flags, int k, uint64_t tag) {
-    for (uint32_t i = 0; i < kMaxSpins; ++i)
-        if (ld_acquire_u64(flags + k) == tag) return true;
-    note_timeout();
-    return false;
-}
-
 __device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, float4 acc[4], const Lane32& L) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -483,6 +455,9 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     const int64_t P1 = imin<int64_t>(P0 + span, E);
     int pend_node = -1;                      // a node that started in an earlier CTA and ends here
     Acc pend;
+    __shared__ int s_stored;                 // this CTA left a partial for a later CTA
+    if (threadIdx.x == 0) s_stored = 0;
+    __syncthreads();
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot) {
         const int m = sp_node[warp][slot];
@@ -504,19 +479,28 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         } else {
             // slot 1: starts here and runs past this CTA; slot 0: covers all of it
             lay.store(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * P::kPartFloats, sum);
+            if (lane == 0) s_stored = 1;
         }
     }
-    // publish this CTA's partials: every writer fences, then one release store
+    // Publish this CTA's partial (a CTA leaves at most one: for the node that
+    // runs past its end): every writer fences, then one release store of the
+    // launch's tag.  Exactly one CTA consumes each published flag (the CTA
+    // where that node ends) and resets it to 0 after its wait, so no flag
+    // keeps a tag past the launch: a CUDA graph replays this launch with the
+    // same tag, and must not find the previous replay's flags set.
     __threadfence();
     __syncthreads();
-    const uint64_t tag = launch_tag(salt);
-    if (threadIdx.x == 0) st_release_u64(flags + blockIdx.x, tag);
+    const uint64_t tag = flag_tag(launch_tag(salt));
+    if (threadIdx.x == 0 && s_stored) st_release_u64(flags + blockIdx.x, tag);
     if (pend_node < 0) return;
     // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
     // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
     const int b0 = (int)(__ldg(row_ptr + pend_node) / span);
     if (lane == 0)
-        for (int k = b0; k < (int)blockIdx.x; ++k) wait_flag(flags, k, tag);
+        for (int k = b0; k < (int)blockIdx.x; ++k) {
+            wait_flag(flags, k, tag);
+            flags[k] = 0;
+        }
     __syncwarp();
     Acc total;
     lay.load_cg(cta_part + ((int64_t)b0 * 2 + 1) * P::kPartFloats, total);
@@ -739,11 +723,6 @@ static Scratch scratch_at(void* base, int64_t windows, int C, int R) {
     return sc;
 }
 
-// Per-call value mixed into the C == 32 forward's launch tags.
-static uint64_t next_salt() {
-    static std::atomic<uint64_t> counter{0x2545F4914F6CDD1Dull ^ (uint64_t)(uintptr_t)&counter};
-    return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
-}
 
 // Warps per CTA of the single-wave forward for a lane layout: 16, or as many
 // rings as one SM's shared memory holds.

@@ -14,48 +14,16 @@
 // them.  A position whose perm entry is not a valid edge id gets zero rows,
 // so consumers need no branch.
 //
-// Every wait is bounded: after kMaxSpins unsuccessful tries the wait counts a
-// timeout in g_zs_timeouts (and sets the caller's flag word, if one is
-// registered) and returns, so a lost completion can never hang the GPU;
-// zs_check_timeouts() and the flag word report it.
+// Every wait is bounded (zs_wait.cuh): a lost completion can never hang the
+// GPU; zs_check_timeouts() and the caller's flag word report it.
 #pragma once
 
 #include "zs_common.cuh"
+#include "zs_wait.cuh"
 
 namespace zs {
 
-// Count of bounded waits that ran out in this translation unit's kernels.
-static __device__ unsigned int g_zs_timeouts;
-// Caller-registered word (device memory or host memory the device can reach)
-// set to 1 when a bounded wait runs out; NULL when none is registered.
-static __device__ unsigned int* g_zs_timeout_flag;
-
-// Host: read and clear this translation unit's count (synchronises the device).
-static inline unsigned int take_timeouts_local() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_zs_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
-    if (v) cudaMemcpyToSymbol(g_zs_timeouts, &zero, sizeof(zero));
-    return v;
-}
-
-// Host: register the flag word of the current device for this translation
-// unit's kernels (synchronous copy to the device symbol).
-static inline cudaError_t set_timeout_flag_local(unsigned int* flag) {
-    return cudaMemcpyToSymbol(g_zs_timeout_flag, &flag, sizeof(flag));
-}
-
-// Device: record one bounded wait that ran out.
-__device__ __forceinline__ void note_timeout() {
-    atomicAdd(&g_zs_timeouts, 1u);
-    unsigned int* f = g_zs_timeout_flag;
-    if (f) {
-        *reinterpret_cast<volatile unsigned int*>(f) = 1u;
-        __threadfence_system();
-    }
-}
-
 constexpr int kCoupSlotFloats = 20;         // coupling slot of the 15-row ladder (coup_slot_floats(15))
-constexpr uint32_t kMaxSpins = 1u << 22;
 constexpr uint32_t kRingArrivals = 33;      // the expect-tx arrival plus one cp.async arrival per lane
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

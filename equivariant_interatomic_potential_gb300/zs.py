@@ -356,8 +356,14 @@ def zs_backward_csr(g: torch.Tensor, coup: torch.Tensor, rad: torch.Tensor, row_
 
 
 def zs_check_timeouts() -> None:
-    """Raise ZsError if a bounded device wait ran out since the last check (synchronises)."""
-    _check("zs_check_timeouts", load().zs_check_timeouts())
+    """Raise ZsError if a bounded device wait ran out since the last check
+    (synchronises).  Also clears the current device's page-locked timeout
+    flag (``timeout_flag``), if registered: the timeout has been reported."""
+    st = load().zs_check_timeouts()
+    f = _flags.get(torch.cuda.current_device()) if torch.cuda.is_available() else None
+    if f is not None:
+        f[0] = 0
+    _check("zs_check_timeouts", st)
 
 
 def zs_set_timeout_flag(flag: torch.Tensor | None) -> None:

@@ -242,6 +242,7 @@ def test_bounded_wait_reports_timeout():
         assert lib.zs_check_timeouts() == 4     # ZS_ERR_TIMEOUT, counter cleared
         assert b"bounded waits ran out" in lib.zs_last_error()
         assert lib.zs_check_timeouts() == 0
+    zs.zs_check_timeouts()                      # the binding's flag word (if registered) is cleared too
     # the context is still usable afterwards
     w = workloads.make_workload("tiny")
     res = run_gpu(w)
