@@ -130,12 +130,6 @@ bwd_gen(const float* __restrict__ g, const float* __restrict__ coup, const float
 // Positions at or after row_ptr[N] hold edges without a node: zeros.
 // --------------------------------------------------------------------------
 
-__device__ __forceinline__ int first_node_b(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
-    const int n_lb = lower_bound_i32(row_ptr, N + 1, p0);
-    if (n_lb >= 1 && n_lb <= N && (int64_t)__ldg(row_ptr + n_lb) > p0) return n_lb - 1;
-    return n_lb;
-}
-
 // Lane layout of the CSR-order C == 32 backward: the 8 lanes of group
 // grp = lane/8 own one edge of every 4 consecutive positions, lane q = lane%8
 // owns channels 4q..4q+3 of ALL 15 rows.  One warp instruction therefore
@@ -207,7 +201,7 @@ bwd_csr_quad(const float* __restrict__ g, const float* __restrict__ coup, const 
         for (int i = 0; i < S; ++i) ring.issue(perm, coup, R, rad, E, Q.lane);
         const int vend = __ldg(row_ptr + N);
         // this group's node: n covers positions [.., b); G holds its rows 1..R
-        int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
+        int n = p0 < vend ? first_node_warp(row_ptr, N, p0, Q.lane) : N;
         int b = n < N ? __ldg(row_ptr + n + 1) : 0;
         int c = 0;   // row_ptr[n + 2], fetched one node ahead
         float4 G[kSmemG ? 1 : R];
@@ -606,7 +600,7 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
     const int64_t p0 = (int64_t)gw * KW;
     const int64_t p1 = imin<int64_t>(p0 + KW, E);
     const int64_t vend = __ldg(row_ptr + N);
-    int n = p0 < vend ? first_node_b(row_ptr, N, p0) : N;
+    int n = p0 < vend ? first_node_warp(row_ptr, N, p0, lane) : N;
     for (int64_t pos = p0; pos < p1; ++pos) {
         int d = -1;
         if (pos < vend) {

@@ -163,14 +163,6 @@ __device__ __forceinline__ void add_edge32(const TileView& v, int j, float4 acc[
     acc[3] = f4_fma(crow[3], b, acc[3]);   // row 15 of group 3 is padding, never stored
 }
 
-// First node to visit for a window starting at p0: the node containing p0
-// when it starts before p0, else the first node starting at or after p0.
-__device__ __forceinline__ int first_node(const int32_t* __restrict__ row_ptr, int32_t N, int64_t p0) {
-    const int n_lb = lower_bound_i32(row_ptr, N + 1, p0);
-    if (n_lb >= 1 && n_lb <= N && (int64_t)__ldg(row_ptr + n_lb) > p0) return n_lb - 1;
-    return n_lb;
-}
-
 __device__ __forceinline__ void load_part32_cg(const float* __restrict__ part, float4 acc[4], const Lane32& L) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -381,7 +373,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         // current node n covers positions [a, b); empty nodes this window owns
         // (those starting in it, or all trailing ones for the last window) are zeroed
         // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead
-        int n = first_node(row_ptr, N, p0);
+        int n = first_node_warp(row_ptr, N, p0, lane);
         int a = n < N ? __ldg(row_ptr + n) : 0;
         int b = n < N ? __ldg(row_ptr + n + 1) : 0;
         int c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
@@ -495,19 +487,28 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     if (pend_node < 0) return;
     // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
     // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
+    // (the lanes wait for the flags in parallel, and the partials are loaded
+    // a few at a time before they are added, still in CTA order: a global
+    // access costs several hundred nanoseconds, and on a skewed graph a node
+    // spans tens of CTAs)
     const int b0 = (int)(__ldg(row_ptr + pend_node) / span);
-    if (lane == 0)
-        for (int k = b0; k < (int)blockIdx.x; ++k) {
-            wait_flag(flags, k, tag);
-            flags[k] = 0;
-        }
+    const int bx = (int)blockIdx.x;
+    for (int k = b0 + lane; k < bx; k += 32) {
+        wait_flag(flags, k, tag);
+        flags[k] = 0;
+    }
     __syncwarp();
+    constexpr int kB = sizeof(Acc) <= 64 ? 4 : 1;   // partials in flight, within the register budget
     Acc total;
     lay.load_cg(cta_part + ((int64_t)b0 * 2 + 1) * P::kPartFloats, total);
-    for (int k = b0 + 1; k < (int)blockIdx.x; ++k) {
-        Acc t;
-        lay.load_cg(cta_part + (int64_t)k * 2 * P::kPartFloats, t);
-        P::add_to(total, t);
+    for (int k0 = b0 + 1; k0 < bx; k0 += kB) {
+        Acc t[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+            if (k0 + u < bx) lay.load_cg(cta_part + (int64_t)(k0 + u) * 2 * P::kPartFloats, t[u]);
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+            if (k0 + u < bx) P::add_to(total, t[u]);
     }
     P::add_to(total, pend);
     lay.put(o, pend_node, total);
@@ -577,7 +578,7 @@ fwd_gen_main(const float* __restrict__ coup, int cld, const float* __restrict__ 
     const int64_t p1 = min(p0 + kGenWin, E);
     const bool is_last = gw == Wtot - 1;
     int crossing = -1;   // the node that starts in this window and continues past it
-    for (int n = first_node(row_ptr, N, p0); n < N; ++n) {
+    for (int n = first_node_warp(row_ptr, N, p0, lane); n < N; ++n) {
         const int a = __ldg(row_ptr + n), b = __ldg(row_ptr + n + 1);
         if (a >= p1 && !(is_last && a == b)) break;
         float* node = o.out + (int64_t)n * D * C;
