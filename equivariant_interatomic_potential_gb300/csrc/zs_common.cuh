@@ -164,6 +164,41 @@ __device__ __forceinline__ int lower_bound_warp(const int32_t* a, int n, int64_t
     return lo;
 }
 
+// lower_bound_warp split into rounds, so that a kernel can interleave the
+// search's dependent loads with other start-up loads: begin() issues the
+// first round's loads, resolve() consumes a round and load() issues the
+// next, until done().
+struct WarpSearch {
+    int lo, hi, step, idx, v;
+    int64_t key;
+    __device__ __forceinline__ void begin(const int32_t* a, int n, int64_t key_, int lane) {
+        lo = 0;
+        hi = n;
+        key = key_;
+        load(a, lane);
+    }
+    __device__ __forceinline__ void load(const int32_t* a, int lane) {
+        if (lo >= hi) return;
+        step = ((hi - lo) + 31) >> 5;
+        idx = lo + lane * step;
+        v = idx < hi ? __ldg(a + idx) : 0;
+    }
+    __device__ __forceinline__ bool done() const { return lo >= hi; }
+    __device__ __forceinline__ void resolve() {
+        if (lo >= hi) return;
+        const bool ge = idx >= hi || (int64_t)v >= key;
+        const unsigned m = __ballot_sync(0xffffffffu, ge);
+        if (m == 0) {
+            lo += 31 * step + 1;
+        } else {
+            const int f = __ffs(m) - 1;
+            const int nhi = lo + f * step < hi ? lo + f * step : hi;
+            if (f > 0) lo += (f - 1) * step + 1;
+            hi = nhi;
+        }
+    }
+};
+
 // The first CSR node a window of positions starting at p0 visits: the node
 // containing p0 when it starts before p0, else the first node starting at or
 // after p0 (which may be empty).  Whole warp, as lower_bound_warp.

@@ -344,6 +344,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     static_assert(2 * P::kPartFloats * 4 <= Layout::kRad + Layout::kCoup, "two partials fit a warp's idle ring");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int sp_node[W][2];
+    __shared__ int2 sp_rows[W][2];                     // (row_ptr[m], row_ptr[m + 1]) of sp_node's nodes
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     P lay(lane);
@@ -354,10 +355,19 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
     const bool is_last = gw == Wtot - 1;
+    // Start-up.  A dependent global load costs several hundred nanoseconds,
+    // so the independent ones go out together: the end of the valid
+    // positions (vend), the first perm blocks and the first round of the
+    // search for the window's first node; the ring's first tiles are issued
+    // as soon as perm arrives, while the search finishes.
     const int vend = __ldg(row_ptr + N);              // positions from vend on hold no node
-    const int pe = imax(p0, imin(p1, vend));
+    WarpSearch ns;
+    if (active) ns.begin(row_ptr, N + 1, p0, lane);
     Ring ring;
-    ring.init(smem + (size_t)warp * Layout::kBytes, p0, active ? pe : p0, lane);
+    ring.init(smem + (size_t)warp * Layout::kBytes, p0, p1, lane);
+    if (active) ring.prefetch_perm(perm, lane);
+    const int pe = imax(p0, imin(p1, vend));
+    ring.set_end(active ? pe : p0);
     lay.bind(ring);
     if (lane < 2) sp_node[warp][lane] = -1;
     __syncwarp();
@@ -367,16 +377,29 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     P::zero(acc);
     bool have0 = false, have1 = false;
     if (active) {
-        ring.prefetch_perm(perm, lane);
+        ns.resolve();
+        ns.load(row_ptr, lane);
 #pragma unroll
         for (int i = 0; i < S; ++i) ring.issue(perm, coup, cld, rad, E, lane);
+        while (!ns.done()) {
+            ns.resolve();
+            ns.load(row_ptr, lane);
+        }
         // current node n covers positions [a, b); empty nodes this window owns
         // (those starting in it, or all trailing ones for the last window) are zeroed
-        // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead
-        int n = first_node_warp(row_ptr, N, p0, lane);
-        int a = n < N ? __ldg(row_ptr + n) : 0;
-        int b = n < N ? __ldg(row_ptr + n + 1) : 0;
-        int c = n + 2 <= N ? __ldg(row_ptr + n + 2) : 0;
+        // a = row_ptr[n], b = row_ptr[n+1]; c = row_ptr[n+2] is fetched one node ahead.
+        // The first node is n_lb (first row_ptr entry >= p0) or the one before it;
+        // row_ptr[n_lb - 1 .. n_lb + 2] arrive in one round (lane k holds entry n_lb - 1 + k).
+        const int n_lb = ns.lo;
+        const int ik = n_lb - 1 + lane;
+        const int rk = (lane < 4 && ik >= 0 && ik <= N) ? __ldg(row_ptr + ik) : 0;
+        const int r0 = __shfl_sync(0xffffffffu, rk, 0), r1 = __shfl_sync(0xffffffffu, rk, 1);
+        const int r2 = __shfl_sync(0xffffffffu, rk, 2), r3 = __shfl_sync(0xffffffffu, rk, 3);
+        const bool back = n_lb >= 1 && n_lb <= N && (int64_t)r1 > p0;
+        int n = back ? n_lb - 1 : n_lb;
+        int a = n < N ? (back ? r0 : r1) : 0;
+        int b = n < N ? (back ? r1 : r2) : 0;
+        int c = n + 2 <= N ? (back ? r2 : r3) : 0;
         auto step = [&]() {
             ++n;
             a = b;
@@ -412,7 +435,10 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
                     } else {
                         acc0 = acc;
                         have0 = true;
-                        if (lane == 0) sp_node[warp][0] = n;
+                        if (lane == 0) {
+                            sp_node[warp][0] = n;
+                            sp_rows[warp][0] = make_int2(a, b);
+                        }
                     }
                     P::zero(acc);
                     step();
@@ -426,10 +452,16 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
             if (a < p0) {
                 acc0 = acc;
                 have0 = true;
-                if (lane == 0) sp_node[warp][0] = n;
+                if (lane == 0) {
+                    sp_node[warp][0] = n;
+                    sp_rows[warp][0] = make_int2(a, b);
+                }
             } else {
                 have1 = true;
-                if (lane == 0) sp_node[warp][1] = n;
+                if (lane == 0) {
+                    sp_node[warp][1] = n;
+                    sp_rows[warp][1] = make_int2(a, b);
+                }
             }
         }
     }
@@ -446,6 +478,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     const int64_t P0 = imin<int64_t>((int64_t)blockIdx.x * span, E);
     const int64_t P1 = imin<int64_t>(P0 + span, E);
     int pend_node = -1;                      // a node that started in an earlier CTA and ends here
+    int pend_ma = 0;                         // its first position
     Acc pend;
     __shared__ int s_stored;                 // this CTA left a partial for a later CTA
     if (threadIdx.x == 0) s_stored = 0;
@@ -462,11 +495,12 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
             lay.load(reinterpret_cast<const float*>(smem + (size_t)w2 * Layout::kBytes), t);
             P::add_to(sum, t);
         }
-        const int ma = __ldg(row_ptr + m), mb = __ldg(row_ptr + m + 1);
+        const int ma = sp_rows[warp][slot].x, mb = sp_rows[warp][slot].y;
         if (ma >= P0 && mb <= P1) {
             lay.put(o, m, sum);
         } else if (ma < P0 && mb <= P1) {
             pend_node = m;
+            pend_ma = ma;
             pend = sum;
         } else {
             // slot 1: starts here and runs past this CTA; slot 0: covers all of it
@@ -491,7 +525,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     // a few at a time before they are added, still in CTA order: a global
     // access costs several hundred nanoseconds, and on a skewed graph a node
     // spans tens of CTAs)
-    const int b0 = (int)(__ldg(row_ptr + pend_node) / span);
+    const int b0 = (int)(pend_ma / span);
     const int bx = (int)blockIdx.x;
     for (int k = b0 + lane; k < bx; k += 32) {
         wait_flag(flags, k, tag);

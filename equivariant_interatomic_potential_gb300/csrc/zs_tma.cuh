@@ -138,6 +138,14 @@ struct TileRing {
         __syncwarp();
     }
 
+    // Narrow the range to [p0, pe_) once its end is known (the ring may have
+    // been set up for a wider range so that its first perm blocks could be
+    // fetched early; entries fetched past pe_ are never issued).
+    __device__ __forceinline__ void set_end(int pe_) {
+        pe = pe_;
+        ntiles = pe > p0 ? (pe - p0 + T - 1) / T : 0;
+    }
+
     __device__ __forceinline__ int load_block(const int32_t* __restrict__ perm, int blk, int lane) const {
         const int j = p0 + blk * 32 + lane;
         return (blk * kPB < ntiles && j < pe) ? ld_hint_i(perm + j, pol) : -1;
