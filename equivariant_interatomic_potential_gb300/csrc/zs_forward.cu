@@ -43,7 +43,7 @@ constexpr int kFwdThreads = kFwdWarps * 32;
 #define ZS_FWD_STAGES 2
 #endif
 #ifndef ZS_FWD_TILE
-#define ZS_FWD_TILE 8
+#define ZS_FWD_TILE 16
 #endif
 constexpr int kTmaWarps = ZS_FWD_WARPS;
 constexpr int kTmaStages = ZS_FWD_STAGES;
