@@ -73,53 +73,71 @@ csr_upsweep(const int32_t* __restrict__ keys_in, int64_t E, int32_t N, int shift
     pdl_wait();
     pdl_trigger();
     __syncthreads();
-    // counts do not depend on the order of the increments
+    // counts do not depend on the order of the increments; the tile's keys
+    // are all loaded before the first increment (one round trip, not eight)
     const int64_t base = (int64_t)blockIdx.x * kTile;
-    for (int i = tid; i < kTile; i += kCsrThreads) {
-        const int64_t idx = base + i;
-        if (idx < E) atomicAdd(&cnt[(key_of(keys_in, idx, N, kFirst) >> shift) & (kRadix - 1)], 1);
+    int dig[kTile / kCsrThreads];
+#pragma unroll
+    for (int u = 0; u < kTile / kCsrThreads; ++u) {
+        const int64_t idx = base + u * kCsrThreads + tid;
+        dig[u] = idx < E ? (key_of(keys_in, idx, N, kFirst) >> shift) & (kRadix - 1) : -1;
     }
+#pragma unroll
+    for (int u = 0; u < kTile / kCsrThreads; ++u)
+        if (dig[u] >= 0) atomicAdd(&cnt[dig[u]], 1);
     __syncthreads();
     hist[(int64_t)tid * T + blockIdx.x] = cnt[tid];
 }
 
-// One warp per row: exclusive scan of hist[d, 0..T) in place, total to tot[d],
-// for rows d < rows (digits of the radix path, nodes of the counting path).
+// One CTA per row: exclusive scan of hist[d, 0..T) in place, total to tot[d].
+// Thread i takes the consecutive entries [i * per, (i + 1) * per), all loaded
+// before they are added (a row is one round trip of loads, not one per
+// 256 entries).
+constexpr int kScanPer = 16;
 __global__ void __launch_bounds__(kCsrThreads)
-csr_scan(int32_t* __restrict__ hist, int T, int rows, int32_t* __restrict__ tot) {
-    constexpr int R = 8;
-    const int lane = threadIdx.x & 31;
-    const int d = blockIdx.x * kCsrWarps + (threadIdx.x >> 5);
+csr_scan(int32_t* __restrict__ hist, int T, int32_t* __restrict__ tot) {
+    __shared__ int wsum[kCsrWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t* row = hist + (int64_t)blockIdx.x * T;
     pdl_wait();
     pdl_trigger();
-    if (d >= rows) return;
-    int32_t* row = hist + (int64_t)d * T;
     int carry = 0;
-    for (int base = 0; base < T; base += 32 * R) {
-        int v[R];
-        int s = 0;
+    for (int c0 = 0; c0 < T; c0 += kScanPer * kCsrThreads) {
+        const int per = imin(kScanPer, (imin(T - c0, kScanPer * kCsrThreads) + kCsrThreads - 1) / kCsrThreads);
+        const int i0 = c0 + tid * per;
+        int v[kScanPer];
+        int own = 0;
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            const int i = base + lane * R + k;
-            v[k] = i < T ? row[i] : 0;
-            s += v[k];
+        for (int k = 0; k < kScanPer; ++k) {
+            v[k] = (k < per && i0 + k < T) ? row[i0 + k] : 0;
+            own += v[k];
         }
-        int incl = s;
+        int incl = own;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += y;
         }
-        int run = carry + incl - s;
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int pre = carry;
+        int all = carry;
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            const int i = base + lane * R + k;
-            if (i < T) row[i] = run;
-            run += v[k];
+        for (int w = 0; w < kCsrWarps; ++w) {
+            if (w < warp) pre += wsum[w];
+            all += wsum[w];
         }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+        int run = pre + incl - own;
+#pragma unroll
+        for (int k = 0; k < kScanPer; ++k)
+            if (k < per && i0 + k < T) {
+                row[i0 + k] = run;
+                run += v[k];
+            }
+        carry = all;
+        __syncthreads();
     }
-    if (lane == 0) tot[d] = carry;
+    if (tid == 0) tot[blockIdx.x] = carry;
 }
 
 template <bool kFirst>
@@ -137,6 +155,8 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
     pdl_wait();
     pdl_trigger();
 
+    // this tile's offset within each digit, loaded now beside the totals
+    const int hv = hist[(int64_t)tid * T + blockIdx.x];
     // Exclusive scan of the 256 digit totals (kCsrThreads == kRadix).
     {
         const int v = tot[tid];
@@ -158,6 +178,8 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
     int32_t key[kCsrItems], val[kCsrItems];
     int rank[kCsrItems], dig[kCsrItems];
     const unsigned lt = lanemask_lt();
+    // every item's key and value are loaded before the ranking starts (its
+    // warp synchronisations would otherwise hold each load back to its round)
 #pragma unroll
     for (int i = 0; i < kCsrItems; ++i) {
         const int64_t idx = base + i * 32 + lane;
@@ -165,6 +187,10 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
         key[i] = valid ? key_of(keys_in, idx, N, kFirst) : 0;
         val[i] = valid ? (kFirst ? (int32_t)idx : __ldg(vals_in + idx)) : 0;
         dig[i] = valid ? ((key[i] >> shift) & (kRadix - 1)) : kRadix;
+    }
+#pragma unroll
+    for (int i = 0; i < kCsrItems; ++i) {
+        const bool valid = dig[i] < kRadix;
         const unsigned peers = digit_peers(dig[i] & (kRadix - 1), valid);
         rank[i] = valid ? cnt[warp][dig[i]] + __popc(peers & lt) : 0;
         __syncwarp();
@@ -196,7 +222,7 @@ csr_downsweep(const int32_t* __restrict__ keys_in, const int32_t* __restrict__ v
         for (int w = 0; w < warp; ++w) pre += wsum[w];
         const int local = pre + incl - own;  // first tile slot of digit d
         // global position of the tile's first key of digit d, minus its tile slot
-        dbase[d] = dbase[d] + hist[(int64_t)d * T + blockIdx.x] - local;
+        dbase[d] = dbase[d] + hv - local;
 #pragma unroll
         for (int w = 0; w < kCsrWarps; ++w) cnt[w][d] += local;
     }
@@ -591,7 +617,7 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
             int32_t* vout = last ? perm : reinterpret_cast<int32_t*>(ws + p.off_v[pass & 1]);
             if (first) launch(csr_upsweep<true>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
             else launch(csr_upsweep<false>, p.T, kCsrThreads, 0, s, kin, E, N, shift, hist, p.T);
-            launch(csr_scan, kRadix / kCsrWarps, kCsrThreads, 0, s, hist, p.T, kRadix, tot);
+            launch(csr_scan, kRadix, kCsrThreads, 0, s, hist, p.T, tot);
             if (first) launch(csr_downsweep<true>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
             else launch(csr_downsweep<false>, p.T, kCsrThreads, 0, s, kin, vin, E, N, shift, (const int32_t*)hist, (const int32_t*)tot, p.T, kout, vout);
             kin = kout;
