@@ -614,7 +614,18 @@ bwd_csr_gen(const float* __restrict__ g, const float* __restrict__ coup, const f
 }
 
 constexpr int64_t kSmallCotangentBytes = int64_t(16) << 20;   // 16 MiB
-constexpr int kEdgeWarpsSmall = 12;   // 2-stage rings of 4 edges: 12 warps fit one SM's shared memory
+#ifndef ZS_EDGE_SMALL_W
+#define ZS_EDGE_SMALL_W 12
+#endif
+#ifndef ZS_EDGE_SMALL_S
+#define ZS_EDGE_SMALL_S 2
+#endif
+#ifndef ZS_EDGE_SMALL_T
+#define ZS_EDGE_SMALL_T 4
+#endif
+constexpr int kEdgeWarpsSmall = ZS_EDGE_SMALL_W;   // 2-stage rings of 4 edges: 12 warps fit one SM's shared memory
+constexpr int kEdgeStagesSmall = ZS_EDGE_SMALL_S;
+constexpr int kEdgeTileSmall = ZS_EDGE_SMALL_T;
 constexpr int kEdgeWarpsLarge = 8;    // 3-stage rings of 4 edges: 8 warps
 
 // One warp waits on an mbarrier that nothing arrives on, with a limit of
@@ -840,7 +851,8 @@ static zs_status backward_impl(const char* name, const float* g, const float* co
         // tiles in flight per warp.
         const bool small_g = (int64_t)N * 16 * kC32 * 4 <= kSmallCotangentBytes;
         if (small_g)
-            launch_edge_quad<3, kEdgeWarpsSmall, 2, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
+            launch_edge_quad<3, kEdgeWarpsSmall, kEdgeStagesSmall, kEdgeTileSmall>(g, coup, (int)cld, rad, dst, E, N, d_coup,
+                                                                                    (int)dld, d_rad, scale, s);
         else
             launch_edge_quad<3, kEdgeWarpsLarge, 3, 4>(g, coup, (int)cld, rad, dst, E, N, d_coup, (int)dld, d_rad, scale, s);
     } else {

@@ -46,6 +46,11 @@
  *   - Destinations outside [0, N) belong to no node (reading of the pages,
  *     which leave them undefined): the CSR build counts them and places them
  *     after all valid edges; the backward gives those edges zero gradients.
+ *   - Operands are contiguous row-major arrays (the coupling rows may be
+ *     strided through the *_ld entry points).  As on the pages, where the
+ *     inputs are flattened to contiguous before they enter the operator, a
+ *     caller holding a sliced view of the radial operand makes it
+ *     contiguous first; the PyTorch operators over this library do that.
  *   - Any C >= 1 is accepted.  C == 32 with 16-byte aligned float4 operands
  *     (rad and out in the forward; g, rad and d_rad in the backward) takes
  *     the vectorised path; every other case takes a per-channel path with

@@ -167,3 +167,42 @@ def test_operator_raises_on_timeout_flag():
     out2 = ag.zonal_scatter_from_dst(coup, rad, dst, w.N)
     torch.cuda.synchronize()
     assert int(flag[0]) == 0 and torch.equal(out, out2)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("how", ["slots", "channels", "edges"])
+def test_sliced_view_radial_inputs(how):
+    # A radial operand that is a view into a wider buffer (a slice of its
+    # slot axis, of its channel axis, or every other edge row).  As on the
+    # pages, the operator makes its inputs contiguous before the kernels;
+    # the gradient flows back into the wider buffer through the view.
+    w = workloads.make_random(300, 20000, 32, seed=31, hot_node=4, hot_fraction=0.3)
+    E, C = w.E, w.C
+    rad = dev(w.rad)
+    if how == "slots":
+        base = torch.zeros((E, 4, C), device="cuda")
+        base[:, 1:] = rad
+        view = lambda b: b[:, 1:, :]  # noqa: E731
+    elif how == "channels":
+        base = torch.zeros((E, 3, C + 8), device="cuda")
+        base[:, :, 4:4 + C] = rad
+        view = lambda b: b[:, :, 4:4 + C]  # noqa: E731
+    else:
+        base = torch.zeros((2 * E, 3, C), device="cuda")
+        base[::2] = rad
+        view = lambda b: b[::2]  # noqa: E731
+    base.requires_grad_(True)
+    coup = dev(w.coup).requires_grad_(True)
+    v = view(base)
+    assert not v.is_contiguous()
+    out = ag.zonal_scatter_from_dst(coup, v, dev(w.dst), w.N)
+    d_coup, d_base = torch.autograd.grad(out, (coup, base), dev(w.grad_out))
+    row_ptr, perm, _ = oracle.build_csr(w.dst, w.N)
+    ref, absum = oracle.forward(w.coup, w.rad, row_ptr, perm, w.N)
+    assert_close(out.detach().cpu().numpy(), ref, absum, "forward")
+    dc, dr, adc, adr = oracle.backward(w.grad_out, w.coup, w.rad, w.dst, w.N)
+    assert_close(d_coup.cpu().numpy(), dc, adc, "d_coup")
+    assert_close(view(d_base).cpu().numpy(), dr, adr, "d_rad")
+    mask = torch.ones_like(d_base, dtype=torch.bool)
+    view(mask).fill_(False)
+    assert torch.all(d_base[mask] == 0)
