@@ -361,9 +361,12 @@ struct EdgeRingLayout {
     static constexpr int kG = S * T * R * kC32 * 4;   // cotangent rows 1..R per edge
     static constexpr int kRad = S * T * LM * kC32 * 4;
     static constexpr int kCoup = S * T * R * 4;
-    static constexpr int kMeta = S * T * 4;
+    static constexpr int kMeta = (S * T * 4 + 15) / 16 * 16;
     static constexpr int kBars = S * 8;
     static constexpr int kBytes = (kG + kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
+    // bulk-copy destinations start on 16-byte boundaries, mbarriers on 8-byte ones
+    static_assert(kG % 16 == 0 && kRad % 16 == 0 && kCoup % 16 == 0 && kMeta % 16 == 0, "16-byte aligned regions");
+    static_assert((kG + kRad + kCoup + kMeta) % 8 == 0, "mbarriers 8-byte aligned");
 };
 template <int S, int T, int LM = 3>
 struct EdgeRing {
@@ -514,7 +517,8 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
     int sample = -1;
     if (active) {
         ring.prefetch(dst, Q.lane);
-        sample = ring.blk_cur;
+        // votes only for destinations that are nodes (others have no cotangent rows)
+        sample = (ring.blk_cur >= 0 && ring.blk_cur < N) ? ring.blk_cur : -1;
 #pragma unroll
         for (int i = 0; i < S; ++i) ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
     }

@@ -91,6 +91,8 @@ struct RingLayout {
     static constexpr int kMeta = S * T * 8;                                 // (edge id, coupling offset)
     static constexpr int kBars = S * 8;
     static constexpr int kBytes = (kRad + kCoup + kMeta + kBars + 127) / 128 * 128;
+    // copy destinations start on 16-byte boundaries, mbarriers on 8-byte ones
+    static_assert(kRad % 16 == 0 && kCoup % 16 == 0 && kMeta % 8 == 0, "aligned regions");
 };
 
 // One warp's stream of tiles over [p0, pe).  kPol is the L2 policy of the

@@ -165,6 +165,23 @@ def test_out_of_range_destinations(C):
     assert np.all(res["d_coup"][idx] == 0) and np.all(res["d_rad"][idx] == 0)
 
 
+@pytest.mark.parametrize("N,bad_fraction", [(0, 1.0), (50, 0.8), (4096, 0.5)])
+def test_out_of_range_destinations_dominate(N, bad_fraction):
+    # most edges share one out-of-range destination: the edge-order backward's
+    # per-CTA hot-destination vote must pass over it (it has no cotangent rows)
+    w = workloads.make_random(max(N, 1), 60000, 32, seed=17 + N)
+    rng = np.random.default_rng(18 + N)
+    idx = rng.random(w.E) < bad_fraction
+    w.dst[idx] = N + 3
+    w.dst[~idx] = np.minimum(w.dst[~idx], max(N - 1, 0))
+    w = workloads.Workload(w.name, N, w.E, w.C, w.seed, w.src, w.dst, w.coup, w.rad, w.grad_out[:N])
+    res = run_gpu(w)
+    row_ptr, perm = check_csr(w, res)
+    check_forward(w, res, row_ptr, perm)
+    check_backward(w, res)
+    assert np.all(res["d_coup"][idx] == 0) and np.all(res["d_rad"][idx] == 0)
+
+
 @pytest.mark.parametrize("N", [1, 2, 255, 256, 257, 4095, 4096, 65535, 65536, 65537, 300000])
 def test_csr_radix_pass_boundaries(N):
     rng = np.random.default_rng(N)
