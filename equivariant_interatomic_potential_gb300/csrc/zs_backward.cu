@@ -495,6 +495,7 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
     static_assert(T % 4 == 0, "tiles hold whole groups of four edges");
     constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D, RF = LM * kC32;
     constexpr int K = (R + 7) / 8;
+    constexpr bool kEarlyRefill = T == 4 && R <= 15;   // one edge per group, its rows fit in registers
     using Ring = EdgeRing<S, T, LM>;
     using Layout = EdgeRingLayout<S, T, LM>;
     const float* __restrict__ scale = kGeneral ? scale_arg : nullptr;
@@ -533,6 +534,63 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
         for (int k = 0; k < ring.ntiles; ++k) {
             const int st = ring.acquire();
             const int e0 = p0 + k * T;
+            if constexpr (kEarlyRefill) {
+                // One edge per group: its rows go to registers first, and the
+                // stage is refilled before the arithmetic, so the next tile's
+                // copies are in flight a few hundred cycles sooner (the ring
+                // is only two stages deep).  Same arithmetic, same order.
+                const int j = Q.grp;
+                const int m = ring.meta[st * T + j];
+                const float sc = (scale && m >= 0) ? __ldg(scale + m) : 1.f;
+                const float* gj = (m == hot ? hot_g : ring.gs + (st * T + j) * (R * kC32)) + 4 * Q.q;
+                const float* rrow = ring.rads + (st * T + j) * RF + 4 * Q.q;
+                float4 a[LM];
+#pragma unroll
+                for (int l = 0; l < LM; ++l) a[l] = *reinterpret_cast<const float4*>(rrow + l * kC32);
+                const float* crow = ring.coups + st * T * R + j * R;
+                float c[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) c[r] = crow[r];
+                float4 G[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) G[r] = *reinterpret_cast<const float4*>(gj + r * kC32);
+                __syncwarp();
+                ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
+                float4 sl[LM];
+                float pr[8 * K];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int l = ladder_slot(r);
+                    if ((l + 1) * (l + 1) - 1 == r)   // first row of its degree
+                        sl[l] = make_float4(c[r] * G[r].x, c[r] * G[r].y, c[r] * G[r].z, c[r] * G[r].w);
+                    else
+                        sl[l] = f4_fma(c[r], G[r], sl[l]);
+                    pr[r] = f4_dot(G[r], a[l]);
+                }
+#pragma unroll
+                for (int r = R; r < 8 * K; ++r) pr[r] = 0.f;
+                float t[K];
+                group_reduce<K>(pr, Q, t);
+                if (m == -2) continue;
+                const bool ok = m >= 0;
+                const int64_t e = e0 + j;
+                const int row = 4 * K * Q.b2 + 2 * K * Q.b1 + K * Q.b0;
+                float* dc = d_coup + e * dld + row;
+                float* dr = d_rad + e * RF + 4 * Q.q;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (scale && ok) {
+#pragma unroll
+                    for (int l = 0; l < LM; ++l) sl[l] = make_float4(sl[l].x * sc, sl[l].y * sc, sl[l].z * sc, sl[l].w * sc);
+#pragma unroll
+                    for (int q = 0; q < K; ++q) t[q] *= sc;
+                }
+#pragma unroll
+                for (int l = 0; l < LM; ++l) st_hint4(dr + l * kC32, ok ? sl[l] : z, pol_out);
+#pragma unroll
+                for (int q = 0; q < K; ++q)
+                    if (row + q < R) st_stream(dc + q, ok ? t[q] : 0.f);
+                continue;
+            }
 #pragma unroll
             for (int i = 0; i < T / 4; ++i) {
                 const int j = 4 * i + Q.grp;
