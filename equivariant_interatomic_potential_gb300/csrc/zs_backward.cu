@@ -578,7 +578,7 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
                 float* dc = d_coup + e * dld + row;
                 float* dr = d_rad + e * RF + 4 * Q.q;
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (scale && ok) {
+                if (scale && ok) {   // gradients of the scaled output: the destination's scale times these
 #pragma unroll
                     for (int l = 0; l < LM; ++l) sl[l] = make_float4(sl[l].x * sc, sl[l].y * sc, sl[l].z * sc, sl[l].w * sc);
 #pragma unroll
@@ -589,8 +589,7 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
 #pragma unroll
                 for (int q = 0; q < K; ++q)
                     if (row + q < R) st_stream(dc + q, ok ? t[q] : 0.f);
-                continue;
-            }
+            } else {
 #pragma unroll
             for (int i = 0; i < T / 4; ++i) {
                 const int j = 4 * i + Q.grp;
@@ -642,6 +641,7 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
             }
             __syncwarp();
             ring.issue(dst, coup, cld, coup_bulk != 0, rad, g, N, Q.lane);
+            }
         }
     }
     ring.drain();

@@ -24,7 +24,16 @@
 namespace zs {
 
 constexpr int kCoupSlotFloats = 20;         // coupling slot of the 15-row ladder (coup_slot_floats(15))
-constexpr uint32_t kRingArrivals = 33;      // the expect-tx arrival plus one cp.async arrival per lane
+// The coupling spans travel as 16-byte cp.async pieces signalled by one
+// arrival per lane (default), or as one bulk copy per edge counted in bytes
+// like the radial rows (ZS_RING_COUP_BULK=1: measured slower for the forward,
+// 62 against 57 us on the 4096-node graph; the small bulk copies cost more
+// than the pieces).
+#ifndef ZS_RING_COUP_BULK
+#define ZS_RING_COUP_BULK 0
+#endif
+constexpr bool kCoupBulk = ZS_RING_COUP_BULK != 0;
+constexpr uint32_t kRingArrivals = kCoupBulk ? 1 : 33;   // the expect-tx arrival (plus one cp.async arrival per lane)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -205,20 +214,25 @@ struct TileRing {
             meta[st * T + lane] = make_int2(valid ? e : -1, off);
         }
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        const uint32_t cbytes = kCoupBulk ? __reduce_add_sync(0xffffffffu, (valid && !tail) ? 16u * nch : 0u) : 0u;
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadBytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadBytes + cbytes);
         __syncwarp();
         if (valid) {
             bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * RadFloats, kRadBytes, bar, pol);
             if (!tail) {
                 const char* src = reinterpret_cast<const char*>(coup_g) - mis + cstart;
                 const uint32_t dst = smem_u32(cslot);
+                if constexpr (kCoupBulk) {
+                    bulk_g2s(dst, src, 16u * nch, bar, pol_c);
+                } else {
 #pragma unroll
-                for (int k = 0; k < kChunks; ++k)
-                    if (k < nch) cp_async16(dst + 16 * k, src + 16 * k, pol_c);
+                    for (int k = 0; k < kChunks; ++k)
+                        if (k < nch) cp_async16(dst + 16 * k, src + 16 * k, pol_c);
+                }
             }
         }
-        cp_async_arrive(bar);
+        if constexpr (!kCoupBulk) cp_async_arrive(bar);
     }
 
     // Wait for the next tile in order; returns its stage.
