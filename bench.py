@@ -125,6 +125,17 @@ def ncu_traffic(kernel_key: str, workload: str):
         return None
 
 
+def make_graph(config: str, lmax: int = 3):
+    """One of the named configurations, or "uniform:N:E" (a seeded graph of E
+    edges with uniform destinations over N nodes, C = 32: extra sizes for
+    profiling, not a headline workload)."""
+    from equivariant_interatomic_potential_gb300 import workloads
+    if config.startswith("uniform:"):
+        _, n, e = config.split(":")
+        return workloads.make_random(int(n), int(e), 32, seed=int(n) + int(e), lmax=lmax)
+    return workloads.make_workload(config, lmax=lmax)
+
+
 # ---------------------------------------------------------------- ranks
 
 def reduce_max(value: float, world: int, device) -> float:
@@ -227,7 +238,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    w = workloads.make_workload(args.config, lmax=args.lmax)
+    w = make_graph(args.config, lmax=args.lmax)
     N, E, C, L = w.N, w.E, w.C, args.lmax
     D, R = (L + 1) ** 2, (L + 1) ** 2 - 1
     dev = torch.device("cuda", local)
@@ -558,7 +569,8 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
             "achieved": kernels[dom]["GBs"], "peak": peak, "unit": "GB/s",
             "frac": kernels[dom]["GBs"] / peak, "peak_kind": peak_kind,
             "frac_of_nominal_8000": kernels[dom]["GBs"] / NOMINAL_HBM_GBS,
-            "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward, args.config) if L == 3 else None,
+            "traffic": ncu_traffic(dom if dom == "fwd" else "bwd_" + args.backward,
+                                   args.config if L == 3 else f"{args.config}@lmax{L}") if not args.scaled else None,
             "algorithmic_bytes_per_launch": ab[dom]}
     ms_per_step = total_ms / args.steps
     fwd_bwd_us = kernels["fwd"]["us_back_to_back"] + kernels["bwd"]["us_back_to_back"]
@@ -599,7 +611,7 @@ def run_oracle(config: str, min_seconds: float, w=None, lmax: int = 3, threads: 
     import oracle
     from equivariant_interatomic_potential_gb300 import workloads
 
-    w = workloads.make_workload(config, lmax=lmax) if w is None else w
+    w = make_graph(config, lmax=lmax) if w is None else w
     oracle.build()
     oracle.set_threads(threads)
     reps, t_csr, t_fwd, t_bwd = 0, 0.0, 0.0, 0.0
@@ -659,7 +671,7 @@ def main():
         if rank != 0:
             return
         from equivariant_interatomic_potential_gb300 import workloads
-        w = workloads.make_workload(args.config, lmax=args.lmax)
+        w = make_graph(args.config, lmax=args.lmax)
         cores = os.cpu_count() or 1
         t0 = time.perf_counter()
         steps = []
