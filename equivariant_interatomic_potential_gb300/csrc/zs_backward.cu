@@ -386,7 +386,7 @@ struct EdgeRing {
     uint64_t pol_stream, pol_g;
     int hot;        // destination whose cotangent rows the CTA holds in its hot slot, kNoHot for none
 
-    __device__ __forceinline__ void init(unsigned char* base, int p0_, int p1_, int lane) {
+    __device__ __forceinline__ void init(unsigned char* base, int p0_, int p1_, int lane, int stream_hint) {
         gs = reinterpret_cast<float*>(base);
         rads = reinterpret_cast<float*>(base + Layout::kG);
         coups = reinterpret_cast<float*>(base + Layout::kG + Layout::kRad);
@@ -397,7 +397,7 @@ struct EdgeRing {
         ntiles = p1 > p0 ? (p1 - p0 + T - 1) / T : 0;
         issued = 0;
         consumed = 0;
-        pol_stream = l2_evict_first();
+        pol_stream = l2_policy(stream_hint);
         pol_g = l2_evict_last();
         hot = kNoHot;
         if (lane < S) mbar_init(bar0 + 8 * lane, 1);
@@ -477,6 +477,21 @@ struct EdgeRing {
     }
 };
 
+// L2 policies of the edge-order backward's streams, chosen by measurement.
+// While the cotangent block is small next to L2 (kSmallCotangentBytes), the
+// radial, coupling and dst reads are evict-normal and the d_rad rows
+// evict-last: on the 4096-node graph that made the backward 4 % faster and
+// the kernel launched after it faster too (the cause was not isolated).  A
+// larger block loses its lines to evict-last stores (the 32768-node backward
+// was a third slower), so there the streams and the stores are evict-first.
+struct StreamPolicy {
+    int reads;    // L2 hint of the radial, coupling and dst reads
+    int grads;    // L2 hint of the d_rad stores
+};
+__host__ __device__ constexpr StreamPolicy stream_policy(bool small_cotangent) {
+    return small_cotangent ? StreamPolicy{kL2Normal, kL2EvictLast} : StreamPolicy{kL2EvictFirst, kL2EvictFirst};
+}
+
 // --------------------------------------------------------------------------
 // The edge-order C == 32 backward for the ladder of degree LM in the quad
 // lane layout: one edge per 8-lane group, lane q owns channels 4q..4q+3 of
@@ -491,7 +506,7 @@ __global__ void __launch_bounds__(W * 32, 1)
 bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const float* __restrict__ rad,
               const int32_t* __restrict__ dst, int E, int32_t N, int KW, int Wtot,
               float* __restrict__ d_coup, float* __restrict__ d_rad, const float* __restrict__ scale_arg,
-              int cld_arg, int dld_arg, int coup_bulk_arg) {
+              int cld_arg, int dld_arg, int coup_bulk_arg, StreamPolicy pol) {
     static_assert(T % 4 == 0, "tiles hold whole groups of four edges");
     constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D, RF = LM * kC32;
     constexpr int K = (R + 7) / 8;
@@ -512,9 +527,9 @@ bwd_edge_quad(const float* __restrict__ g, const float* __restrict__ coup, const
     const int p0 = active ? (int)imin<int64_t>((int64_t)gw * KW, E) : E;
     const int p1 = active ? (int)imin<int64_t>((int64_t)p0 + KW, E) : E;
     Ring ring;
-    ring.init(smem + (size_t)warp * Layout::kBytes, p0, p1, Q.lane);
+    ring.init(smem + (size_t)warp * Layout::kBytes, p0, p1, Q.lane, pol.reads);
     float* hot_g = reinterpret_cast<float*>(smem + (size_t)W * Layout::kBytes);
-    const uint64_t pol_out = l2_evict_first();
+    const uint64_t pol_out = l2_policy(pol.grads);
     int sample = -1;
     if (active) {
         ring.prefetch(dst, Q.lane);
@@ -814,16 +829,17 @@ void launch_edge_quad(const float* g, const float* coup, int cld, const float* r
     static_assert(W * EdgeRingLayout<S, T, LM>::kBytes + quad_hot_bytes<LM>() + W * 8 <= 232448,
                   "rings and hot slot fit an SM");
     const int bulk = (cld == R && aligned16(coup)) ? 1 : 0;
+    const StreamPolicy pol = stream_policy((int64_t)N * Ladder<LM>::D * kC32 * 4 <= kSmallCotangentBytes);
     if (scale == nullptr && dld == R && bulk) {
         static std::atomic<uint64_t> attr_done[kMaxDevices];
         set_smem_limit_once(bwd_edge_quad<W, S, T, LM, false>, smem, attr_done);
         launch(bwd_edge_quad<W, S, T, LM, false>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
-               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk, pol);
     } else {
         static std::atomic<uint64_t> attr_done[kMaxDevices];
         set_smem_limit_once(bwd_edge_quad<W, S, T, LM, true>, smem, attr_done);
         launch(bwd_edge_quad<W, S, T, LM, true>, (unsigned)ctas, W * 32, smem, s, g, coup, rad, dst, (int)E, N,
-               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk);
+               (int)KW, (int)Wtot, d_coup, d_rad, scale, cld, dld, bulk, pol);
     }
 }
 
