@@ -68,7 +68,7 @@ __host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
 // graph replays its kernel nodes with the same arguments and, as measured,
 // the same tag.  Protocols built on it must therefore leave no flag set
 // when the launch ends (see the forward), or take their tag from device
-// memory instead (see the CSR build's epoch).
+// memory instead (an epoch word that every launch advances).
 __device__ __forceinline__ uint64_t launch_tag(uint64_t salt) {
     uint64_t id;
     asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
