@@ -301,7 +301,29 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
                  :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem) : "memory");
 }
 
+// 8- and 16-byte copies (both addresses aligned to the size).
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
+                 :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async16b(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// n int32 from global src to shared dst (16-byte aligned): 16-byte pieces
+// when src is 16-byte aligned too, else 4-byte ones; CTA-cooperative.
+__device__ __forceinline__ void copy_ints(int32_t* dst, const int32_t* src, int n, int tid, int nthreads) {
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const int n4 = n >> 2;
+        for (int j = tid; j < n4; j += nthreads) cp_async16b(dst + 4 * j, src + 4 * j);
+        for (int i = 4 * n4 + tid; i < n; i += nthreads) cp_async4(dst + i, src + i);
+    } else {
+        for (int i = tid; i < n; i += nthreads) cp_async4(dst + i, src + i);
+    }
+}
 
 __device__ __forceinline__ int32_t clamp_key(int32_t k, int32_t N) { return (uint32_t)k < (uint32_t)N ? k : N; }
 
@@ -324,7 +346,7 @@ csr_count_rank(const int32_t* __restrict__ dst, int64_t E, int32_t N, int rounds
     pdl_wait();
     pdl_trigger();
     // the tile's keys land in packed[] while the counters are cleared
-    for (int i = tid; i < n_in_tile; i += kCntThreads) cp_async4(packed + i, dst + tbase + i);
+    copy_ints(reinterpret_cast<int32_t*>(packed), dst + tbase, n_in_tile, tid, kCntThreads);
     // kCntWarps * npairs words, a multiple of four
     for (int i = tid; i < kCntWarps * npairs / 4; i += kCntThreads) reinterpret_cast<uint4*>(cnt_words)[i] = make_uint4(0u, 0u, 0u, 0u);
     cp_async_wait_all();
@@ -440,10 +462,12 @@ csr_scan_cols(int32_t* __restrict__ M, int T, int S, int nkeys, int32_t* __restr
     }
 }
 
-// Shared memory of csr_count_scatter: the tile's row of M, the node totals,
-// kCntWarps warp sums, the tile's keys, its ranks (two per word).
+// Shared memory of csr_count_scatter (int32 words, each array starting on a
+// 16-byte boundary): the node totals, the tile's row of M, kCntWarps warp
+// sums, the tile's keys, its ranks (two per word).
+__host__ __device__ __forceinline__ int align4(int n) { return (n + 3) & ~3; }
 inline int count_scatter_smem(int nkeys, int rounds) {
-    return (2 * count_pairs(nkeys) + nkeys + kCntWarps + rounds * kCntThreads + rounds * kCntThreads / 2) * 4;
+    return (align4(nkeys) + align4(2 * count_pairs(nkeys)) + kCntWarps + rounds * kCntThreads + rounds * kCntThreads / 2) * 4;
 }
 
 // Dynamic shared memory requested so that no two CTAs of a kernel share an SM
@@ -459,11 +483,11 @@ csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ 
                   const int32_t* __restrict__ M, const int32_t* __restrict__ tot,
                   int64_t E, int32_t N, int rounds,
                   int32_t* __restrict__ perm, int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
-    extern __shared__ int32_t kbase[];
+    extern __shared__ __align__(16) int32_t ktot[];
     const int nkeys = N + 1;
     const int S = 2 * count_pairs(nkeys);
-    int32_t* ktot = kbase + S;
-    int32_t* wsum = ktot + nkeys;
+    int32_t* kbase = ktot + align4(nkeys);
+    int32_t* wsum = kbase + align4(S);
     int32_t* skey = wsum + kCntWarps;
     uint32_t* srank = reinterpret_cast<uint32_t*>(skey + rounds * kCntThreads);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -474,12 +498,15 @@ csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ 
     // every input of the tile in one batch of asynchronous copies: the tile's
     // row of M, the node totals, the tile's keys and its ranks (in pairs; the
     // tile starts on an even edge, an odd last edge is read directly)
-    for (int k = tid; k < nkeys; k += kCntThreads) {
-        cp_async4(kbase + k, M + (int64_t)blockIdx.x * S + k);
-        cp_async4(ktot + k, tot + k);
-    }
-    for (int i = tid; i < n_in_tile; i += kCntThreads) cp_async4(skey + i, dst + tbase + i);
-    for (int j = tid; j < n_in_tile / 2; j += kCntThreads) cp_async4(srank + j, rank + tbase + 2 * j);
+    // (rows of M are S = even counts long: 8-byte pieces; the rank array and
+    // the tile start are 16-byte aligned: 16-byte pieces of eight ranks)
+    const int32_t* mrow = M + (int64_t)blockIdx.x * S;
+    for (int j = tid; j < S / 2; j += kCntThreads) cp_async8(kbase + 2 * j, mrow + 2 * j);
+    copy_ints(ktot, tot, nkeys, tid, kCntThreads);
+    copy_ints(skey, dst + tbase, n_in_tile, tid, kCntThreads);
+    const int n8 = n_in_tile >> 3;
+    for (int j = tid; j < n8; j += kCntThreads) cp_async16b(srank + 4 * j, rank + tbase + 8 * j);
+    for (int j = 4 * n8 + tid; j < n_in_tile / 2; j += kCntThreads) cp_async4(srank + j, rank + tbase + 2 * j);
     if ((n_in_tile & 1) && tid == 0) srank[n_in_tile / 2] = __ldg(rank + tbase + n_in_tile - 1);
     cp_async_wait_all();
     __syncthreads();
