@@ -57,11 +57,15 @@ def algorithmic_bytes(N: int, E: int, C: int, lmax: int = 3) -> dict:
     return {"fwd": fwd, "bwd": bwd, "csr": csr}
 
 
-def kernel_figures(ab: dict, b2b: dict, per: dict, E: int, peak: float, peak_kind: str, names) -> dict:
+def kernel_figures(ab: dict, b2b: dict, per: dict, E: int, peak: float, peak_kind: str, names,
+                   marginal: dict | None = None) -> dict:
     """Per entry point: the roofline figures from the back-to-back launches
     (b2b: mean microseconds per launch) and, alongside, the launches
     bracketed inside a step (per: microseconds of each; launch latency and
-    the previous kernel's L2 write-backs included).  Fractions of the peak
+    the previous kernel's L2 write-backs included) and, where given, the
+    marginal cost in the step (marginal: the whole step's microseconds minus
+    those of the same step without that entry point, events only at the ends
+    of both loops, so programmatic overlap is kept).  Fractions of the peak
     in use and of the nominal 8 TB/s HBM3e rate."""
     kernels = {}
     for k in names:
@@ -73,6 +77,9 @@ def kernel_figures(ab: dict, b2b: dict, per: dict, E: int, peak: float, peak_kin
                       "edges_per_s": E / (us * 1e-6),
                       "us_in_step_mean": us_step, "us_in_step_median": statistics.median(per[k]),
                       "frac_in_step": ab[k] / (us_step * 1e-6) / 1e9 / peak}
+        if marginal and k in marginal:
+            kernels[k]["us_marginal_in_step"] = marginal[k]
+            kernels[k]["frac_marginal_in_step"] = ab[k] / (marginal[k] * 1e-6) / 1e9 / peak
     return kernels
 
 
@@ -391,6 +398,27 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         b.record(stream)
     torch.cuda.synchronize()
     per[other_name] = [a.elapsed_time(b) * 1e3 for a, b in oth]
+
+    # per-kernel durations (3): the step's time minus that of the same step
+    # without one entry point (its inputs are still valid: each set's CSR was
+    # built in the warm-up), K steps between two events each
+    def loop_us(fns):
+        for i in range(3):
+            for fn in fns:
+                fn(sets[i % n_sets])
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(args.steps):
+            for fn in fns:
+                fn(sets[i % n_sets])
+        z.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) * 1e3 / args.steps
+    step_us = loop_us((csr, fwd, bwd))
+    marginal = {"csr": step_us - loop_us((fwd, bwd)), "fwd": step_us - loop_us((csr, bwd)),
+                "bwd": step_us - loop_us((csr, fwd))}
     # per-kernel durations (2): K launches of one entry point back to back over
     # the rotating sets, events at the ends: the steady-state cost of a launch,
     # its own write-backs included and its launch latency overlapped
@@ -562,7 +590,7 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
         ab["bwd"] += extra["bwd"]
     peak, peak_kind = measured_peaks()
     ab["bwd_edge"] = ab["bwd_csr"] = ab["bwd"]
-    kernels = kernel_figures(ab, b2b, per, E, peak, peak_kind, ("csr", "fwd", "bwd", other_name))
+    kernels = kernel_figures(ab, b2b, per, E, peak, peak_kind, ("csr", "fwd", "bwd", other_name), marginal)
     dom = max(("fwd", "bwd"), key=lambda k: kernels[k]["us_back_to_back"])
     bwd_entry = "zs_backward_csr" if args.backward == "csr" else "zs_backward"
     roof = {"kernel": {"fwd": "zs_forward", "bwd": bwd_entry}[dom], "bound": "hbm",

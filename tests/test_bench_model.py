@@ -64,3 +64,13 @@ def test_kernel_figures():
     assert abs(f["edges_per_s"] - 1000 / 200e-6) < 1e-3
     assert f["us_in_step_mean"] == 300.0 and f["us_in_step_median"] == 250.0
     assert abs(f["frac_in_step"] - 10 ** 9 / 300e-6 / 1e9 / 10000.0) < 1e-12
+
+
+def test_kernel_figures_marginal():
+    # the marginal cost in the step: 1 GB in 250 us is 4000 GB/s, 0.4 of a 10000 GB/s peak
+    ab = {"fwd": 10 ** 9, "bwd": 10 ** 9}
+    k = bench.kernel_figures(ab, {"fwd": 200.0, "bwd": 200.0}, {"fwd": [300.0], "bwd": [300.0]}, 1000, 10000.0,
+                             "measured", ("fwd", "bwd"), {"fwd": 250.0})
+    assert k["fwd"]["us_marginal_in_step"] == 250.0
+    assert abs(k["fwd"]["frac_marginal_in_step"] - 0.4) < 1e-12
+    assert "us_marginal_in_step" not in k["bwd"]
