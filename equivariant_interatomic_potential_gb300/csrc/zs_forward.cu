@@ -483,12 +483,17 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     __shared__ int s_stored;                 // this CTA left a partial for a later CTA
     if (threadIdx.x == 0) s_stored = 0;
     __syncthreads();
+    // The sums of this warp's slots; the partial a later CTA needs is stored
+    // and published first, the finished nodes are written after the flag.
+    Acc sums[2];
+    int put_node[2] = {-1, -1};
+    bool wrote_part = false;
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot) {
         const int m = sp_node[warp][slot];
         if (m < 0) continue;
         if (warp > 0 && (sp_node[warp - 1][0] == m || sp_node[warp - 1][1] == m)) continue;
-        Acc sum;
+        Acc& sum = sums[slot];
         lay.load(part + slot * P::kPartFloats, sum);
         for (int w2 = warp + 1; w2 < W && sp_node[w2][0] == m; ++w2) {
             Acc t;
@@ -497,7 +502,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         }
         const int ma = sp_rows[warp][slot].x, mb = sp_rows[warp][slot].y;
         if (ma >= P0 && mb <= P1) {
-            lay.put(o, m, sum);
+            put_node[slot] = m;
         } else if (ma < P0 && mb <= P1) {
             pend_node = m;
             pend_ma = ma;
@@ -505,19 +510,23 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         } else {
             // slot 1: starts here and runs past this CTA; slot 0: covers all of it
             lay.store(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * P::kPartFloats, sum);
+            wrote_part = true;
             if (lane == 0) s_stored = 1;
         }
     }
     // Publish this CTA's partial (a CTA leaves at most one: for the node that
-    // runs past its end): every writer fences, then one release store of the
+    // runs past its end): its writers fence, then one release store of the
     // launch's tag.  Exactly one CTA consumes each published flag (the CTA
     // where that node ends) and resets it to 0 after its wait, so no flag
     // keeps a tag past the launch: a CUDA graph replays this launch with the
     // same tag, and must not find the previous replay's flags set.
-    __threadfence();
+    if (wrote_part) __threadfence();
     __syncthreads();
     const uint64_t tag = flag_tag(launch_tag(salt));
     if (threadIdx.x == 0 && s_stored) st_release_u64(flags + blockIdx.x, tag);
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot)
+        if (put_node[slot] >= 0) lay.put(o, put_node[slot], sums[slot]);
     if (pend_node < 0) return;
     // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
     // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
