@@ -30,6 +30,8 @@
 #include "zs_common.cuh"
 #include "zs_tma.cuh"
 
+#include <type_traits>
+
 namespace zs {
 namespace {
 
@@ -782,11 +784,23 @@ constexpr int kMinTmaSpan = imin(imin(tma_span<ChanLayout<1>>(), tma_span<ChanLa
                                  imin(imin(tma_span<QuadLayout>(), tma_span<ChanLayout<4>>()),
                                       tma_span<ChanLayout<5>>()));
 
-static int tma_warps_for(int lmax) {
+// Small graphs at lmax 3: windows of fewer than kShortWindow positions at
+// the full warp count take kQuadWarpsSmall warps per CTA instead (longer
+// windows, fewer cut nodes to combine; on the 1000-node graph, 69-edge
+// windows of 15 warps took 22.8 us, 104-edge windows of 10 warps 21.2 us;
+// 8 warps, 21.8 / 23.3 us at 12 / 8; the 4096-node graph keeps 15).  Both
+// spans, 15 x 16 and 10 x 16 positions per CTA, are at least kMinTmaSpan.
+constexpr int kShortWindow = 96;
+constexpr int kQuadWarpsSmall = 10;
+
+static int tma_warps_for(int lmax, int64_t E) {
     switch (lmax) {
         case 1: return tma_warps<ChanLayout<1>>();
         case 2: return tma_warps<ChanLayout<2>>();
-        case 3: return tma_warps<QuadLayout>();
+        case 3: {
+            constexpr int W = tma_warps<QuadLayout>();
+            return ceil_div(E, (int64_t)num_sms() * W) < kShortWindow ? kQuadWarpsSmall : W;
+        }
         case 4: return tma_warps<ChanLayout<4>>();
         default: return tma_warps<ChanLayout<5>>();
     }
@@ -821,7 +835,7 @@ static FwdPlan fwd_plan(const float* rad, const NodeOut& o, int64_t E, int C, in
     if (p.fast) {
         // Balanced single wave: one CTA of W warps per SM, every warp the same
         // number of CSR positions (at least one tile).
-        p.W = tma_warps_for(lmax);
+        p.W = tma_warps_for(lmax, E);
         const int64_t warps_max = (int64_t)num_sms() * p.W;
         p.KW = imax<int64_t>(ceil_div(E, warps_max), tma_tile_for(lmax));   // < 2^31: E < 2^31
         p.Wtot = imax<int64_t>(ceil_div(E, p.KW), 1);
@@ -846,17 +860,30 @@ static void launch_gen(const FwdPlan& p, const float* coup, int cld, const float
            kGenWin, (const float*)sc.part, o);
 }
 
-template <class P>
-static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
-                       const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
-                       cudaStream_t s) {
-    constexpr int W = tma_warps<P>();
+template <class P, int W>
+static void launch_tma_w(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
+                         const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
+                         cudaStream_t s) {
     auto kernel = fwd_tma<W, kTmaStages, P::kTileEdges, P>;
     const int smem = W * RingLayout<kTmaStages, P::kTileEdges, P::kRadFloats, P::kCoupRow>::kBytes;
     static std::atomic<uint64_t> attr_done[kMaxDevices];
     set_smem_limit_once(kernel, smem, attr_done);
     launch(kernel, (unsigned)p.ctas, W * 32, smem, s, coup, cld, rad, row_ptr, perm, (int)E, N, (int)p.KW,
            (int)p.Wtot, o, sc.part, sc.flags, next_salt());
+}
+
+template <class P>
+static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
+                       cudaStream_t s) {
+    if constexpr (std::is_same<P, QuadLayout>::value) {
+        static_assert(kQuadWarpsSmall * QuadLayout::kTileEdges >= kMinTmaSpan, "the workspace covers the small span");
+        if (p.W == kQuadWarpsSmall) {
+            launch_tma_w<P, kQuadWarpsSmall>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s);
+            return;
+        }
+    }
+    launch_tma_w<P, tma_warps<P>()>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s);
 }
 
 static void launch_forward(const FwdPlan& p, const float* coup, int cld, const float* rad, const int32_t* row_ptr,
