@@ -253,14 +253,19 @@ struct ChanLayout {
 #pragma unroll
         for (int r = 0; r < R; ++r) a.v[r] = 0.f;
     }
-    // At lmax 4 the coupling span is read as kSlot / 4 broadcast 16-byte
-    // loads; the row starts O floats into it (O = 0..3, the same for every
-    // lane), so the FMAs are unrolled once per O and picked by a warp-uniform
-    // switch.  Each accumulator still takes one FMA per edge in edge order.
-    // Measured on the n4096 graph: lmax 4 98 -> 88 us; lmax 2 unchanged and
-    // lmax 1 slower (3 rows do not pay for the switch); lmax 5 would spill
-    // (35 accumulators), so those keep one broadcast LDS.32 per row.
-    static constexpr bool kVecCoup = R >= 16 && R <= 24;
+    // At lmax 4 and 5 the coupling span is read as kSlot / 4 broadcast
+    // 16-byte loads; the row starts O floats into it (O = 0..3, the same for
+    // every lane), so the FMAs are unrolled once per O and picked by a
+    // warp-uniform switch.  Each accumulator still takes one FMA per edge in
+    // edge order.  Measured on the n4096 graph: lmax 4 98 -> 88 us, lmax 5
+    // (12 warps instead of 16) 128 -> 111 us: its shared-memory instruction
+    // queue had been the limit; lmax 2 unchanged and lmax 1 slower (3 rows do
+    // not pay for the switch), so those keep one broadcast LDS.32 per row.
+    static constexpr bool kVecCoup = R >= 16;
+    // lmax 5 holds 35 accumulators, the node's first piece and the 40-float
+    // coupling span: 163 registers, so 12 warps (at 16 the 128-register cap
+    // spills)
+    static constexpr int kMaxWarps = LM == 5 ? 12 : 16;
     template <int O>
     __device__ __forceinline__ static void fma_rows(const float (&cf)[kSlot], const float (&rv)[LM], Acc& a) {
 #pragma unroll
@@ -772,24 +777,37 @@ static Scratch scratch_at(void* base, int64_t windows, int C, int R) {
 
 // Warps per CTA of the single-wave forward for a lane layout: 16, or as many
 // rings as one SM's shared memory holds.
+template <class P, class = void>
+struct MaxWarpsOf { static constexpr int value = 16; };
+template <class P>
+struct MaxWarpsOf<P, std::void_t<decltype(P::kMaxWarps)>> { static constexpr int value = P::kMaxWarps; };
+template <class P>
+constexpr int layout_max_warps() { return MaxWarpsOf<P>::value; }
+
 template <class P>
 constexpr int tma_warps() {
     constexpr int bytes = RingLayout<kTmaStages, P::kTileEdges, P::kRadFloats, P::kCoupRow>::kBytes;
-    return (232448 / bytes) < kTmaWarps ? (232448 / bytes) : kTmaWarps;
+    constexpr int cap = imin(kTmaWarps, layout_max_warps<P>());
+    return (232448 / bytes) < cap ? (232448 / bytes) : cap;
 }
 
+// A CTA of the single-wave path covers at least kMinTmaSpan CSR positions
+// (so the workspace, sized per kMinTmaSpan positions, holds every CTA's
+// partials): each warp's window is at least tma_min_window positions.
+constexpr int kMinTmaSpan = 128;
 template <class P>
-constexpr int tma_span() { return tma_warps<P>() * P::kTileEdges; }
-constexpr int kMinTmaSpan = imin(imin(tma_span<ChanLayout<1>>(), tma_span<ChanLayout<2>>()),
-                                 imin(imin(tma_span<QuadLayout>(), tma_span<ChanLayout<4>>()),
-                                      tma_span<ChanLayout<5>>()));
+constexpr int tma_min_window(int W) {
+    return (kMinTmaSpan + W - 1) / W > P::kTileEdges
+               ? ((kMinTmaSpan + W - 1) / W + P::kTileEdges - 1) / P::kTileEdges * P::kTileEdges
+               : P::kTileEdges;
+}
 
 // Small graphs at lmax 3: windows of fewer than kShortWindow positions at
 // the full warp count take kQuadWarpsSmall warps per CTA instead (longer
 // windows, fewer cut nodes to combine; on the 1000-node graph, 69-edge
 // windows of 15 warps took 22.8 us, 104-edge windows of 10 warps 21.2 us;
 // 8 warps, 21.8 / 23.3 us at 12 / 8; the 4096-node graph keeps 15).  Both
-// spans, 15 x 16 and 10 x 16 positions per CTA, are at least kMinTmaSpan.
+// take windows of at least tma_min_window positions.
 constexpr int kShortWindow = 96;
 constexpr int kQuadWarpsSmall = 10;
 
@@ -806,13 +824,13 @@ static int tma_warps_for(int lmax, int64_t E) {
     }
 }
 
-static int tma_tile_for(int lmax) {
+static int tma_min_window_for(int lmax, int W) {
     switch (lmax) {
-        case 1: return ChanLayout<1>::kTileEdges;
-        case 2: return ChanLayout<2>::kTileEdges;
-        case 3: return QuadLayout::kTileEdges;
-        case 4: return ChanLayout<4>::kTileEdges;
-        default: return ChanLayout<5>::kTileEdges;
+        case 1: return tma_min_window<ChanLayout<1>>(W);
+        case 2: return tma_min_window<ChanLayout<2>>(W);
+        case 3: return tma_min_window<QuadLayout>(W);
+        case 4: return tma_min_window<ChanLayout<4>>(W);
+        default: return tma_min_window<ChanLayout<5>>(W);
     }
 }
 
@@ -837,7 +855,8 @@ static FwdPlan fwd_plan(const float* rad, const NodeOut& o, int64_t E, int C, in
         // number of CSR positions (at least one tile).
         p.W = tma_warps_for(lmax, E);
         const int64_t warps_max = (int64_t)num_sms() * p.W;
-        p.KW = imax<int64_t>(ceil_div(E, warps_max), tma_tile_for(lmax));   // < 2^31: E < 2^31
+        // CTAs cover at least kMinTmaSpan positions: ceil(E / kMinTmaSpan) of them at most
+        p.KW = imax<int64_t>(ceil_div(E, warps_max), tma_min_window_for(lmax, p.W));   // < 2^31: E < 2^31
         p.Wtot = imax<int64_t>(ceil_div(E, p.KW), 1);
         p.ctas = ceil_div(p.Wtot, p.W);
         p.windows = p.ctas;
@@ -877,7 +896,6 @@ static void launch_tma(const FwdPlan& p, const float* coup, int cld, const float
                        const int32_t* perm, int64_t E, int32_t N, const NodeOut& o, const Scratch& sc,
                        cudaStream_t s) {
     if constexpr (std::is_same<P, QuadLayout>::value) {
-        static_assert(kQuadWarpsSmall * QuadLayout::kTileEdges >= kMinTmaSpan, "the workspace covers the small span");
         if (p.W == kQuadWarpsSmall) {
             launch_tma_w<P, kQuadWarpsSmall>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s);
             return;
