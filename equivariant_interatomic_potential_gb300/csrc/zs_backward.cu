@@ -15,7 +15,8 @@
 
 // L2 policy of the CSR-order backward's coupling spans: normal, since a span
 // shares its sectors with the neighbouring edges' rows, which the CSR-order
-// walk reaches later (the ring's radial rows and perm are evict-first).
+// walk reaches later (the ring's radial rows and perm are evict-first below
+// lmax 4).
 #ifndef ZS_BWDC_COUP_POL
 #define ZS_BWDC_COUP_POL kL2Normal
 #endif
@@ -182,7 +183,10 @@ bwd_csr_quad(const float* __restrict__ g, const float* __restrict__ coup, const 
     // a node's R cotangent rows: in registers up to 24 rows, else in this
     // lane's own column of shared memory ([row][lane] float4, no sharing)
     constexpr bool kSmemG = R > 24;
-    using Ring = TileRing<S, T, kL2EvictFirst, RF, R, ZS_BWDC_COUP_POL>;
+    // radial rows and perm: evict-first, but evict-normal from lmax 4 on
+    // (measured on the n4096 graph: lmax 4 147 -> 144 us, lmax 5 233 -> 227
+    // us; lmax 2 and 3 were slower with it)
+    using Ring = TileRing<S, T, (LM >= 4 ? kL2Normal : kL2EvictFirst), RF, R, ZS_BWDC_COUP_POL>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const QuadLane Q(threadIdx.x & 31);
