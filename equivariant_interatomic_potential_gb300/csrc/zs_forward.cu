@@ -335,6 +335,10 @@ struct ChanLayout {
     }
 };
 
+// A node whose partials come from at least this many earlier CTAs is
+// combined by all warps of the CTA where it ends.
+constexpr int kSplitPartials = 8;
+
 // Single-wave forward at C = 32, fed by TMA rings.  W warps per CTA, one CTA
 // per SM; warp gw owns the window [gw*KW, gw*KW + KW) of CSR positions and
 // walks it in position order, closing a node when its last position is
@@ -488,7 +492,11 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     int pend_ma = 0;                         // its first position
     Acc pend;
     __shared__ int s_stored;                 // this CTA left a partial for a later CTA
-    if (threadIdx.x == 0) s_stored = 0;
+    __shared__ int s_pend_b0, s_pend_np;     // the pend node's first CTA, and how many CTAs before this one it spans
+    if (threadIdx.x == 0) {
+        s_stored = 0;
+        s_pend_np = 0;
+    }
     __syncthreads();
     // The sums of this warp's slots; the partial a later CTA needs is stored
     // and published first, the finished nodes are written after the flag.
@@ -514,6 +522,10 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
             pend_node = m;
             pend_ma = ma;
             pend = sum;
+            if (lane == 0) {
+                s_pend_b0 = (int)(ma / span);
+                s_pend_np = (int)blockIdx.x - (int)(ma / span);
+            }
         } else {
             // slot 1: starts here and runs past this CTA; slot 0: covers all of it
             lay.store(cta_part + ((int64_t)blockIdx.x * 2 + (ma < P0 ? 0 : 1)) * P::kPartFloats, sum);
@@ -534,6 +546,47 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
 #pragma unroll
     for (int slot = 0; slot < 2; ++slot)
         if (put_node[slot] >= 0) lay.put(o, put_node[slot], sums[slot]);
+    const int bx = (int)blockIdx.x;
+    const int np = s_pend_np;                // the same in every warp (written before the barrier above)
+    if (np >= kSplitPartials) {
+        // A node cut by many CTAs (a hub of a skewed graph): its earlier
+        // CTAs' partials are split over this CTA's warps, warp w adding those
+        // of CTAs b0 + w, b0 + w + W, ... in CTA order, and the warps' sums
+        // are added in warp order.  A fixed order whoever finishes first.
+        const int pb0 = s_pend_b0;
+        for (int k = pb0 + warp + W * lane; k < bx; k += W * 32) {
+            wait_flag(flags, k, tag);
+            flags[k] = 0;
+        }
+        __syncwarp();
+        constexpr int kB = sizeof(Acc) <= 64 ? 4 : 1;
+        Acc sw;
+        P::zero(sw);
+        for (int k0 = pb0 + warp; k0 < bx; k0 += W * kB) {
+            Acc t[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int k = k0 + u * W;
+                if (k < bx) lay.load_cg(cta_part + ((int64_t)k * 2 + (k == pb0 ? 1 : 0)) * P::kPartFloats, t[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+                if (k0 + u * W < bx) P::add_to(sw, t[u]);
+        }
+        lay.store(reinterpret_cast<float*>(smem + (size_t)warp * Layout::kBytes), sw);
+        __syncthreads();
+        if (pend_node < 0) return;
+        Acc total;
+        lay.load(reinterpret_cast<const float*>(smem), total);
+        for (int w = 1; w < imin(W, np); ++w) {
+            Acc t;
+            lay.load(reinterpret_cast<const float*>(smem + (size_t)w * Layout::kBytes), t);
+            P::add_to(total, t);
+        }
+        P::add_to(total, pend);
+        lay.put(o, pend_node, total);
+        return;
+    }
     if (pend_node < 0) return;
     // node pend_node began in CTA b0 (its slot-1 partial), covered CTAs
     // b0+1 .. blockIdx.x-1 (slot-0 partials) and ends here: add in CTA order
@@ -542,7 +595,6 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
     // access costs several hundred nanoseconds, and on a skewed graph a node
     // spans tens of CTAs)
     const int b0 = (int)(pend_ma / span);
-    const int bx = (int)blockIdx.x;
     for (int k = b0 + lane; k < bx; k += 32) {
         wait_flag(flags, k, tag);
         flags[k] = 0;
