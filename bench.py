@@ -338,14 +338,14 @@ def run_gpu_arm(args, rank: int, world: int) -> dict | None:
                                 P(b.ws_fwd), fwd_ws_bytes, sp)
             assert st == 0, lib.zs_last_error()
 
-    # zs_build_csr: three launches on its one-pass counting path (N + 1 <= 5120),
+    # zs_build_csr: three launches on its one-pass counting path (N + 1 <= 5120; one for E <= 8192),
     # else three per 8-bit radix pass plus the row_ptr pass (one launch for E = 0);
     # zs_forward: one kernel at C = 32 (aligned tensors), else main kernel and
     # fix-up; the backward: one kernel (none for E = 0)
     if E == 0:
         csr_launches = 1
     elif N + 1 <= 5120:
-        csr_launches = 3
+        csr_launches = 1 if E <= 8192 else 3   # one CTA, one launch for up to 8192 edges
     else:
         csr_launches = 3 * max(1, (max(N, 1).bit_length() + 7) // 8) + 1
     launches_per_step = csr_launches + (1 if C == 32 else 2) + (1 if E > 0 else 0)

@@ -550,6 +550,120 @@ csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ 
     }
 }
 
+// Small graphs (E <= kCntMaxRounds * kCntThreads edges): the whole counting
+// path in one CTA and one launch -- csr_count_rank's ranking and counts, then
+// csr_count_scatter's node bases and scatter, the counts staying in shared
+// memory (with one tile, every edge's offset within its key is its rank).
+constexpr int kSingleMaxEdges = kCntMaxRounds * kCntThreads;
+inline int count_single_smem(int nkeys, int rounds) {
+    return count_rank_smem(nkeys, rounds) + 2 * count_pairs(nkeys) * 4;
+}
+
+__global__ void __launch_bounds__(kCntThreads, 1)
+csr_count_single(const int32_t* __restrict__ dst, int64_t E, int32_t N, int rounds,
+                 int32_t* __restrict__ perm, int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
+    extern __shared__ uint32_t cnt_words[];
+    __shared__ int32_t wsum[kCntWarps];
+    const int nkeys = N + 1;
+    const int npairs = count_pairs(nkeys);
+    uint16_t* cnt = reinterpret_cast<uint16_t*>(cnt_words);
+    uint32_t* packed = cnt_words + kCntWarps * npairs;                          // [TS]: key << 16 | rank
+    int32_t* ktot = reinterpret_cast<int32_t*>(packed + rounds * kCntThreads);   // [2 * npairs]: key totals, then bases
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int TW = rounds * 32;
+    const int n = (int)E;
+    pdl_wait();
+    pdl_trigger();
+    copy_ints(reinterpret_cast<int32_t*>(packed), dst, n, tid, kCntThreads);
+    for (int i = tid; i < kCntWarps * npairs / 4; i += kCntThreads) reinterpret_cast<uint4*>(cnt_words)[i] = make_uint4(0u, 0u, 0u, 0u);
+    cp_async_wait_all();
+    __syncthreads();
+    // ranks within each warp's run of edges, by claim and verify (see csr_count_rank)
+    const unsigned lt = lanemask_lt();
+    uint16_t* wcnt = cnt + 2 * warp * npairs;
+    for (int r = 0; r < rounds; ++r) {
+        const int i = warp * TW + r * 32 + lane;
+        const bool valid = i < n;
+        const int key = valid ? clamp_key((int32_t)packed[i], N) : 0;
+        const uint32_t before = valid ? wcnt[key] : 0u;
+        __syncwarp();
+        if (valid) wcnt[key] = (uint16_t)(before | ((uint32_t)lane << 10));
+        __syncwarp();
+        const int owner = valid ? (int)(wcnt[key] >> 10) : lane;
+        unsigned lost = __ballot_sync(0xffffffffu, valid && owner != lane);
+        unsigned peers = 1u << lane;
+        while (lost) {
+            const int w = __shfl_sync(0xffffffffu, owner, __ffs(lost) - 1);
+            const unsigned group = __ballot_sync(0xffffffffu, valid && owner == w);
+            if (group & (1u << lane)) peers = group;
+            lost &= ~group;
+        }
+        __syncwarp();
+        if (valid) {
+            if (lane == __ffs(peers) - 1) wcnt[key] = (uint16_t)(before + __popc(peers));
+            packed[i] = ((uint32_t)key << 16) | (before + __popc(peers & lt));
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // per pair of keys: exclusive prefix over the warps, and the key totals
+    for (int q = tid; q < npairs; q += kCntThreads) {
+        uint32_t c[kCntWarps];
+#pragma unroll
+        for (int w = 0; w < kCntWarps; ++w) c[w] = cnt_words[w * npairs + q];
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kCntWarps; ++w) {
+            cnt_words[w * npairs + q] = run;
+            run += c[w];
+        }
+        ktot[2 * q] = (int32_t)(run & 0xffffu);
+        ktot[2 * q + 1] = (int32_t)(run >> 16);
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kCntThreads) {
+        const uint32_t p = packed[i];
+        const int w = i / TW;
+        packed[i] = (p & 0xffff0000u) | ((p & 0xffffu) + cnt[2 * w * npairs + (p >> 16)]);
+    }
+    // node bases: exclusive scan of the totals (thread tid takes keys [k0, k0 + per))
+    const int per = (nkeys + kCntThreads - 1) / kCntThreads;
+    const int k0 = tid * per;
+    int32_t v[kCntMaxPer];
+    int32_t own = 0;
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        v[j] = (j < per && k0 + j < nkeys) ? ktot[k0 + j] : 0;
+        own += v[j];
+    }
+    int32_t incl = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t run = incl - own;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        const int k = k0 + j;
+        if (j < per && k < nkeys) {
+            row_ptr[k] = run;
+            if (k == N && bad) *bad = v[j];
+            ktot[k] = run;
+            run += v[j];
+        }
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < n; i += kCntThreads) {
+        const uint32_t p = packed[i];
+        perm[ktot[p >> 16] + (int32_t)(p & 0xffffu)] = i;
+    }
+}
+
 struct CsrPlan {
     bool counting = false;
     int T = 0;
@@ -618,6 +732,14 @@ extern "C" zs_status zs_build_csr(const int32_t* dst, int64_t E, int32_t N,
         int32_t* M = reinterpret_cast<int32_t*>(ws + p.off_hist);
         int32_t* tot = reinterpret_cast<int32_t*>(ws + p.off_tot);
         uint16_t* rank = reinterpret_cast<uint16_t*>(ws + p.off_rank);
+        if (E <= kSingleMaxEdges) {
+            static std::atomic<uint64_t> single_smem_set[kMaxDevices];
+            set_smem_limit_once(csr_count_single, count_single_smem(kCntMaxKeys, kCntMaxRounds), single_smem_set);
+            const int rounds = (int)((E + kCntThreads - 1) / kCntThreads);
+            launch(csr_count_single, 1, kCntThreads, count_single_smem(N + 1, rounds), s, dst, E, N, rounds, perm,
+                   row_ptr, bad_dst_count);
+            return check_launch("zs_build_csr");
+        }
         const int smem = count_rank_smem(kCntMaxKeys, kCntMaxRounds);
         set_smem_limit_once(csr_count_rank, smem, rank_smem_set);
         const int S = 2 * count_pairs(N + 1);
