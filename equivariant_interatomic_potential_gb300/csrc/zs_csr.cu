@@ -7,8 +7,9 @@
 // sequential counting sort; keys outside [0, N) count as key N, after all
 // valid ones.
 //
-// Counting path (N + 1 <= kCntMaxKeys, every bench-sized graph): one pass,
-// three launches with no inter-CTA waiting:
+// Counting path (N + 1 <= kCntMaxKeys, every bench-sized graph but the
+// largest): one pass, three launches with no inter-CTA waiting (one launch of
+// one CTA, count_single, for up to kSingleMaxEdges edges):
 //   count_rank    -- per tile of edges, each edge's stable rank among the
 //                    tile's edges of the same node (warp match + per-warp
 //                    running counts in shared memory, then a prefix over
