@@ -82,6 +82,17 @@ def test_edge_count_boundaries(E):
     check_backward(w, res)
 
 
+@pytest.mark.parametrize("E", [152 * 15 * 96, 152 * 15 * 96 + 1])
+def test_forward_warp_count_switch(E):
+    # on a 152-SM GB300 the lmax-3 forward runs 10 warps per CTA up to 218880
+    # edges (15-warp windows under 96 positions) and 15 from the next edge on
+    w = workloads.make_random(1000, E, 32, seed=E)
+    res = run_gpu(w)
+    row_ptr, perm = check_csr(w, res)
+    check_forward(w, res, row_ptr, perm)
+    check_backward(w, res)
+
+
 @pytest.mark.parametrize("N,E,hot", [(1, 5000, None), (50, 20000, 7), (3000, 100000, 11), (2, 70000, 0)])
 def test_heavy_nodes(N, E, hot):
     # one node takes most edges: its CSR run crosses many warp and CTA windows
