@@ -328,6 +328,104 @@ __device__ __forceinline__ void copy_ints(int32_t* dst, const int32_t* src, int 
 
 __device__ __forceinline__ int32_t clamp_key(int32_t k, int32_t N) { return (uint32_t)k < (uint32_t)N ? k : N; }
 
+// Ranks within each warp's run of a tile (warp w owns edges [w * 32 * rounds,
+// (w + 1) * 32 * rounds) of the tile): packed[i] holds edge i's key on entry
+// and key << 16 | (its rank among the warp's earlier edges of that key) on
+// exit; wcnt (the warp's 16-bit counters, zeroed) ends with the warp's count
+// of every key.  Per round of 32 edges, the lanes holding each key (peers)
+// are found by claim and verify: every lane writes its lane id into bits
+// 10..14 of its key's counter (count < 1024 stays in bits 0..9), reads the
+// slot back, and lanes that lost the claim are grouped with the winner by
+// one ballot per contested key.  Uncontested rounds cost no ballot loop.
+__device__ __forceinline__ void rank_in_warp(uint32_t* packed, uint16_t* wcnt, int rounds, int n, int32_t N, int warp,
+                                             int lane) {
+    const unsigned lt = lanemask_lt();
+    const int TW = rounds * 32;
+    for (int r = 0; r < rounds; ++r) {
+        const int i = warp * TW + r * 32 + lane;
+        const bool valid = i < n;
+        const int key = valid ? clamp_key((int32_t)packed[i], N) : 0;
+        const uint32_t before = valid ? wcnt[key] : 0u;          // count so far, owner bits clear
+        __syncwarp();
+        if (valid) wcnt[key] = (uint16_t)(before | ((uint32_t)lane << 10));
+        __syncwarp();
+        const int owner = valid ? (int)(wcnt[key] >> 10) : lane;
+        unsigned lost = __ballot_sync(0xffffffffu, valid && owner != lane);
+        unsigned peers = 1u << lane;
+        while (lost) {
+            const int w = __shfl_sync(0xffffffffu, owner, __ffs(lost) - 1);
+            const unsigned group = __ballot_sync(0xffffffffu, valid && owner == w);
+            if (group & (1u << lane)) peers = group;
+            lost &= ~group;
+        }
+        __syncwarp();
+        if (valid) {
+            if (lane == __ffs(peers) - 1) wcnt[key] = (uint16_t)(before + __popc(peers));
+            packed[i] = ((uint32_t)key << 16) | (before + __popc(peers & lt));
+        }
+        __syncwarp();
+    }
+}
+
+// Pair q of keys: the warps' counters turned into exclusive prefixes over the
+// warps (both 16-bit halves at once: every partial sum is below 2^16); the
+// tile's two counts are returned in the halves of the result.
+__device__ __forceinline__ uint32_t prefix_over_warps(uint32_t* cnt_words, int npairs, int q) {
+    uint32_t c[kCntWarps];
+#pragma unroll
+    for (int w = 0; w < kCntWarps; ++w) c[w] = cnt_words[w * npairs + q];
+    uint32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < kCntWarps; ++w) {
+        cnt_words[w * npairs + q] = run;
+        run += c[w];
+    }
+    return run;
+}
+
+// Node bases: an exclusive scan of the nkeys totals in tot (shared memory),
+// thread tid taking keys [tid * per, (tid + 1) * per).  base[k] = first CSR
+// position of key k plus off[k] (off may alias base; NULL: 0); with row_ptr,
+// the positions go to row_ptr too and the total of key N (invalid keys) to
+// *bad.  Every thread of the CTA must call it (it synchronises the CTA).
+__device__ __forceinline__ void key_bases(const int32_t* tot, const int32_t* off, int32_t* base, int nkeys, int32_t N,
+                                          int32_t* wsum, int32_t* __restrict__ row_ptr, int32_t* __restrict__ bad) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = (nkeys + kCntThreads - 1) / kCntThreads;
+    const int k0 = tid * per;
+    int32_t v[kCntMaxPer], o[kCntMaxPer];
+    int32_t own = 0;
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        const bool in = j < per && k0 + j < nkeys;
+        v[j] = in ? tot[k0 + j] : 0;
+        o[j] = (in && off) ? off[k0 + j] : 0;
+        own += v[j];
+    }
+    int32_t incl = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t run = incl - own;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+    for (int j = 0; j < kCntMaxPer; ++j) {
+        const int k = k0 + j;
+        if (j < per && k < nkeys) {
+            if (row_ptr) {
+                row_ptr[k] = run;
+                if (k == N && bad) *bad = v[j];
+            }
+            base[k] = run + o[j];
+            run += v[j];
+        }
+    }
+}
+
 // Per tile: each edge's stable rank among the tile's edges of the same key
 // (to rank[]), and the tile's count of every key (to row `tile` of M, whose
 // rows hold 2 * count_pairs(N + 1) counts).
@@ -353,50 +451,11 @@ csr_count_rank(const int32_t* __restrict__ dst, int64_t E, int32_t N, int rounds
     cp_async_wait_all();
     __syncthreads();
 
-    const unsigned lt = lanemask_lt();
-    uint16_t* wcnt = cnt + 2 * warp * npairs;
-    // Per round of 32 edges: the lanes holding each key (peers), found by
-    // claim and verify -- every lane writes its lane id into bits 10..14 of
-    // its key's counter (count < 1024 stays in bits 0..9), reads the slot
-    // back, and lanes that lost the claim are grouped with the winner by one
-    // ballot per contested key.  Uncontested rounds cost no ballot loop.
-    for (int r = 0; r < rounds; ++r) {
-        const int i = warp * TW + r * 32 + lane;
-        const bool valid = i < n_in_tile;
-        const int key = valid ? clamp_key((int32_t)packed[i], N) : 0;
-        const uint32_t before = valid ? wcnt[key] : 0u;          // count so far, owner bits clear
-        __syncwarp();
-        if (valid) wcnt[key] = (uint16_t)(before | ((uint32_t)lane << 10));
-        __syncwarp();
-        const int owner = valid ? (int)(wcnt[key] >> 10) : lane;
-        unsigned lost = __ballot_sync(0xffffffffu, valid && owner != lane);
-        unsigned peers = 1u << lane;
-        while (lost) {
-            const int w = __shfl_sync(0xffffffffu, owner, __ffs(lost) - 1);
-            const unsigned group = __ballot_sync(0xffffffffu, valid && owner == w);
-            if (group & (1u << lane)) peers = group;
-            lost &= ~group;
-        }
-        __syncwarp();
-        if (valid) {
-            if (lane == __ffs(peers) - 1) wcnt[key] = (uint16_t)(before + __popc(peers));
-            packed[i] = ((uint32_t)key << 16) | (before + __popc(peers & lt));
-        }
-        __syncwarp();
-    }
+    rank_in_warp(packed, cnt + 2 * warp * npairs, rounds, n_in_tile, N, warp, lane);
     __syncthreads();
-    // per pair of keys: exclusive prefix of the counters over the warps (both
-    // halves at once: every partial sum is below 2^16), tile counts to M
+    // per pair of keys: prefixes over the warps, tile counts to M
     for (int q = tid; q < npairs; q += kCntThreads) {
-        uint32_t c[kCntWarps];
-#pragma unroll
-        for (int w = 0; w < kCntWarps; ++w) c[w] = cnt_words[w * npairs + q];
-        uint32_t run = 0;
-#pragma unroll
-        for (int w = 0; w < kCntWarps; ++w) {
-            cnt_words[w * npairs + q] = run;
-            run += c[w];
-        }
+        const uint32_t run = prefix_over_warps(cnt_words, npairs, q);
         reinterpret_cast<int2*>(M + (int64_t)blockIdx.x * 2 * npairs)[q] = make_int2((int)(run & 0xffffu), (int)(run >> 16));
     }
     __syncthreads();
@@ -491,7 +550,7 @@ csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ 
     int32_t* wsum = kbase + align4(S);
     int32_t* skey = wsum + kCntWarps;
     uint32_t* srank = reinterpret_cast<uint32_t*>(skey + rounds * kCntThreads);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int64_t tbase = (int64_t)blockIdx.x * rounds * kCntThreads;
     const int n_in_tile = (int)imin<int64_t>((int64_t)rounds * kCntThreads, E - tbase);
     pdl_wait();
@@ -511,38 +570,7 @@ csr_count_scatter(const int32_t* __restrict__ dst, const uint16_t* __restrict__ 
     if ((n_in_tile & 1) && tid == 0) srank[n_in_tile / 2] = __ldg(rank + tbase + n_in_tile - 1);
     cp_async_wait_all();
     __syncthreads();
-    // thread tid scans keys [k0, k0 + per)
-    const int per = (nkeys + kCntThreads - 1) / kCntThreads;
-    const int k0 = tid * per;
-    int32_t v[kCntMaxPer];
-    int32_t own = 0;
-#pragma unroll
-    for (int j = 0; j < kCntMaxPer; ++j) {
-        v[j] = (j < per && k0 + j < nkeys) ? ktot[k0 + j] : 0;
-        own += v[j];
-    }
-    int32_t incl = own;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int32_t run = incl - own;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
-#pragma unroll
-    for (int j = 0; j < kCntMaxPer; ++j) {
-        const int k = k0 + j;
-        if (j < per && k < nkeys) {
-            if (blockIdx.x == 0) {
-                row_ptr[k] = run;
-                if (k == N && bad) *bad = v[j];
-            }
-            kbase[k] += run;
-            run += v[j];
-        }
-    }
+    key_bases(ktot, kbase, kbase, nkeys, N, wsum, blockIdx.x == 0 ? row_ptr : nullptr, bad);
     __syncthreads();
 #pragma unroll 4
     for (int i = tid; i < n_in_tile; i += kCntThreads) {
@@ -579,45 +607,11 @@ csr_count_single(const int32_t* __restrict__ dst, int64_t E, int32_t N, int roun
     for (int i = tid; i < kCntWarps * npairs / 4; i += kCntThreads) reinterpret_cast<uint4*>(cnt_words)[i] = make_uint4(0u, 0u, 0u, 0u);
     cp_async_wait_all();
     __syncthreads();
-    // ranks within each warp's run of edges, by claim and verify (see csr_count_rank)
-    const unsigned lt = lanemask_lt();
-    uint16_t* wcnt = cnt + 2 * warp * npairs;
-    for (int r = 0; r < rounds; ++r) {
-        const int i = warp * TW + r * 32 + lane;
-        const bool valid = i < n;
-        const int key = valid ? clamp_key((int32_t)packed[i], N) : 0;
-        const uint32_t before = valid ? wcnt[key] : 0u;
-        __syncwarp();
-        if (valid) wcnt[key] = (uint16_t)(before | ((uint32_t)lane << 10));
-        __syncwarp();
-        const int owner = valid ? (int)(wcnt[key] >> 10) : lane;
-        unsigned lost = __ballot_sync(0xffffffffu, valid && owner != lane);
-        unsigned peers = 1u << lane;
-        while (lost) {
-            const int w = __shfl_sync(0xffffffffu, owner, __ffs(lost) - 1);
-            const unsigned group = __ballot_sync(0xffffffffu, valid && owner == w);
-            if (group & (1u << lane)) peers = group;
-            lost &= ~group;
-        }
-        __syncwarp();
-        if (valid) {
-            if (lane == __ffs(peers) - 1) wcnt[key] = (uint16_t)(before + __popc(peers));
-            packed[i] = ((uint32_t)key << 16) | (before + __popc(peers & lt));
-        }
-        __syncwarp();
-    }
+    rank_in_warp(packed, cnt + 2 * warp * npairs, rounds, n, N, warp, lane);
     __syncthreads();
     // per pair of keys: exclusive prefix over the warps, and the key totals
     for (int q = tid; q < npairs; q += kCntThreads) {
-        uint32_t c[kCntWarps];
-#pragma unroll
-        for (int w = 0; w < kCntWarps; ++w) c[w] = cnt_words[w * npairs + q];
-        uint32_t run = 0;
-#pragma unroll
-        for (int w = 0; w < kCntWarps; ++w) {
-            cnt_words[w * npairs + q] = run;
-            run += c[w];
-        }
+        const uint32_t run = prefix_over_warps(cnt_words, npairs, q);
         ktot[2 * q] = (int32_t)(run & 0xffffu);
         ktot[2 * q + 1] = (int32_t)(run >> 16);
     }
@@ -627,36 +621,8 @@ csr_count_single(const int32_t* __restrict__ dst, int64_t E, int32_t N, int roun
         const int w = i / TW;
         packed[i] = (p & 0xffff0000u) | ((p & 0xffffu) + cnt[2 * w * npairs + (p >> 16)]);
     }
-    // node bases: exclusive scan of the totals (thread tid takes keys [k0, k0 + per))
-    const int per = (nkeys + kCntThreads - 1) / kCntThreads;
-    const int k0 = tid * per;
-    int32_t v[kCntMaxPer];
-    int32_t own = 0;
-#pragma unroll
-    for (int j = 0; j < kCntMaxPer; ++j) {
-        v[j] = (j < per && k0 + j < nkeys) ? ktot[k0 + j] : 0;
-        own += v[j];
-    }
-    int32_t incl = own;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int32_t run = incl - own;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
-#pragma unroll
-    for (int j = 0; j < kCntMaxPer; ++j) {
-        const int k = k0 + j;
-        if (j < per && k < nkeys) {
-            row_ptr[k] = run;
-            if (k == N && bad) *bad = v[j];
-            ktot[k] = run;
-            run += v[j];
-        }
-    }
+    // node bases (one tile: an edge's offset within its key is its rank)
+    key_bases(ktot, nullptr, ktot, nkeys, N, wsum, row_ptr, bad);
     __syncthreads();
 #pragma unroll 4
     for (int i = tid; i < n; i += kCntThreads) {
