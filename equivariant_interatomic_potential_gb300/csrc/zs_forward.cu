@@ -223,9 +223,10 @@ struct QuadLayout {
 // written as 128-byte lines.
 template <int LM>
 struct ChanLayout {
-    // small rows: more edges per tile keep more bytes in flight (measured
-    // better for lmax 1, 2, 4; lmax 5 keeps 8 and its 16 warps)
-    static constexpr int kTileEdges = LM <= 4 ? 16 : 8;
+    // tiles of 16 edges for the small rows of lmax 1 and 2 (8 and 32 were
+    // slower); 8 for lmax 4 and 5, whose rings then fit more warps (lmax 4:
+    // 16 warps of 8-edge tiles 77 us against 11 of 16-edge tiles 84 us)
+    static constexpr int kTileEdges = LM <= 3 ? 16 : 8;
     static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
     static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
     static constexpr int kSlot = coup_slot_floats(kCoupRow);
