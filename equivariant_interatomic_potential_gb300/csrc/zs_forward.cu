@@ -855,12 +855,12 @@ constexpr int tma_min_window(int W) {
                : P::kTileEdges;
 }
 
-// Small graphs at lmax 3: windows of fewer than kShortWindow positions at
-// the full warp count take kQuadWarpsSmall warps per CTA instead (longer
-// windows, fewer cut nodes to combine; on the 1000-node graph, 69-edge
-// windows of 15 warps took 22.8 us, 104-edge windows of 10 warps 21.2 us;
-// 8 warps, 21.8 / 23.3 us at 12 / 8; the 4096-node graph keeps 15).  Both
-// take windows of at least tma_min_window positions.
+// Small graphs at lmax 3: when the full warp count would leave windows of
+// fewer than kShortWindow positions, kQuadWarpsSmall warps per CTA take
+// longer windows with fewer cut nodes to combine (on the 1000-node graph,
+// 69-edge windows of 15 warps took 22.8 us, 104-edge windows of 10 warps
+// 21.2 us, 12 and 8 warps 21.8 and 23.3 us; the 4096-node graph keeps 15).
+// Either way a window has at least tma_min_window positions.
 constexpr int kShortWindow = 96;
 constexpr int kQuadWarpsSmall = 10;
 
