@@ -336,6 +336,121 @@ struct ChanLayout {
     }
 };
 
+// EdgeQuadLayout (small ladders): group g = lane/8 takes edge j + g of each
+// step of four edges, quad q = lane%8 channels 4q..4q+3 of all R rows.  Per
+// four edges a lane issues lmax LDS.128 of its edge's radial row, R LDS.32 of
+// its coupling row and 4R FFMA, against 4 x (lmax + R) loads and 4R FFMA
+// with lane = channel.  Each group sums every fourth edge of a node; the four
+// sums are added across the groups (XOR 8, then XOR 16: the same bits in
+// every lane) when the node is written or its partial stored.  A loaded
+// partial sits in group 0 with zeros in the other groups, so that it takes
+// the same reduction exactly.
+template <int LM>
+struct EdgeQuadLayout {
+    static constexpr int kStep = 4;
+    static constexpr int kTileEdges = 16;
+    static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
+    static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
+    static constexpr int kSlot = coup_slot_floats(kCoupRow);
+    struct Acc {
+        float4 v[R];
+    };
+    struct View {
+        const float* ra;    // radial rows of the stage, at this lane's channel quad
+        const float* cp;    // coupling spans of the stage
+        const int2* mt;
+    };
+    int lane, g, q;
+    const float *rb, *cb;
+    __device__ __forceinline__ explicit EdgeQuadLayout(int l) : lane(l), g(l >> 3), q(l & 7) {}
+    template <class Ring>
+    __device__ __forceinline__ void bind(const Ring& ring) {
+        rb = ring.rad + 4 * q;
+        cb = ring.coup;
+    }
+    template <int T>
+    __device__ __forceinline__ View view(int st, const int2* meta) const {
+        return View{rb + st * T * kRadFloats, cb + st * T * kSlot, meta + st * T};
+    }
+    __device__ __forceinline__ static void zero(Acc& a) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // Edges j .. j + 3 of the tile; group g adds edge j + g if it is before stop.
+    __device__ __forceinline__ void add_step(const View& v, int j, int stop, Acc& a) const {
+        const int e = j + g;
+        if (e < stop) {
+            float4 rv[LM];
+#pragma unroll
+            for (int l = 0; l < LM; ++l) rv[l] = *reinterpret_cast<const float4*>(v.ra + e * kRadFloats + l * kC32);
+            const float* cr = v.cp + e * kSlot + v.mt[e].y;
+#pragma unroll
+            for (int r = 0; r < R; ++r) a.v[r] = f4_fma(cr[r], rv[ladder_slot(r)], a.v[r]);
+        }
+    }
+    __device__ __forceinline__ static Acc reduce(const Acc& a) {
+        Acc s;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float4 x = f4_add(a.v[r], f4_shfl_xor(a.v[r], 8));
+            s.v[r] = f4_add(x, f4_shfl_xor(x, 16));
+        }
+        return s;
+    }
+    __device__ __forceinline__ void put(const NodeOut& o, int n, const Acc& a) const {
+        const Acc s = reduce(a);
+        const int64_t at = (int64_t)n * kNodeFloats + 4 * q;
+        const float sc = o.scale ? __ldg(o.scale + n) : 1.f;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if ((r & 3) == g) {
+                const float4 x = s.v[r];
+                *reinterpret_cast<float4*>(o.out + at + (1 + r) * kC32) =
+                    o.scale ? make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc) : x;
+                if (o.raw) *reinterpret_cast<float4*>(o.raw + at + (1 + r) * kC32) = x;
+            }
+        if (g == 3) {   // the zero scalar row
+            *reinterpret_cast<float4*>(o.out + at) = z;
+            if (o.raw) *reinterpret_cast<float4*>(o.raw + at) = z;
+        }
+    }
+    __device__ __forceinline__ void zero_node(const NodeOut& o, int n) const {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = lane; i < D * kC32 / 4; i += 32) {
+            reinterpret_cast<float4*>(o.out + (int64_t)n * kNodeFloats)[i] = z;
+            if (o.raw) reinterpret_cast<float4*>(o.raw + (int64_t)n * kNodeFloats)[i] = z;
+        }
+    }
+    __device__ __forceinline__ void store(float* p, const Acc& a) const {
+        const Acc s = reduce(a);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if ((r & 3) == g) *reinterpret_cast<float4*>(p + r * kC32 + 4 * q) = s.v[r];
+    }
+    __device__ __forceinline__ void load(const float* p, Acc& a) const {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            a.v[r] = g == 0 ? *reinterpret_cast<const float4*>(p + r * kC32 + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ __forceinline__ void load_cg(const float* p, Acc& a) const {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            a.v[r] = g == 0 ? __ldcg(reinterpret_cast<const float4*>(p + r * kC32 + 4 * q))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ __forceinline__ static void add_to(Acc& a, const Acc& b) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) a.v[r] = f4_add(a.v[r], b.v[r]);
+    }
+};
+
+// Edges a layout adds per call: 4 for EdgeQuadLayout (add_step), else 1 (add).
+template <class P, class = void>
+struct StepOf { static constexpr int value = 1; };
+template <class P>
+struct StepOf<P, std::void_t<decltype(P::kStep)>> { static constexpr int value = P::kStep; };
+
 // A node whose partials come from at least this many earlier CTAs is
 // combined by all warps of the CTA where it ends.
 constexpr int kSplitPartials = 8;
@@ -433,12 +548,22 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
             int j = 0;
             while (j < jt) {
                 const int stop = imin(b - tb, jt);   // the current node covers position tb + j
-                if (j == 0 && stop == T) {
+                if constexpr (StepOf<P>::value == 1) {
+                    if (j == 0 && stop == T) {
 #pragma unroll
-                    for (int jj = 0; jj < T; ++jj) lay.add(v, jj, acc);
-                } else {
+                        for (int jj = 0; jj < T; ++jj) lay.add(v, jj, acc);
+                    } else {
 #pragma unroll 4
-                    for (int jj = j; jj < stop; ++jj) lay.add(v, jj, acc);
+                        for (int jj = j; jj < stop; ++jj) lay.add(v, jj, acc);
+                    }
+                } else {
+                    constexpr int kS = StepOf<P>::value;
+                    if (j == 0 && stop == T) {
+#pragma unroll
+                        for (int jj = 0; jj < T; jj += kS) lay.add_step(v, jj, T, acc);
+                    } else {
+                        for (int jj = j; jj < stop; jj += kS) lay.add_step(v, jj, stop, acc);
+                    }
                 }
                 j = stop;
                 if (tb + j == b) {                   // node n ends inside this window
@@ -866,7 +991,7 @@ constexpr int kQuadWarpsSmall = 10;
 
 static int tma_warps_for(int lmax, int64_t E) {
     switch (lmax) {
-        case 1: return tma_warps<ChanLayout<1>>();
+        case 1: return tma_warps<EdgeQuadLayout<1>>();
         case 2: return tma_warps<ChanLayout<2>>();
         case 3: {
             constexpr int W = tma_warps<QuadLayout>();
@@ -879,7 +1004,7 @@ static int tma_warps_for(int lmax, int64_t E) {
 
 static int tma_min_window_for(int lmax, int W) {
     switch (lmax) {
-        case 1: return tma_min_window<ChanLayout<1>>(W);
+        case 1: return tma_min_window<EdgeQuadLayout<1>>(W);
         case 2: return tma_min_window<ChanLayout<2>>(W);
         case 3: return tma_min_window<QuadLayout>(W);
         case 4: return tma_min_window<ChanLayout<4>>(W);
@@ -962,7 +1087,7 @@ static void launch_forward(const FwdPlan& p, const float* coup, int cld, const f
                            const Scratch& sc, cudaStream_t s) {
     if (p.fast) {
         switch (lmax) {
-            case 1: launch_tma<ChanLayout<1>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
+            case 1: launch_tma<EdgeQuadLayout<1>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
             case 2: launch_tma<ChanLayout<2>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
             case 3: launch_tma<QuadLayout>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
             case 4: launch_tma<ChanLayout<4>>(p, coup, cld, rad, row_ptr, perm, E, N, o, sc, s); break;
