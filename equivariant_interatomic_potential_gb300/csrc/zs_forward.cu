@@ -349,6 +349,10 @@ template <int LM>
 struct EdgeQuadLayout {
     static constexpr int kStep = 4;
     static constexpr int kTileEdges = 16;
+    // lmax 2 would hold 8 float4 accumulators twice: 165 registers at 12
+    // warps, and no faster than ChanLayout<2> (43.7 against 43.5 us), which
+    // it keeps; this layout serves lmax 1
+    static constexpr int kMaxWarps = LM >= 2 ? 12 : 16;
     static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
     static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
     static constexpr int kSlot = coup_slot_floats(kCoupRow);
