@@ -349,6 +349,10 @@ template <int LM>
 struct EdgeQuadLayout {
     static constexpr int kStep = 4;
     static constexpr int kTileEdges = 16;
+#ifndef ZS_FWD_RADPIECES1
+#define ZS_FWD_RADPIECES1 1
+#endif
+    static constexpr bool kRadPieces = LM == 1 && ZS_FWD_RADPIECES1;   // 128-byte rows as 16-byte pieces
     // lmax 2 would hold 8 float4 accumulators twice: 165 registers at 12
     // warps, and no faster than ChanLayout<2> (43.7 against 43.5 us), which
     // it keeps; this layout serves lmax 1
@@ -449,6 +453,12 @@ struct EdgeQuadLayout {
     }
 };
 
+// Whether a layout's ring copies the radial rows as 16-byte pieces.
+template <class P, class = void>
+struct RadPiecesOf { static constexpr bool value = false; };
+template <class P>
+struct RadPiecesOf<P, std::void_t<decltype(P::kRadPieces)>> { static constexpr bool value = P::kRadPieces; };
+
 // Edges a layout adds per call: 4 for EdgeQuadLayout (add_step), else 1 (add).
 template <class P, class = void>
 struct StepOf { static constexpr int value = 1; };
@@ -469,7 +479,7 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
         int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
         uint64_t* __restrict__ flags, uint64_t salt) {
-    using Ring = TileRing<S, T, kFwdRadPol, P::kRadFloats, P::kCoupRow, kFwdCoupPol>;
+    using Ring = TileRing<S, T, kFwdRadPol, P::kRadFloats, P::kCoupRow, kFwdCoupPol, RadPiecesOf<P>::value>;
     using Layout = typename Ring::Layout;
     using Acc = typename P::Acc;
     static_assert(2 * P::kPartFloats * 4 <= Layout::kRad + Layout::kCoup, "two partials fit a warp's idle ring");

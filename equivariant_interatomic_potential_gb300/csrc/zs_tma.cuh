@@ -109,10 +109,16 @@ struct RingLayout {
 // coupling spans (kL2EvictFirst for bytes read exactly once; a coupling span
 // shares its 32-byte sectors with the neighbouring edges' rows, which a
 // gather in CSR order reads later).
-template <int S, int T, int kPol = kL2Normal, int RadFloats = 96, int CoupRow = 15, int kCoupPol = kPol>
+// kRadPieces: the radial rows travel as 16-byte cp.async pieces, 32 / (row
+// pieces) rows per warp instruction, instead of one bulk copy per row
+// (measured faster for the 128-byte rows of lmax 1 only).
+template <int S, int T, int kPol = kL2Normal, int RadFloats = 96, int CoupRow = 15, int kCoupPol = kPol,
+          bool kRadPieces = false>
 struct TileRing {
     static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
     static_assert(RadFloats % 4 == 0, "radial rows are whole 16-byte pieces");
+    static_assert(!kRadPieces || (32 % (RadFloats / 4) == 0 && T % (32 / (RadFloats / 4)) == 0),
+                  "a warp instruction copies whole rows of whole steps");
     using Layout = RingLayout<S, T, RadFloats, CoupRow>;
     static constexpr int kSlot = coup_slot_floats(CoupRow);
     static constexpr int kChunks = coup_max_chunks(CoupRow);
@@ -144,7 +150,7 @@ struct TileRing {
         consumed = 0;
         pol = l2_policy(kPol);
         pol_c = l2_policy(kCoupPol);
-        if (lane < S) mbar_init(bar0 + 8 * lane, kRingArrivals);
+        if (lane < S) mbar_init(bar0 + 8 * lane, kRadPieces ? 33u : kRingArrivals);
         mbar_fence_init();
         __syncwarp();
     }
@@ -216,10 +222,21 @@ struct TileRing {
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         const uint32_t cbytes = kCoupBulk ? __reduce_add_sync(0xffffffffu, (valid && !tail) ? 16u * nch : 0u) : 0u;
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, nvalid * kRadBytes + cbytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar, (kRadPieces ? 0u : nvalid * kRadBytes) + cbytes);
         __syncwarp();
+        if constexpr (kRadPieces) {
+            constexpr int kPieces = RadFloats / 4, kRows = 32 / kPieces;
+#pragma unroll
+            for (int j0 = 0; j0 < T; j0 += kRows) {
+                const int j = j0 + lane / kPieces, piece = lane % kPieces;
+                const int ej = __shfl_sync(0xffffffffu, e, j);
+                if ((uint32_t)ej < (uint32_t)E)
+                    cp_async16(smem_u32(rad + (st * T + j) * RadFloats) + 16 * piece,
+                               rad_g + (int64_t)ej * RadFloats + 4 * piece, pol);
+            }
+        }
         if (valid) {
-            bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * RadFloats, kRadBytes, bar, pol);
+            if constexpr (!kRadPieces) bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * RadFloats, kRadBytes, bar, pol);
             if (!tail) {
                 const char* src = reinterpret_cast<const char*>(coup_g) - mis + cstart;
                 const uint32_t dst = smem_u32(cslot);
@@ -232,7 +249,7 @@ struct TileRing {
                 }
             }
         }
-        if constexpr (!kCoupBulk) cp_async_arrive(bar);
+        if constexpr (!kCoupBulk || kRadPieces) cp_async_arrive(bar);
     }
 
     // Wait for the next tile in order; returns its stage.
