@@ -227,6 +227,10 @@ struct ChanLayout {
     // slower); 8 for lmax 4 and 5, whose rings then fit more warps (lmax 4:
     // 16 warps of 8-edge tiles 77 us against 11 of 16-edge tiles 84 us)
     static constexpr int kTileEdges = LM <= 3 ? 16 : 8;
+    // lmax 2's 256-byte rows as 16-byte pieces, two rows per warp instruction
+    // (43.7 -> 42.1 us; lmax 4's 512-byte rows gained nothing, lmax 3 and 5
+    // lost with them)
+    static constexpr bool kRadPieces = LM == 2;
     static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
     static constexpr int kRadFloats = LM * kC32, kCoupRow = R, kPartFloats = R * kC32, kNodeFloats = D * kC32;
     static constexpr int kSlot = coup_slot_floats(kCoupRow);
@@ -349,10 +353,9 @@ template <int LM>
 struct EdgeQuadLayout {
     static constexpr int kStep = 4;
     static constexpr int kTileEdges = 16;
-#ifndef ZS_FWD_RADPIECES1
-#define ZS_FWD_RADPIECES1 1
-#endif
-    static constexpr bool kRadPieces = LM == 1 && ZS_FWD_RADPIECES1;   // 128-byte rows as 16-byte pieces
+    // the 128-byte rows of lmax 1 as 16-byte pieces, four rows per warp
+    // instruction (30.8 -> 24.4 us against one bulk copy per row)
+    static constexpr bool kRadPieces = LM == 1;
     // lmax 2 would hold 8 float4 accumulators twice: 165 registers at 12
     // warps, and no faster than ChanLayout<2> (43.7 against 43.5 us), which
     // it keeps; this layout serves lmax 1
