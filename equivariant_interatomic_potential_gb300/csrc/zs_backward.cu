@@ -379,6 +379,7 @@ struct EdgeRing {
     // An edge's cotangent rows as 16-byte cp.async pieces by the whole warp
     // when they are at most 32 pieces (lmax 1: 45.1 -> 42.4 us), else one
     // bulk copy per edge.
+    // (as pieces, lmax 2's 64 were no faster and lmax 3's 120 much slower)
     static constexpr bool kGPieces = Ladder<LM>::R * kC32 / 4 <= 32;
     using Layout = EdgeRingLayout<S, T, LM>;
     static constexpr int R = Ladder<LM>::R, D = Ladder<LM>::D;
@@ -469,9 +470,11 @@ struct EdgeRing {
             for (int j = 0; j < T; ++j) {
                 const int dj = __shfl_sync(0xffffffffu, d, j);
                 const bool fj = __shfl_sync(0xffffffffu, fetch, j);
-                if (fj && lane < kPieces)
-                    cp_async16(smem_u32(gs + (st * T + j) * (R * kC32)) + 16 * lane,
-                               g_g + (int64_t)dj * (D * kC32) + kC32 + 4 * lane, pol_g);
+#pragma unroll
+                for (int q = lane; q < kPieces; q += 32)
+                    if (fj)
+                        cp_async16(smem_u32(gs + (st * T + j) * (R * kC32)) + 16 * q,
+                                   g_g + (int64_t)dj * (D * kC32) + kC32 + 4 * q, pol_g);
             }
             cp_async_arrive(bar);
         } else if (fetch) {
