@@ -34,13 +34,18 @@ def _run(w, s):
                                                  pdc=pdc, pdr=pdr).items()}
 
 
-@pytest.mark.parametrize("case", ["c32", "c40", "lmax2", "hot", "n4096"])
+@pytest.mark.parametrize("case", ["c32", "c40", "lmax2", "hot", "n4096", "lmax1c32", "lmax2c32", "lmax5c32"])
 def test_scaled_matches_oracle(case):
     if case == "n4096":
         w = workloads.make_workload("n4096")
     else:
+        # the C = 32 ladders take their own lane layouts (edge quads at lmax 1,
+        # lane = channel with piece-copied rows at lmax 2, wide couplings at 5);
+        # a hot node makes partials cross many CTAs
         N, E, C, lmax, hot = {"c32": (500, 40000, 32, 3, None), "c40": (200, 9000, 40, 3, None),
-                              "lmax2": (150, 7000, 16, 2, None), "hot": (80, 150000, 32, 3, 9)}[case]
+                              "lmax2": (150, 7000, 16, 2, None), "hot": (80, 150000, 32, 3, 9),
+                              "lmax1c32": (300, 30000, 32, 1, 7), "lmax2c32": (300, 30000, 32, 2, 7),
+                              "lmax5c32": (300, 30000, 32, 5, 7)}[case]
         w = workloads.make_random(N, E, C, seed=E + C, lmax=lmax, hot_node=hot, hot_fraction=0.6 if hot else 0.0)
     s = _factor(w, len(case))
     r = _run(w, s)
