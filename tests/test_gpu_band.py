@@ -28,7 +28,8 @@ def _band(w, seg_offset, seed):
     return band, seg_offset + 1, D
 
 
-@pytest.mark.parametrize("lmax,C,seg", [(3, 32, 0), (3, 32, 15), (3, 40, 15), (2, 32, 8), (5, 16, 0)])
+@pytest.mark.parametrize("lmax,C,seg", [(3, 32, 0), (3, 32, 15), (3, 40, 15), (2, 32, 8), (5, 16, 0), (1, 32, 3),
+                                        (5, 32, 35)])
 def test_band_matches_contiguous_and_oracle(lmax, C, seg):
     w = workloads.make_random(400, 50000, C, seed=lmax * 100 + seg, lmax=lmax, hot_node=2, hot_fraction=0.3)
     band_h, first, D = _band(w, seg, seg + 7)
