@@ -267,6 +267,10 @@ struct ChanLayout {
     // queue had been the limit; lmax 2 unchanged and lmax 1 slower (3 rows do
     // not pay for the switch), so those keep one broadcast LDS.32 per row.
     static constexpr bool kVecCoup = R >= 16;
+    // and their ring lands each coupling row at the start of its slot (4-byte
+    // copies), so the row offset is 0 and no switch is needed: lmax 4 76.6 ->
+    // 73.4 us, lmax 5 110.8 -> 106.6 us
+    static constexpr bool kCoupAligned = kVecCoup;
     // lmax 5 holds 35 accumulators, the node's first piece and the 40-float
     // coupling span: 163 registers, so 12 warps (at 16 the 128-register cap
     // spills)
@@ -291,11 +295,15 @@ struct ChanLayout {
                 cf[4 * k + 2] = q.z;
                 cf[4 * k + 3] = q.w;
             }
-            switch (v.mt[j].y) {
-                case 0: fma_rows<0>(cf, rv, a); break;
-                case 1: fma_rows<1>(cf, rv, a); break;
-                case 2: fma_rows<2>(cf, rv, a); break;
-                default: fma_rows<3>(cf, rv, a); break;
+            if constexpr (kCoupAligned) {
+                fma_rows<0>(cf, rv, a);
+            } else {
+                switch (v.mt[j].y) {
+                    case 0: fma_rows<0>(cf, rv, a); break;
+                    case 1: fma_rows<1>(cf, rv, a); break;
+                    case 2: fma_rows<2>(cf, rv, a); break;
+                    default: fma_rows<3>(cf, rv, a); break;
+                }
             }
         } else {
             const float* cr = v.cp + j * kSlot + v.mt[j].y;
@@ -456,6 +464,12 @@ struct EdgeQuadLayout {
     }
 };
 
+// Whether a layout's ring puts each coupling row at the start of its slot.
+template <class P, class = void>
+struct CoupAlignedOf { static constexpr bool value = false; };
+template <class P>
+struct CoupAlignedOf<P, std::void_t<decltype(P::kCoupAligned)>> { static constexpr bool value = P::kCoupAligned; };
+
 // Whether a layout's ring copies the radial rows as 16-byte pieces.
 template <class P, class = void>
 struct RadPiecesOf { static constexpr bool value = false; };
@@ -482,7 +496,8 @@ fwd_tma(const float* __restrict__ coup, int cld, const float* __restrict__ rad,
         const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
         int E, int32_t N, int KW, int Wtot, NodeOut o, float* __restrict__ cta_part,
         uint64_t* __restrict__ flags, uint64_t salt) {
-    using Ring = TileRing<S, T, kFwdRadPol, P::kRadFloats, P::kCoupRow, kFwdCoupPol, RadPiecesOf<P>::value>;
+    using Ring = TileRing<S, T, kFwdRadPol, P::kRadFloats, P::kCoupRow, kFwdCoupPol, RadPiecesOf<P>::value,
+                          CoupAlignedOf<P>::value>;
     using Layout = typename Ring::Layout;
     using Acc = typename P::Acc;
     static_assert(2 * P::kPartFloats * 4 <= Layout::kRad + Layout::kCoup, "two partials fit a warp's idle ring");

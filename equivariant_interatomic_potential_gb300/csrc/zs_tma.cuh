@@ -69,6 +69,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" :: "r"(dst), "l"(src), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "l"(pol) : "memory");
 }
@@ -112,8 +116,11 @@ struct RingLayout {
 // kRadPieces: the radial rows travel as 16-byte cp.async pieces, 32 / (row
 // pieces) rows per warp instruction, instead of one bulk copy per row
 // (measured faster for the 128-byte rows of lmax 1 only).
+// kCoupAligned: each coupling row lands at the start of its slot (4-byte
+// cp.async copies by the whole warp, row offset 0) instead of as the
+// 16-byte-aligned span holding it.
 template <int S, int T, int kPol = kL2Normal, int RadFloats = 96, int CoupRow = 15, int kCoupPol = kPol,
-          bool kRadPieces = false>
+          bool kRadPieces = false, bool kCoupAligned = false>
 struct TileRing {
     static_assert(T >= 1 && T <= 32 && 32 % T == 0, "a tile is at most one edge per lane and divides 32");
     static_assert(RadFloats % 4 == 0, "radial rows are whole 16-byte pieces");
@@ -150,7 +157,7 @@ struct TileRing {
         consumed = 0;
         pol = l2_policy(kPol);
         pol_c = l2_policy(kCoupPol);
-        if (lane < S) mbar_init(bar0 + 8 * lane, kRadPieces ? 33u : kRingArrivals);
+        if (lane < S) mbar_init(bar0 + 8 * lane, (kRadPieces || kCoupAligned) ? 33u : kRingArrivals);
         mbar_fence_init();
         __syncwarp();
     }
@@ -192,7 +199,7 @@ struct TileRing {
         int64_t cstart = 0;
         int off = 0, nch = 0;
         bool tail = false;
-        if (valid) {
+        if (valid && !kCoupAligned) {
             const int64_t b0 = mis + (int64_t)e * cld * 4;
             cstart = b0 & ~(int64_t)15;
             off = (int)(b0 - cstart) >> 2;          // 0..3
@@ -235,9 +242,21 @@ struct TileRing {
                                rad_g + (int64_t)ej * RadFloats + 4 * piece, pol);
             }
         }
+        if constexpr (kCoupAligned) {
+            // the T rows, 4 bytes a lane, each from its own first float
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                const int ej = __shfl_sync(0xffffffffu, e, j);
+                if ((uint32_t)ej < (uint32_t)E) {
+                    const uint32_t cdst = smem_u32(coup + (st * T + j) * kSlot);
+#pragma unroll
+                    for (int r = lane; r < CoupRow; r += 32) cp_async4(cdst + 4 * r, coup_g + (int64_t)ej * cld + r, pol_c);
+                }
+            }
+        }
         if (valid) {
             if constexpr (!kRadPieces) bulk_g2s(smem_u32(rslot), rad_g + (int64_t)e * RadFloats, kRadBytes, bar, pol);
-            if (!tail) {
+            if (!kCoupAligned && !tail) {
                 const char* src = reinterpret_cast<const char*>(coup_g) - mis + cstart;
                 const uint32_t dst = smem_u32(cslot);
                 if constexpr (kCoupBulk) {
@@ -249,7 +268,7 @@ struct TileRing {
                 }
             }
         }
-        if constexpr (!kCoupBulk || kRadPieces) cp_async_arrive(bar);
+        if constexpr (!kCoupBulk || kRadPieces || kCoupAligned) cp_async_arrive(bar);
     }
 
     // Wait for the next tile in order; returns its stage.
